@@ -1,0 +1,183 @@
+/*
+ * pa.h — C ABI of the paged KV-cache library (libpa.so, CUDA for sm_103a).
+ *
+ * Three operations make up the decode-step hot path of PagedAttention:
+ *
+ *   pa_decode       attention of one new query per sequence over that
+ *                   sequence's cached keys/values, read through its block
+ *                   table;
+ *   pa_append_kv    store each new token's key/value rows into its slot;
+ *   pa_copy_blocks  copy whole blocks, the copy-on-write step for blocks that
+ *                   several sequences share.
+ *
+ * Sources (web pages on PagedAttention):
+ *   [A] "PagedAttention: From Operating System Virtual Memory to Large
+ *       Language Model Memory Systems", section 2 Background — the attention
+ *       formula softmax(Q K^T / sqrt(d)) V; section 4 Core Innovation —
+ *       logical KV blocks -> block table -> physical GPU blocks.
+ *   [B] "PagedAttention — 把 KV cache 当虚拟内存页来管理", 核心要点 (each
+ *       generated token's key/value is saved and re-read on later steps),
+ *       实践案例 案例 2 (locate: logical block t / block_size through the
+ *       table, offset t % block_size; the attention kernel does this one
+ *       extra lookup), 案例 3 (reference counts, copy-on-write, one block is
+ *       the copy unit), 踩过的坑 (16-token blocks are the default).
+ *   [C] "KV Cache与长上下文管理", section "让 Round Robin / Sliding Window 变成
+ *       O(1) 操作" — a sliding window by recycling pages and rewriting the
+ *       page table, with no K/V movement.
+ *   [D] "PagedAttention 的技术溯源与演进脉络" (mjmagnets article), section 2.2
+ *       — a long sequence is cut into several attention units; here those are
+ *       the context partitions merged by a log-sum-exp reduce.
+ *
+ * Memory and ownership.  Every pointer argument is DEVICE memory owned by the
+ * caller unless stated otherwise; the library allocates nothing, keeps no
+ * per-call state and never synchronises: all work is enqueued on `stream`
+ * (a cudaStream_t; NULL means the legacy default stream).  The functions are
+ * thread-safe.  The only state is a per-device cache of SM count and kernel
+ * occupancy, filled on first use.
+ *
+ * Layouts (row-major, densely packed):
+ *   q, out           [num_seqs][num_heads][head_dim]
+ *   k_cache, v_cache [num_blocks][num_kv_heads][block_size][head_dim]
+ *                    (one (block, kv head) tile is contiguous)
+ *   block_tables     int32 [num_seqs][max_blocks_per_seq]
+ *   context_lens     int32 [num_seqs]
+ *   k, v (append)    [num_tokens][num_kv_heads][head_dim]
+ *   slot_mapping     int64 [num_tokens], slot = physical_block * block_size + offset
+ *   src_dst_pairs    int64 [num_pairs][2]
+ * Query head h reads kv head h / (num_heads / num_kv_heads).
+ *
+ * Errors.  Bad scalar arguments, null pointers, misaligned pointers (q,
+ * caches, k, v must be 16-byte aligned) and a too-small workspace are found
+ * on the host before anything is launched (PA_ERR_*).  Bad array CONTENTS on
+ * the device (a table entry outside [0, num_blocks), a slot or pair outside
+ * the pool) are never dereferenced: the token, row or pair is skipped and a
+ * bit is OR-ed into *err_word (a device uint32, nullable, sticky: the caller
+ * clears and reads it).  No kernel traps or asserts.
+ */
+#ifndef PA_H
+#define PA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define PA_API __attribute__((visibility("default")))
+#else
+#define PA_API
+#endif
+
+typedef struct CUstream_st *pa_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+    PA_OK = 0,
+    PA_ERR_INVALID_ARGUMENT = 1, /* null pointer, negative size, misalignment, bad enum */
+    PA_ERR_UNSUPPORTED = 2,      /* a shape or dtype this build does not implement */
+    PA_ERR_WORKSPACE_TOO_SMALL = 3,
+    PA_ERR_CUDA = 4              /* a CUDA runtime call or launch failed */
+} pa_status;
+
+typedef enum { PA_F32 = 0, PA_F16 = 1, PA_BF16 = 2 } pa_dtype;
+
+/* Bits OR-ed into *err_word by the kernels. */
+#define PA_DEVERR_BAD_BLOCK 0x1u /* decode: table entry outside [0, num_blocks); its tokens were left out */
+#define PA_DEVERR_BAD_SLOT 0x2u  /* append: slot >= num_blocks * block_size; the row was not written */
+#define PA_DEVERR_BAD_PAIR 0x4u  /* copy: src or dst outside [0, num_blocks); the pair was skipped */
+#define PA_DEVERR_TIMEOUT 0x8u   /* a pipeline wait gave up (about 2 s); the output is not valid */
+#define PA_DEVERR_BAD_LEN 0x10u  /* decode: context_lens[s] > max_blocks_per_seq * block_size; clamped to that */
+
+/*
+ * Bytes of scratch pa_decode needs for split-context partials (0 when no
+ * sequence can span more than one partition).  The arguments mean the same as
+ * in pa_decode; partition_size 0 selects the default.  The workspace holds,
+ * per (sequence, query head, partition), the running max, the softmax
+ * denominator and the unnormalised output row in fp32.
+ */
+PA_API size_t pa_decode_workspace_size(int num_seqs, int num_heads, int head_dim, int block_size,
+                                int max_blocks_per_seq, int window, int partition_size);
+
+/*
+ * Paged decode attention [A][B][C][D].
+ *
+ * For each sequence s and query head h, with L = context_lens[s] and the
+ * attended tokens t in [max(0, L - window), L) when window > 0, else [0, L):
+ *   k_t = k_cache[table[s][t / block_size]][h / G][t % block_size][:] (same for v_t)
+ *   x_t = scale * <q[s][h], k_t>
+ *   out[s][h] = sum_t exp(x_t - max x) v_t / sum_t exp(x_t - max x)
+ * out[s][h] is 0 when no token is attended (L == 0).  Only table entries of
+ * attended tokens are read: a sliding window is expressed purely by rewriting
+ * table rows (entries of tokens outside the window may hold anything).
+ *
+ * Arguments (spec order first):
+ *   out           [num_seqs][num_heads][head_dim] of out_dtype (written)
+ *   q             [num_seqs][num_heads][head_dim] of dtype
+ *   k_cache, v_cache  pool of dtype, layout above
+ *   block_tables, context_lens  int32, layout above
+ *   num_heads % num_kv_heads == 0 and num_heads / num_kv_heads in {1, 2, 4, 8}
+ *   head_dim in {64, 128}; block_size in {8, 16, 32}
+ *   scale         usually 1 / sqrt(head_dim)
+ *   window        0 = whole context, > 0 = last `window` tokens
+ *   dtype         element type of q, k_cache and v_cache
+ *   out_dtype     element type of out (fp32 keeps the full accuracy)
+ *   max_blocks_per_seq  row stride of block_tables; every context must fit:
+ *                 context_lens[s] <= max_blocks_per_seq * block_size
+ *   num_blocks    pool size, for the bounds check of table entries
+ *   partition_size  tokens per context partition, a multiple of block_size,
+ *                 at most 256 blocks; 0 = default (512 tokens)
+ *   workspace, workspace_bytes  scratch of at least pa_decode_workspace_size()
+ *                 bytes (may be NULL when that size is 0)
+ *   err_word      device uint32 or NULL
+ * num_seqs == 0 returns PA_OK without launching.
+ */
+PA_API pa_status pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache,
+                    const int32_t *block_tables, const int32_t *context_lens,
+                    int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                    int block_size, float scale, int window,
+                    pa_dtype dtype, pa_dtype out_dtype, int max_blocks_per_seq,
+                    int num_blocks, int partition_size, void *workspace,
+                    size_t workspace_bytes, uint32_t *err_word, pa_stream_t stream);
+
+/*
+ * Append [B 核心要点, 案例 2]: for every token i with slot = slot_mapping[i] >= 0
+ *   k_cache[slot / block_size][h][slot % block_size][:] = k[i][h][:]   (all h)
+ *   v_cache[...] = v[i][h][:]
+ * A bit-exact copy (k, v and the caches share `dtype`).  A negative slot is
+ * padding and is skipped; a slot >= num_blocks * block_size is skipped and
+ * flagged.  Two tokens naming one slot leave that slot holding one of them
+ * (unspecified which): callers must not do this.
+ * num_tokens == 0 returns PA_OK without launching.
+ */
+PA_API pa_status pa_append_kv(const void *k, const void *v, const int64_t *slot_mapping,
+                       void *k_cache, void *v_cache, int num_tokens, int num_kv_heads,
+                       int head_dim, int block_size, int num_blocks, pa_dtype dtype,
+                       uint32_t *err_word, pa_stream_t stream);
+
+/*
+ * Copy-on-write block copy [B 案例 3]: for each pair (src, dst) copy block src
+ * onto block dst in both caches (all kv heads, all rows).  A pair naming a
+ * block outside the pool is skipped and flagged.  A destination that repeats
+ * or that is also a source makes the result order-dependent: callers must not
+ * do this.  num_pairs == 0 returns PA_OK without launching.
+ */
+PA_API pa_status pa_copy_blocks(const int64_t *src_dst_pairs, int num_pairs, void *k_cache,
+                         void *v_cache, int num_kv_heads, int head_dim, int block_size,
+                         int num_blocks, pa_dtype dtype, uint32_t *err_word,
+                         pa_stream_t stream);
+
+/* Static text for a status code. */
+PA_API const char *pa_status_string(pa_status status);
+
+/* Detail of the last PA_ERR_* returned on the calling thread ("" if none). */
+PA_API const char *pa_last_error_detail(void);
+
+/* Library version, (major << 16) | (minor << 8) | patch. */
+PA_API int pa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H */

@@ -1,0 +1,330 @@
+// C-ABI entry points of libpa: argument checks, launch planning, launches.
+// The operations and their sources are documented in include/pa.h.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <map>
+#include <mutex>
+#include <string>
+#include <tuple>
+
+#include "pa.h"
+#include "pa_decode.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+
+const void *reduce_kernel(int head_dim) {
+    if (head_dim == 64)
+        return reinterpret_cast<const void *>(&pa_reduce_kernel<64>);
+    if (head_dim == 128)
+        return reinterpret_cast<const void *>(&pa_reduce_kernel<128>);
+    return nullptr;
+}
+
+namespace {
+
+thread_local std::string g_detail;
+
+pa_status fail(pa_status st, const std::string &why) {
+    g_detail = why;
+    return st;
+}
+
+pa_status cuda_fail(cudaError_t e, const char *what) {
+    g_detail = std::string(what) + ": " + cudaGetErrorName(e) + " (" + cudaGetErrorString(e) + ")";
+    return PA_ERR_CUDA;
+}
+
+int elt_bytes(int dtype) { return dtype == PA_F32 ? 4 : 2; }
+bool dtype_ok(int dtype) { return dtype == PA_F32 || dtype == PA_F16 || dtype == PA_BF16; }
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool block_size_ok(int bs) { return bs == 8 || bs == 16 || bs == 32; }
+bool head_dim_ok(int d) { return d == 64 || d == 128; }
+
+// Per-device facts and per-kernel launch settings, filled on first use.
+std::mutex g_mu;
+std::map<int, int> g_sms;
+std::map<std::pair<int, const void *>, size_t> g_smem_set;
+std::map<std::tuple<int, const void *, size_t>, int> g_occ;
+
+cudaError_t device_sms(int *dev, int *sms) {
+    cudaError_t e = cudaGetDevice(dev);
+    if (e != cudaSuccess)
+        return e;
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto it = g_sms.find(*dev);
+    if (it != g_sms.end()) {
+        *sms = it->second;
+        return cudaSuccess;
+    }
+    e = cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, *dev);
+    if (e == cudaSuccess)
+        g_sms[*dev] = *sms;
+    return e;
+}
+
+cudaError_t prepare_kernel(int dev, const void *fn, size_t smem, int threads, int *blocks_per_sm) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto key = std::make_pair(dev, fn);
+    auto it = g_smem_set.find(key);
+    if (it == g_smem_set.end() || it->second < smem) {
+        cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+        if (e != cudaSuccess)
+            return e;
+        g_smem_set[key] = smem;
+    }
+    auto okey = std::make_tuple(dev, fn, smem);
+    auto oit = g_occ.find(okey);
+    if (oit != g_occ.end()) {
+        *blocks_per_sm = oit->second;
+        return cudaSuccess;
+    }
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, fn, threads, smem);
+    if (e != cudaSuccess)
+        return e;
+    g_occ[okey] = *blocks_per_sm;
+    return cudaSuccess;
+}
+
+constexpr int kDefaultPartition = 512;
+constexpr int kStageBudget = 48 * 1024;
+
+struct DecodePlan {
+    int bpp = 0;
+    int max_parts = 0;
+    size_t workspace = 0;
+};
+
+pa_status plan_decode(int num_seqs, int num_heads, int head_dim, int block_size, int max_blocks_per_seq,
+                      int window, int partition_size, DecodePlan *plan) {
+    if (num_seqs < 0 || num_heads <= 0 || max_blocks_per_seq <= 0 || window < 0)
+        return fail(PA_ERR_INVALID_ARGUMENT, "num_seqs, num_heads, max_blocks_per_seq or window out of range");
+    if (!block_size_ok(block_size))
+        return fail(PA_ERR_UNSUPPORTED, "block_size must be 8, 16 or 32");
+    if (!head_dim_ok(head_dim))
+        return fail(PA_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
+    int P = partition_size == 0 ? kDefaultPartition : partition_size;
+    if (P <= 0 || P % block_size != 0 || P / block_size > kMaxBpp)
+        return fail(PA_ERR_INVALID_ARGUMENT, "partition_size must be a positive multiple of block_size, at most 256 blocks");
+    plan->bpp = P / block_size;
+    long long span_blocks = max_blocks_per_seq;
+    if (window > 0) {
+        const long long wb = (static_cast<long long>(window) + block_size - 1) / block_size + 1;
+        if (wb < span_blocks)
+            span_blocks = wb;
+    }
+    plan->max_parts = static_cast<int>((span_blocks + plan->bpp - 1) / plan->bpp);
+    if (plan->max_parts > 1)
+        plan->workspace = static_cast<size_t>(num_seqs) * num_heads * plan->max_parts * (head_dim + 2) * sizeof(float);
+    else
+        plan->workspace = 0;
+    return PA_OK;
+}
+
+}  // namespace
+}  // namespace pa
+
+using namespace pa;
+
+extern "C" {
+
+size_t pa_decode_workspace_size(int num_seqs, int num_heads, int head_dim, int block_size, int max_blocks_per_seq,
+                                int window, int partition_size) {
+    DecodePlan plan;
+    if (plan_decode(num_seqs, num_heads, head_dim, block_size, max_blocks_per_seq, window, partition_size, &plan) !=
+        PA_OK)
+        return 0;
+    return plan.workspace;
+}
+
+pa_status pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache, const int32_t *block_tables,
+                    const int32_t *context_lens, int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                    int block_size, float scale, int window, pa_dtype dtype, pa_dtype out_dtype,
+                    int max_blocks_per_seq, int num_blocks, int partition_size, void *workspace,
+                    size_t workspace_bytes, uint32_t *err_word, pa_stream_t stream) {
+    g_detail.clear();
+    DecodePlan plan;
+    pa_status st = plan_decode(num_seqs, num_heads, head_dim, block_size, max_blocks_per_seq, window,
+                               partition_size, &plan);
+    if (st != PA_OK)
+        return st;
+    if (num_seqs == 0)
+        return PA_OK;
+    if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens)
+        return fail(PA_ERR_INVALID_ARGUMENT, "null pointer");
+    if (num_kv_heads <= 0 || num_heads % num_kv_heads != 0)
+        return fail(PA_ERR_INVALID_ARGUMENT, "num_heads must be a multiple of num_kv_heads");
+    const int G = num_heads / num_kv_heads;
+    if (G != 1 && G != 2 && G != 4 && G != 8)
+        return fail(PA_ERR_UNSUPPORTED, "num_heads / num_kv_heads must be 1, 2, 4 or 8");
+    if (!dtype_ok(dtype) || !dtype_ok(out_dtype))
+        return fail(PA_ERR_INVALID_ARGUMENT, "unknown dtype");
+    if (num_blocks <= 0)
+        return fail(PA_ERR_INVALID_ARGUMENT, "num_blocks must be positive");
+    if (!std::isfinite(scale))
+        return fail(PA_ERR_INVALID_ARGUMENT, "scale must be finite");
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
+        return fail(PA_ERR_INVALID_ARGUMENT, "q, k_cache and v_cache must be 16-byte aligned");
+    if ((reinterpret_cast<uintptr_t>(out) & (elt_bytes(out_dtype) - 1)) != 0)
+        return fail(PA_ERR_INVALID_ARGUMENT, "out is not aligned to its element size");
+    if (plan.workspace > 0 && (workspace == nullptr || workspace_bytes < plan.workspace))
+        return fail(PA_ERR_WORKSPACE_TOO_SMALL, "workspace smaller than pa_decode_workspace_size()");
+    if (plan.workspace > 0 && !aligned16(workspace))
+        return fail(PA_ERR_INVALID_ARGUMENT, "workspace must be 16-byte aligned");
+
+    const void *fn = dtype == PA_F32   ? decode_kernel_f32(head_dim, G)
+                     : dtype == PA_F16 ? decode_kernel_f16(head_dim, G)
+                                       : decode_kernel_bf16(head_dim, G);
+    if (!fn)
+        return fail(PA_ERR_UNSUPPORTED, "no decode kernel for this dtype / head_dim / group");
+
+    const int row = head_dim * elt_bytes(dtype);
+    const int tile = block_size * row;
+    int S = kStageBudget / (2 * tile);
+    S = S < 2 ? 2 : (S > 8 ? 8 : S);
+    const size_t smem = decode_smem_layout(S, tile, row, G, head_dim).total;
+
+    int dev = 0, sms = 0, per_sm = 0;
+    cudaError_t e = device_sms(&dev, &sms);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "device query");
+    e = prepare_kernel(dev, fn, smem, kDecodeThreads, &per_sm);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "decode kernel set-up");
+    if (per_sm < 1)
+        return fail(PA_ERR_UNSUPPORTED, "decode kernel does not fit on an SM");
+
+    DecodeParams p;
+    p.out = out;
+    p.q = q;
+    p.k_cache = k_cache;
+    p.v_cache = v_cache;
+    p.block_tables = block_tables;
+    p.context_lens = context_lens;
+    const size_t acc_floats = static_cast<size_t>(num_seqs) * num_heads * plan.max_parts * head_dim;
+    p.part_acc = plan.workspace ? static_cast<float *>(workspace) : nullptr;
+    p.part_ml = plan.workspace ? static_cast<float *>(workspace) + acc_floats : nullptr;
+    p.err = err_word;
+    p.num_seqs = num_seqs;
+    p.num_heads = num_heads;
+    p.num_kv_heads = num_kv_heads;
+    p.block_size = block_size;
+    p.window = window;
+    p.max_blocks_per_seq = max_blocks_per_seq;
+    p.max_len = static_cast<int>(std::min<long long>(static_cast<long long>(max_blocks_per_seq) * block_size, 0x7fffffffLL));
+    p.num_blocks = num_blocks;
+    p.bpp = plan.bpp;
+    p.max_parts = plan.max_parts;
+    p.out_dtype = out_dtype;
+    p.stages = S;
+    p.scale_log2 = scale * 1.4426950408889634f;
+
+    const long long items_max = static_cast<long long>(num_seqs) * num_kv_heads * plan.max_parts;
+    long long grid = static_cast<long long>(sms) * per_sm;
+    if (grid > items_max)
+        grid = items_max;
+    if (grid < 1)
+        grid = 1;
+    void *args[] = {&p};
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    e = cudaLaunchKernel(fn, dim3(static_cast<unsigned>(grid)), dim3(kDecodeThreads), args, smem, cs);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "decode launch");
+    if (plan.max_parts > 1) {
+        const long long rows = static_cast<long long>(num_seqs) * num_heads;
+        e = cudaLaunchKernel(reduce_kernel(head_dim), dim3(static_cast<unsigned>((rows + 3) / 4)), dim3(128), args, 0,
+                             cs);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "reduce launch");
+    }
+    return PA_OK;
+}
+
+pa_status pa_append_kv(const void *k, const void *v, const int64_t *slot_mapping, void *k_cache, void *v_cache,
+                       int num_tokens, int num_kv_heads, int head_dim, int block_size, int num_blocks, pa_dtype dtype,
+                       uint32_t *err_word, pa_stream_t stream) {
+    g_detail.clear();
+    if (num_tokens < 0 || num_kv_heads <= 0 || num_blocks <= 0)
+        return fail(PA_ERR_INVALID_ARGUMENT, "num_tokens, num_kv_heads or num_blocks out of range");
+    if (!block_size_ok(block_size))
+        return fail(PA_ERR_UNSUPPORTED, "block_size must be 8, 16 or 32");
+    if (!head_dim_ok(head_dim))
+        return fail(PA_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
+    if (!dtype_ok(dtype))
+        return fail(PA_ERR_INVALID_ARGUMENT, "unknown dtype");
+    if (num_tokens == 0)
+        return PA_OK;
+    if (!k || !v || !slot_mapping || !k_cache || !v_cache)
+        return fail(PA_ERR_INVALID_ARGUMENT, "null pointer");
+    if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache))
+        return fail(PA_ERR_INVALID_ARGUMENT, "k, v and the caches must be 16-byte aligned");
+    if ((reinterpret_cast<uintptr_t>(slot_mapping) & 7u) != 0)
+        return fail(PA_ERR_INVALID_ARGUMENT, "slot_mapping must be 8-byte aligned");
+    int dev = 0, sms = 0;
+    cudaError_t e = device_sms(&dev, &sms);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "device query");
+    e = launch_append(k, v, slot_mapping, k_cache, v_cache, num_tokens, num_kv_heads, head_dim * elt_bytes(dtype),
+                      block_size, num_blocks, err_word, sms, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+        return cuda_fail(e, "append launch");
+    return PA_OK;
+}
+
+pa_status pa_copy_blocks(const int64_t *src_dst_pairs, int num_pairs, void *k_cache, void *v_cache, int num_kv_heads,
+                         int head_dim, int block_size, int num_blocks, pa_dtype dtype, uint32_t *err_word,
+                         pa_stream_t stream) {
+    g_detail.clear();
+    if (num_pairs < 0 || num_kv_heads <= 0 || num_blocks <= 0)
+        return fail(PA_ERR_INVALID_ARGUMENT, "num_pairs, num_kv_heads or num_blocks out of range");
+    if (!block_size_ok(block_size))
+        return fail(PA_ERR_UNSUPPORTED, "block_size must be 8, 16 or 32");
+    if (!head_dim_ok(head_dim))
+        return fail(PA_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
+    if (!dtype_ok(dtype))
+        return fail(PA_ERR_INVALID_ARGUMENT, "unknown dtype");
+    if (num_pairs == 0)
+        return PA_OK;
+    if (!src_dst_pairs || !k_cache || !v_cache)
+        return fail(PA_ERR_INVALID_ARGUMENT, "null pointer");
+    if (!aligned16(k_cache) || !aligned16(v_cache))
+        return fail(PA_ERR_INVALID_ARGUMENT, "the caches must be 16-byte aligned");
+    if ((reinterpret_cast<uintptr_t>(src_dst_pairs) & 7u) != 0)
+        return fail(PA_ERR_INVALID_ARGUMENT, "src_dst_pairs must be 8-byte aligned");
+    int dev = 0, sms = 0;
+    cudaError_t e = device_sms(&dev, &sms);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "device query");
+    const long long block_bytes =
+        static_cast<long long>(num_kv_heads) * block_size * head_dim * elt_bytes(dtype);
+    e = launch_copy_blocks(src_dst_pairs, num_pairs, k_cache, v_cache, block_bytes, num_blocks, err_word, sms,
+                           reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+        return cuda_fail(e, "copy_blocks launch");
+    return PA_OK;
+}
+
+const char *pa_status_string(pa_status status) {
+    switch (status) {
+    case PA_OK:
+        return "PA_OK";
+    case PA_ERR_INVALID_ARGUMENT:
+        return "PA_ERR_INVALID_ARGUMENT";
+    case PA_ERR_UNSUPPORTED:
+        return "PA_ERR_UNSUPPORTED";
+    case PA_ERR_WORKSPACE_TOO_SMALL:
+        return "PA_ERR_WORKSPACE_TOO_SMALL";
+    case PA_ERR_CUDA:
+        return "PA_ERR_CUDA";
+    }
+    return "PA_ERR_UNKNOWN";
+}
+
+const char *pa_last_error_detail(void) { return g_detail.c_str(); }
+
+int pa_version(void) { return (0 << 16) | (1 << 8) | 0; }
+
+}  // extern "C"

@@ -1,0 +1,141 @@
+// KV append and copy-on-write block copy.
+//
+// Append ("PagedAttention — 把 KV cache 当虚拟内存页来管理", 核心要点: every
+// generated token's key/value is saved; 案例 2: slot = physical block *
+// block_size + offset): token i's rows go to
+//   cache[slot / block_size][h][slot % block_size][:].
+// Block copy (same page, 案例 3: copy-on-write, one whole block is the copy
+// unit): for each (src, dst) pair the block's tiles of every kv head, K and V.
+// Both are bit-exact 16-byte vector copies; bad slots / pairs are skipped and
+// flagged in the error word.
+#include <cuda_runtime.h>
+
+#include "pa_device.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+
+namespace {
+
+__device__ inline uint4 ld_stream(const uint4 *p) {
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+// One thread moves one 16-byte chunk of a K row and the matching V chunk.
+// Work index order: token, kv head, chunk -> reads of k / v are contiguous
+// and each (token, head) row is written as one contiguous run.
+__global__ void __launch_bounds__(256) append_kernel(const uint4 *__restrict__ k, const uint4 *__restrict__ v,
+                                                     const int64_t *__restrict__ slots, uint4 *k_cache,
+                                                     uint4 *v_cache, long long num_tokens, int num_kv_heads,
+                                                     int chunks_per_row, int block_size, long long pool_slots,
+                                                     uint32_t *err) {
+    const long long per_token = static_cast<long long>(num_kv_heads) * chunks_per_row;
+    const long long total = num_tokens * per_token;
+    for (long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; idx < total;
+         idx += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const long long i = idx / per_token;
+        const long long rem = idx - i * per_token;
+        const int h = static_cast<int>(rem / chunks_per_row);
+        const int c = static_cast<int>(rem - static_cast<long long>(h) * chunks_per_row);
+        const long long slot = slots[i];
+        if (slot < 0)
+            continue;  // padding
+        if (slot >= pool_slots) {
+            if (err && rem == 0)
+                atomicOr(err, PA_DEVERR_BAD_SLOT);
+            continue;
+        }
+        const long long phys = slot / block_size;
+        const long long off = slot - phys * block_size;
+        const long long dst = ((phys * num_kv_heads + h) * block_size + off) * chunks_per_row + c;
+        const uint4 kr = ld_stream(k + idx);
+        const uint4 vr = ld_stream(v + idx);
+        k_cache[dst] = kr;
+        v_cache[dst] = vr;
+    }
+}
+
+constexpr int kCopyUnroll = 4;
+
+// grid.x: chunks of the block, grid.y: pairs (strided), grid.z: 0 = K, 1 = V.
+__global__ void __launch_bounds__(256) copy_blocks_kernel(const int64_t *__restrict__ pairs, int num_pairs,
+                                                          uint4 *k_cache, uint4 *v_cache,
+                                                          long long chunks_per_block, long long num_blocks,
+                                                          uint32_t *err) {
+    uint4 *cache = blockIdx.z == 0 ? k_cache : v_cache;
+    for (int pi = blockIdx.y; pi < num_pairs; pi += gridDim.y) {
+        const long long src = pairs[2 * pi], dst = pairs[2 * pi + 1];
+        if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
+            if (err && blockIdx.x == 0 && threadIdx.x == 0)
+                atomicOr(err, PA_DEVERR_BAD_PAIR);
+            continue;
+        }
+        const uint4 *s = cache + src * chunks_per_block;
+        uint4 *d = cache + dst * chunks_per_block;
+        const long long step = static_cast<long long>(gridDim.x) * blockDim.x * kCopyUnroll;
+        for (long long base = static_cast<long long>(blockIdx.x) * blockDim.x * kCopyUnroll + threadIdx.x;
+             base < chunks_per_block; base += step) {
+            uint4 r[kCopyUnroll];
+#pragma unroll
+            for (int u = 0; u < kCopyUnroll; ++u) {
+                const long long c = base + static_cast<long long>(u) * blockDim.x;
+                if (c < chunks_per_block)
+                    r[u] = ld_stream(s + c);
+            }
+#pragma unroll
+            for (int u = 0; u < kCopyUnroll; ++u) {
+                const long long c = base + static_cast<long long>(u) * blockDim.x;
+                if (c < chunks_per_block)
+                    d[c] = r[u];
+            }
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_append(const void *k, const void *v, const int64_t *slots, void *k_cache, void *v_cache,
+                          int num_tokens, int num_kv_heads, int row_bytes, int block_size, int num_blocks,
+                          uint32_t *err, int num_sms, cudaStream_t stream) {
+    const int cpr = row_bytes / 16;
+    const long long total = static_cast<long long>(num_tokens) * num_kv_heads * cpr;
+    long long blocks = (total + 255) / 256;
+    const long long cap = static_cast<long long>(num_sms) * 8;
+    if (blocks > cap)
+        blocks = cap;
+    if (blocks < 1)
+        blocks = 1;
+    append_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+        static_cast<const uint4 *>(k), static_cast<const uint4 *>(v), slots, static_cast<uint4 *>(k_cache),
+        static_cast<uint4 *>(v_cache), num_tokens, num_kv_heads, cpr, block_size,
+        static_cast<long long>(num_blocks) * block_size, err);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_copy_blocks(const int64_t *pairs, int num_pairs, void *k_cache, void *v_cache,
+                               long long block_bytes, int num_blocks, uint32_t *err, int num_sms,
+                               cudaStream_t stream) {
+    const long long chunks = block_bytes / 16;
+    const long long per_cta = 256LL * kCopyUnroll;
+    long long gx = (chunks + per_cta - 1) / per_cta;
+    // enough CTAs in flight to cover HBM latency, without exceeding ~8 per SM
+    long long gy = num_pairs;
+    const long long cap = static_cast<long long>(num_sms) * 8;
+    if (gx * gy * 2 > cap) {
+        gy = cap / (2 * gx);
+        if (gy < 1)
+            gy = 1;
+    }
+    if (gy > 65535)
+        gy = 65535;
+    dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(gy), 2);
+    copy_blocks_kernel<<<grid, 256, 0, stream>>>(pairs, num_pairs, static_cast<uint4 *>(k_cache),
+                                                 static_cast<uint4 *>(v_cache), chunks, num_blocks, err);
+    return cudaGetLastError();
+}
+
+}  // namespace pa

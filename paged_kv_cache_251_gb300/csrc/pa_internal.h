@@ -1,0 +1,26 @@
+// Internal interfaces between the C-ABI layer and the kernel translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace pa {
+
+struct DecodeParams;
+
+// Decode kernel entry (as a function pointer for cudaLaunchKernel) for one
+// element type, head_dim and query-group size; nullptr if not built.
+const void *decode_kernel_f32(int head_dim, int group);
+const void *decode_kernel_f16(int head_dim, int group);
+const void *decode_kernel_bf16(int head_dim, int group);
+const void *reduce_kernel(int head_dim);
+
+cudaError_t launch_append(const void *k, const void *v, const int64_t *slots, void *k_cache, void *v_cache,
+                          int num_tokens, int num_kv_heads, int row_bytes, int block_size, int num_blocks,
+                          uint32_t *err, int num_sms, cudaStream_t stream);
+
+cudaError_t launch_copy_blocks(const int64_t *pairs, int num_pairs, void *k_cache, void *v_cache,
+                               long long block_bytes, int num_blocks, uint32_t *err, int num_sms,
+                               cudaStream_t stream);
+
+}  // namespace pa

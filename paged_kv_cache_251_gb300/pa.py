@@ -1,0 +1,148 @@
+"""Thin ctypes binding of libpa (include/pa.h): argument marshalling only.
+
+Every function takes CUDA torch tensors, passes their device pointers and the
+current torch stream to the C ABI, and raises ``PagedAttentionError`` on a
+non-OK status.  There is no CPU path: the library must be built
+(``paged_kv_cache_251_gb300.build``) and the tensors must live on a GPU.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+from pathlib import Path
+
+import torch
+
+LIB_PATH = Path(__file__).resolve().parent / "_lib" / "libpa.so"
+
+PA_OK, PA_ERR_INVALID_ARGUMENT, PA_ERR_UNSUPPORTED, PA_ERR_WORKSPACE_TOO_SMALL, PA_ERR_CUDA = range(5)
+PA_F32, PA_F16, PA_BF16 = 0, 1, 2
+DEVERR_BAD_BLOCK, DEVERR_BAD_SLOT, DEVERR_BAD_PAIR, DEVERR_TIMEOUT, DEVERR_BAD_LEN = 1, 2, 4, 8, 16
+
+DTYPE_CODE = {torch.float32: PA_F32, torch.float16: PA_F16, torch.bfloat16: PA_BF16}
+
+
+class PagedAttentionError(RuntimeError):
+    def __init__(self, status: int, detail: str):
+        super().__init__(f"{_lib.pa_status_string(status).decode()}: {detail}")
+        self.status = status
+
+
+def _load():
+    if not LIB_PATH.exists():
+        raise ImportError(f"libpa.so is not built ({LIB_PATH}); run paged_kv_cache_251_gb300.build.build()")
+    lib = ctypes.CDLL(str(LIB_PATH))
+    P, I, F, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    lib.pa_decode_workspace_size.argtypes = [I, I, I, I, I, I, I]
+    lib.pa_decode_workspace_size.restype = SZ
+    lib.pa_decode.argtypes = [P, P, P, P, P, P, I, I, I, I, I, F, I, I, I, I, I, I, P, SZ, P, P]
+    lib.pa_decode.restype = I
+    lib.pa_append_kv.argtypes = [P, P, P, P, P, I, I, I, I, I, I, P, P]
+    lib.pa_append_kv.restype = I
+    lib.pa_copy_blocks.argtypes = [P, I, P, P, I, I, I, I, I, P, P]
+    lib.pa_copy_blocks.restype = I
+    lib.pa_status_string.argtypes = [I]
+    lib.pa_status_string.restype = ctypes.c_char_p
+    lib.pa_last_error_detail.argtypes = []
+    lib.pa_last_error_detail.restype = ctypes.c_char_p
+    lib.pa_version.argtypes = []
+    lib.pa_version.restype = I
+    return lib
+
+
+_lib = _load()
+
+
+def _check(status: int) -> None:
+    if status != PA_OK:
+        raise PagedAttentionError(status, _lib.pa_last_error_detail().decode())
+
+
+def _ptr(t: torch.Tensor | None):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _cuda(*ts):
+    for t in ts:
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError("every tensor must be a contiguous CUDA tensor")
+
+
+def pa_decode_workspace_size(num_seqs: int, num_heads: int, head_dim: int, block_size: int,
+                             max_blocks_per_seq: int, window: int = 0, partition_size: int = 0) -> int:
+    return int(_lib.pa_decode_workspace_size(num_seqs, num_heads, head_dim, block_size,
+                                             max_blocks_per_seq, window, partition_size))
+
+
+def workspace_for(q: torch.Tensor, block_size: int, max_blocks_per_seq: int, window: int = 0,
+                  partition_size: int = 0) -> torch.Tensor | None:
+    """A workspace tensor sized by pa_decode_workspace_size (None if 0 bytes)."""
+    N, H, d = q.shape
+    n = pa_decode_workspace_size(N, H, d, block_size, max_blocks_per_seq, window, partition_size)
+    if n == 0:
+        return None
+    return torch.empty((n + 15) // 16 * 4, dtype=torch.float32, device=q.device)
+
+
+def pa_decode(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+              block_tables: torch.Tensor, context_lens: torch.Tensor, num_kv_heads: int | None = None,
+              scale: float | None = None, window: int = 0, partition_size: int = 0,
+              workspace: torch.Tensor | None = None, err_word: torch.Tensor | None = None,
+              stream=None) -> torch.Tensor:
+    """out[s, h] = softmax(scale * q[s, h] . K_s^T) V_s over sequence s's cached
+    tokens, read through block_tables[s] (see include/pa.h)."""
+    _cuda(out, q, k_cache, v_cache, block_tables, context_lens, workspace, err_word)
+    N, H, d = q.shape
+    nb, hkv, bs, d2 = k_cache.shape
+    if num_kv_heads is None:
+        num_kv_heads = hkv
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
+        raise TypeError("block_tables and context_lens must be int32")
+    if q.dtype != k_cache.dtype or v_cache.dtype != k_cache.dtype:
+        raise TypeError("q, k_cache and v_cache must share one dtype")
+    if workspace is None:
+        workspace = workspace_for(q, bs, block_tables.shape[1], window, partition_size)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(_lib.pa_decode(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                          _ptr(context_lens), N, H, num_kv_heads, d, bs, float(scale), int(window),
+                          DTYPE_CODE[q.dtype], DTYPE_CODE[out.dtype], block_tables.shape[1], nb,
+                          int(partition_size), _ptr(workspace), ws_bytes, _ptr(err_word), _stream(stream)))
+    return out
+
+
+def pa_append_kv(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor, k_cache: torch.Tensor,
+                 v_cache: torch.Tensor, err_word: torch.Tensor | None = None, stream=None) -> None:
+    """Store token i's K/V rows at slot_mapping[i] (see include/pa.h)."""
+    _cuda(k, v, slot_mapping, k_cache, v_cache, err_word)
+    if slot_mapping.dtype != torch.int64:
+        raise TypeError("slot_mapping must be int64")
+    if k.dtype != k_cache.dtype or v.dtype != k_cache.dtype or v_cache.dtype != k_cache.dtype:
+        raise TypeError("k, v and the caches must share one dtype")
+    nb, hkv, bs, d = k_cache.shape
+    _check(_lib.pa_append_kv(_ptr(k), _ptr(v), _ptr(slot_mapping), _ptr(k_cache), _ptr(v_cache),
+                             slot_mapping.numel(), hkv, d, bs, nb, DTYPE_CODE[k_cache.dtype],
+                             _ptr(err_word), _stream(stream)))
+
+
+def pa_copy_blocks(src_dst_pairs: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                   err_word: torch.Tensor | None = None, stream=None) -> None:
+    """Copy block src onto block dst (K and V, all kv heads) for every pair."""
+    _cuda(src_dst_pairs, k_cache, v_cache, err_word)
+    if src_dst_pairs.dtype != torch.int64:
+        raise TypeError("src_dst_pairs must be int64")
+    nb, hkv, bs, d = k_cache.shape
+    _check(_lib.pa_copy_blocks(_ptr(src_dst_pairs), src_dst_pairs.numel() // 2, _ptr(k_cache),
+                               _ptr(v_cache), hkv, d, bs, nb, DTYPE_CODE[k_cache.dtype],
+                               _ptr(err_word), _stream(stream)))
+
+
+def version() -> tuple[int, int, int]:
+    v = _lib.pa_version()
+    return (v >> 16) & 0xFF, (v >> 8) & 0xFF, v & 0xFF

@@ -1,0 +1,106 @@
+"""CPU checks of the C ABI: the library loads, exports every function that
+include/*.h declares, and rejects bad arguments on the host before any CUDA
+call (fake device addresses are never dereferenced on these paths)."""
+import ctypes
+import re
+from pathlib import Path
+
+import pytest
+
+from paged_kv_cache_251_gb300 import build as pbuild
+
+ROOT = Path(__file__).resolve().parent.parent
+
+
+@pytest.fixture(scope="module")
+def lib():
+    path = pbuild.build()
+    return ctypes.CDLL(str(path))
+
+
+def declared_functions():
+    names = []
+    for h in sorted((ROOT / "include").glob("*.h")):
+        names += re.findall(r"^PA_API\s+[\w\s\*]+?\b(\w+)\s*\(", h.read_text(), flags=re.M)
+    return names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert {"pa_decode", "pa_append_kv", "pa_copy_blocks", "pa_decode_workspace_size",
+            "pa_status_string"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared but not exported"
+
+
+def _decode_args(**over):
+    a = dict(out=0x1000, q=0x2000, k=0x3000, v=0x4000, bt=0x5000, cl=0x6000, N=4, H=8, Hkv=2, d=128,
+             bs=16, scale=0.088, window=0, dtype=1, out_dtype=0, M=8, nb=64, part=0, ws=0, wsb=0, err=0,
+             stream=0)
+    a.update(over)
+    return a
+
+
+def _call_decode(lib, **over):
+    a = _decode_args(**over)
+    P = ctypes.c_void_p
+    f = lib.pa_decode
+    f.restype = ctypes.c_int
+    f.argtypes = [P, P, P, P, P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                  ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                  ctypes.c_int, P, ctypes.c_size_t, P, P]
+    return f(a["out"], a["q"], a["k"], a["v"], a["bt"], a["cl"], a["N"], a["H"], a["Hkv"], a["d"], a["bs"],
+             a["scale"], a["window"], a["dtype"], a["out_dtype"], a["M"], a["nb"], a["part"], a["ws"],
+             a["wsb"], a["err"], a["stream"])
+
+
+def test_decode_host_validation(lib):
+    INV, UNS, WS = 1, 2, 3
+    assert _call_decode(lib, N=0) == 0                     # nothing to do, no launch
+    assert _call_decode(lib, d=96) == UNS
+    assert _call_decode(lib, bs=12) == UNS
+    assert _call_decode(lib, H=12, Hkv=4) == UNS           # group of 3
+    assert _call_decode(lib, H=9, Hkv=2) == INV            # not a multiple
+    assert _call_decode(lib, q=0) == INV
+    assert _call_decode(lib, k=0x3008) == INV              # misaligned cache
+    assert _call_decode(lib, dtype=7) == INV
+    assert _call_decode(lib, part=24) == INV               # not a multiple of the block size
+    assert _call_decode(lib, part=16 * 257) == INV         # more than 256 blocks
+    assert _call_decode(lib, M=100, ws=0, wsb=0) == WS     # 100 blocks span several partitions
+    assert _call_decode(lib, window=-1) == INV
+    assert _call_decode(lib, nb=0) == INV
+    assert _call_decode(lib, scale=float("inf")) == INV
+
+
+def test_workspace_size(lib):
+    f = lib.pa_decode_workspace_size
+    f.restype = ctypes.c_size_t
+    f.argtypes = [ctypes.c_int] * 7
+    # one partition (<= 512 tokens at block 16): no workspace
+    assert f(64, 40, 128, 16, 32, 0, 0) == 0
+    # OPT-13B-shaped batch: table rows of 129 blocks -> 5 partitions of 32 blocks
+    assert f(64, 40, 128, 16, 129, 0, 0) == 64 * 40 * 5 * (128 + 2) * 4
+    # 4 x 131072 tokens, window 32768 (2049 blocks), 512-token partitions -> 65
+    assert f(4, 32, 128, 16, 8192, 32768, 512) == 4 * 32 * 65 * 130 * 4
+    assert f(4, 32, 96, 16, 8192, 0, 0) == 0                # unsupported -> 0
+
+
+def test_cache_ops_host_validation(lib):
+    P, I = ctypes.c_void_p, ctypes.c_int
+    ap = lib.pa_append_kv
+    ap.restype = I
+    ap.argtypes = [P, P, P, P, P, I, I, I, I, I, I, P, P]
+    assert ap(0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 0, 8, 128, 16, 10, 1, None, None) == 0
+    assert ap(0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 4, 8, 100, 16, 10, 1, None, None) == 2
+    assert ap(0x1000, 0x2004, 0x3000, 0x4000, 0x5000, 4, 8, 128, 16, 10, 1, None, None) == 1
+    assert ap(0x1000, 0x2000, 0x3004, 0x4000, 0x5000, 4, 8, 128, 16, 10, 1, None, None) == 1
+    cp = lib.pa_copy_blocks
+    cp.restype = I
+    cp.argtypes = [P, I, P, P, I, I, I, I, I, P, P]
+    assert cp(0x1000, 0, 0x2000, 0x3000, 8, 128, 16, 10, 2, None, None) == 0
+    assert cp(None, 3, 0x2000, 0x3000, 8, 128, 16, 10, 2, None, None) == 1
+    assert cp(0x1000, 3, 0x2000, 0x3000, 8, 128, 24, 10, 2, None, None) == 2
+    st = lib.pa_status_string
+    st.restype = ctypes.c_char_p
+    st.argtypes = [I]
+    assert st(3) == b"PA_ERR_WORKSPACE_TOO_SMALL"

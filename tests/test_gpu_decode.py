@@ -1,0 +1,112 @@
+"""GPU parity of pa_decode against the fp64 oracle (through the C ABI)."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from paged_kv_cache_251_gb300 import workloads as wl
+from paritylib import compare, make_inputs, oracle_decode, run_decode, shape
+
+pytestmark = pytest.mark.gpu
+
+DT = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}
+
+# (N, H, H_kv, d, bs, lens, window, partition)  — each spans several tiles and a ragged tail
+EDGE_CASES = [
+    ("ctx_edges_bs16", 6, 4, 4, 64, 16, [1, 15, 16, 17, 512, 513], 0, 0),
+    ("ctx_edges_bs8", 6, 8, 2, 128, 8, [1, 7, 8, 9, 512, 513], 0, 0),
+    ("ctx_edges_bs32", 5, 8, 8, 128, 32, [31, 32, 33, 1000, 1025], 0, 0),
+    ("one_seq_long", 1, 4, 1, 128, 16, [3001], 0, 0),
+    ("many_parts", 3, 8, 2, 64, 16, [700, 129, 64], 0, 32),
+    ("window_unaligned", 4, 8, 2, 128, 16, [100, 37, 500, 1200], 37, 0),
+    ("window_ge_ctx", 3, 4, 4, 64, 16, [20, 50, 9], 64, 0),
+    ("window_parts", 3, 8, 1, 128, 16, [2000, 777, 40], 300, 64),
+    ("gqa8", 3, 16, 2, 128, 16, [90, 400, 1], 0, 0),
+    ("gqa2_d64", 4, 8, 4, 64, 32, [65, 66, 700, 2], 0, 0),
+    ("empty_seq", 3, 4, 2, 64, 16, [0, 33, 0], 0, 0),
+]
+
+
+@pytest.mark.parametrize("dt", ["f32", "f16", "bf16"])
+@pytest.mark.parametrize("case", EDGE_CASES, ids=[c[0] for c in EDGE_CASES])
+def test_decode_edge_cases(case, dt):
+    name, n, h, hkv, d, bs, lens, window, part = case
+    sh = shape(name, n, h, hkv, d, bs, DT[dt], window=window, seed=17 + n + d + bs)
+    inp = make_inputs(sh, lens)
+    got, err = run_decode(inp, partition_size=part)
+    assert err == 0
+    compare(got, oracle_decode(inp), DT[dt])
+
+
+@pytest.mark.parametrize("out_dt", ["f16", "bf16"])
+def test_decode_low_precision_output(out_dt):
+    sh = shape("lowout", 4, 8, 2, 128, 16, torch.bfloat16, seed=3)
+    inp = make_inputs(sh, [300, 17, 600, 1])
+    got, err = run_decode(inp, out_dtype=DT[out_dt])
+    assert err == 0 and got.dtype == DT[out_dt]
+    compare(got, oracle_decode(inp), torch.bfloat16)
+
+
+def test_tiny_config():
+    """4 sequences, 4 MHA heads, d 64, block 16, fp32, L ~ U[1,100], 64-block pool."""
+    inp = wl.tiny()
+    got, err = run_decode(inp)
+    assert err == 0
+    compare(got, oracle_decode(inp), torch.float32)
+
+
+def test_invalid_table_entries_are_skipped_and_flagged():
+    sh = shape("bad", 3, 4, 2, 64, 16, torch.float16, seed=8)
+    inp = make_inputs(sh, [70, 40, 33])
+    bt = inp.block_tables.clone()
+    bt[0, 1] = inp.num_blocks + 5        # out of the pool
+    bt[2, 0] = -7
+    got, err = run_decode(inp, block_tables=bt)
+    assert err & 1
+    ref = oracle_decode(inp, block_tables=bt, invalid_policy=1)
+    compare(got, ref, torch.float16)
+
+
+def test_context_beyond_table_row_is_clamped_and_flagged():
+    sh = shape("len", 2, 4, 4, 64, 16, torch.float32, seed=9)
+    inp = make_inputs(sh, [40, 20])
+    M = inp.block_tables.shape[1]
+    cl = torch.tensor([M * 16 + 100, 20], dtype=torch.int32)
+    got, err = run_decode(inp, context_lens=cl)
+    assert err & 16
+    # seq 0 is clamped to M*16 tokens; its table holds -1 beyond its 3 blocks
+    ref = oracle_decode(inp, context_lens=torch.tensor([M * 16, 20], dtype=torch.int32), invalid_policy=1)
+    compare(got, ref, torch.float32)
+
+
+def test_table_entries_outside_the_window_are_never_read():
+    """A sliding window touches only its own table entries: poison the rest."""
+    sh = shape("win", 2, 8, 2, 128, 16, torch.bfloat16, window=256, seed=10)
+    inp = make_inputs(sh, [1000, 900])
+    bt = inp.block_tables.clone()
+    for s, L in enumerate([1000, 900]):
+        first = (L - 256) // 16
+        bt[s, :first] = 0x7FFFFFFF
+    got, err = run_decode(inp, block_tables=bt)
+    assert err == 0
+    compare(got, oracle_decode(inp, block_tables=bt), torch.bfloat16)
+
+
+def _sample_pairs(N, H, count, seed):
+    idx = wl.permutation(seed, 1, N * H)[:count]
+    return torch.stack([idx // H, idx % H], dim=1).to(torch.int32)
+
+
+@pytest.mark.parametrize("name", ["opt13b", "gqa"])
+def test_full_size_config_sampled(name):
+    """Full-size workloads in the launch configuration the benchmark times;
+    every output is finite and a sample of rows matches the oracle."""
+    inp = wl.opt13b() if name == "opt13b" else wl.gqa()
+    got, err = run_decode(inp)
+    assert err == 0
+    s = inp.shape
+    pairs = _sample_pairs(s.num_seqs, s.num_heads, 96, seed=77)
+    ref = oracle_decode(inp, pairs=pairs)
+    sel = got[pairs[:, 0].long(), pairs[:, 1].long()]
+    compare(sel, ref, s.dtype)
