@@ -319,6 +319,8 @@ const char *pa_status_string(pa_status status) {
         return "PA_ERR_WORKSPACE_TOO_SMALL";
     case PA_ERR_CUDA:
         return "PA_ERR_CUDA";
+    case PA_ERR_NO_BLOCKS:
+        return "PA_ERR_NO_BLOCKS";
     }
     return "PA_ERR_UNKNOWN";
 }
