@@ -142,6 +142,36 @@ PA_API pa_status pa_decode(void *out, const void *q, const void *k_cache, const 
                     size_t workspace_bytes, uint32_t *err_word, pa_stream_t stream);
 
 /*
+ * pa_decode without any allocation.  No page describes this call: it exists
+ * for callers that cannot allocate device memory (a plugin whose host
+ * framework owns all device allocations, a runtime with a fixed memory
+ * budget, a path that must not pay for cudaMalloc).  Arguments and results
+ * are those of pa_decode without workspace / workspace_bytes: the scratch for
+ * partition partials is one array built into the library,
+ * pa_decode_noalloc_max_scratch() bytes (32 MiB), which every GPU that loads
+ * the library holds until the process exits.
+ *  - A shape whose pa_decode_workspace_size() exceeds that size is rejected
+ *    with PA_ERR_WORKSPACE_TOO_SMALL before anything is launched.
+ *  - The first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress, with that device current) and caches it; make
+ *    that first call before any stream capture.
+ *  - All calls on a device share the array and it keeps the last call's
+ *    contents (nothing in it needs to start at zero).  Calls that overlap on
+ *    the GPU race on it: order them on one stream.
+ * It calls no cudaMalloc, cudaFree or other allocating routine.
+ */
+PA_API pa_status pa_decode_noalloc(void *out, const void *q, const void *k_cache, const void *v_cache,
+                                   const int32_t *block_tables, const int32_t *context_lens,
+                                   int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                                   int block_size, float scale, int window,
+                                   pa_dtype dtype, pa_dtype out_dtype, int max_blocks_per_seq,
+                                   int num_blocks, int partition_size, uint32_t *err_word,
+                                   pa_stream_t stream);
+
+/* Size in bytes of the scratch array pa_decode_noalloc uses. */
+PA_API size_t pa_decode_noalloc_max_scratch(void);
+
+/*
  * Append [B 核心要点, 案例 2]: for every token i with slot = slot_mapping[i] >= 0
  *   k_cache[slot / block_size][h][slot % block_size][:] = k[i][h][:]   (all h)
  *   v_cache[...] = v[i][h][:]

@@ -125,6 +125,9 @@ pa_status plan_decode(int num_seqs, int num_heads, int head_dim, int block_size,
 }
 
 }  // namespace
+
+void set_last_error_detail(const char *why) { g_detail = why; }
+
 }  // namespace pa
 
 using namespace pa;

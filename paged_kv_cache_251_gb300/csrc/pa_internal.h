@@ -23,4 +23,7 @@ cudaError_t launch_copy_blocks(const int64_t *pairs, int num_pairs, void *k_cach
                                long long block_bytes, int num_blocks, uint32_t *err, int num_sms,
                                cudaStream_t stream);
 
+// Text returned by pa_last_error_detail() on the calling thread.
+void set_last_error_detail(const char *why);
+
 }  // namespace pa

@@ -37,6 +37,10 @@ def _load():
     lib.pa_decode_workspace_size.restype = SZ
     lib.pa_decode.argtypes = [P, P, P, P, P, P, I, I, I, I, I, F, I, I, I, I, I, I, P, SZ, P, P]
     lib.pa_decode.restype = I
+    lib.pa_decode_noalloc.argtypes = [P, P, P, P, P, P, I, I, I, I, I, F, I, I, I, I, I, I, P, P]
+    lib.pa_decode_noalloc.restype = I
+    lib.pa_decode_noalloc_max_scratch.argtypes = []
+    lib.pa_decode_noalloc_max_scratch.restype = SZ
     lib.pa_append_kv.argtypes = [P, P, P, P, P, I, I, I, I, I, I, P, P]
     lib.pa_append_kv.restype = I
     lib.pa_copy_blocks.argtypes = [P, I, P, P, I, I, I, I, I, P, P]
@@ -115,6 +119,36 @@ def pa_decode(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_cache
                           DTYPE_CODE[q.dtype], DTYPE_CODE[out.dtype], block_tables.shape[1], nb,
                           int(partition_size), _ptr(workspace), ws_bytes, _ptr(err_word), _stream(stream)))
     return out
+
+
+def pa_decode_noalloc(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                      block_tables: torch.Tensor, context_lens: torch.Tensor, num_kv_heads: int | None = None,
+                      scale: float | None = None, window: int = 0, partition_size: int = 0,
+                      err_word: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """pa_decode for callers that cannot allocate device memory: the partials'
+    scratch is the library's built-in array (pa_decode_noalloc_max_scratch()
+    bytes), shared by all calls on a device, so calls must not overlap on the
+    GPU.  This wrapper allocates nothing either."""
+    _cuda(out, q, k_cache, v_cache, block_tables, context_lens, err_word)
+    N, H, d = q.shape
+    nb, hkv, bs, d2 = k_cache.shape
+    if num_kv_heads is None:
+        num_kv_heads = hkv
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
+        raise TypeError("block_tables and context_lens must be int32")
+    if q.dtype != k_cache.dtype or v_cache.dtype != k_cache.dtype:
+        raise TypeError("q, k_cache and v_cache must share one dtype")
+    _check(_lib.pa_decode_noalloc(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                                  _ptr(context_lens), N, H, num_kv_heads, d, bs, float(scale), int(window),
+                                  DTYPE_CODE[q.dtype], DTYPE_CODE[out.dtype], block_tables.shape[1], nb,
+                                  int(partition_size), _ptr(err_word), _stream(stream)))
+    return out
+
+
+def pa_decode_noalloc_max_scratch() -> int:
+    return int(_lib.pa_decode_noalloc_max_scratch())
 
 
 def pa_append_kv(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor, k_cache: torch.Tensor,
