@@ -1,8 +1,11 @@
 // C-ABI entry points of libpa: argument checks, launch planning, launches.
 // The operations and their sources are documented in include/pa.h.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <climits>
 #include <cmath>
 #include <cstdio>
 #include <map>
@@ -12,6 +15,7 @@
 
 #include "pa.h"
 #include "pa_decode.cuh"
+#include "pa_decode_mha.cuh"
 #include "pa_internal.h"
 
 namespace pa {
@@ -89,7 +93,53 @@ cudaError_t prepare_kernel(int dev, const void *fn, size_t smem, int threads, in
     return cudaSuccess;
 }
 
+// cuTensorMapEncodeTiled, fetched once through the runtime (no link-time
+// dependency on the driver library).
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+cudaError_t g_encode_err = cudaSuccess;
+
+cudaError_t tensor_map_encoder(PFN_cuTensorMapEncodeTiled_v12000 *fn) {
+    std::call_once(g_encode_once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        g_encode_err = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q);
+        if (g_encode_err == cudaSuccess && q != cudaDriverEntryPointSuccess)
+            g_encode_err = cudaErrorSymbolNotFound;
+        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    *fn = g_encode;
+    return g_encode_err;
+}
+
+// 3-D view of a K or V cache [num_blocks * H_kv][block_size][head_dim] with a
+// box of one 128-byte row segment x block_size rows, 128-byte swizzle.
+pa_status kv_tensor_map(CUtensorMap *map, const void *base, int dtype, int head_dim, int block_size,
+                        long long tiles) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
+    cudaError_t e = tensor_map_encoder(&enc);
+    if (e != cudaSuccess || !enc)
+        return cuda_fail(e == cudaSuccess ? cudaErrorSymbolNotFound : e, "cuTensorMapEncodeTiled lookup");
+    const int elt = elt_bytes(dtype);
+    const CUtensorMapDataType dt = dtype == PA_F32   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                   : dtype == PA_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                     : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(block_size),
+                          static_cast<cuuint64_t>(tiles)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(head_dim) * elt,
+                             static_cast<cuuint64_t>(head_dim) * elt * block_size};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / elt), static_cast<cuuint32_t>(block_size), 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(map, dt, 3, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(PA_ERR_INVALID_ARGUMENT, "cuTensorMapEncodeTiled rejected the cache layout (code " +
+                                                 std::to_string(static_cast<int>(r)) + ")");
+    return PA_OK;
+}
+
 constexpr int kDefaultPartition = 512;
+constexpr int kMhaStageBudget = 64 * 1024;
 constexpr int kStageBudget = 48 * 1024;
 
 struct DecodePlan {
@@ -178,28 +228,6 @@ pa_status pa_decode(void *out, const void *q, const void *k_cache, const void *v
     if (plan.workspace > 0 && !aligned16(workspace))
         return fail(PA_ERR_INVALID_ARGUMENT, "workspace must be 16-byte aligned");
 
-    const void *fn = dtype == PA_F32   ? decode_kernel_f32(head_dim, G)
-                     : dtype == PA_F16 ? decode_kernel_f16(head_dim, G)
-                                       : decode_kernel_bf16(head_dim, G);
-    if (!fn)
-        return fail(PA_ERR_UNSUPPORTED, "no decode kernel for this dtype / head_dim / group");
-
-    const int row = head_dim * elt_bytes(dtype);
-    const int tile = block_size * row;
-    int S = kStageBudget / (2 * tile);
-    S = S < 2 ? 2 : (S > 8 ? 8 : S);
-    const size_t smem = decode_smem_layout(S, tile, row, G, head_dim).total;
-
-    int dev = 0, sms = 0, per_sm = 0;
-    cudaError_t e = device_sms(&dev, &sms);
-    if (e != cudaSuccess)
-        return cuda_fail(e, "device query");
-    e = prepare_kernel(dev, fn, smem, kDecodeThreads, &per_sm);
-    if (e != cudaSuccess)
-        return cuda_fail(e, "decode kernel set-up");
-    if (per_sm < 1)
-        return fail(PA_ERR_UNSUPPORTED, "decode kernel does not fit on an SM");
-
     DecodeParams p;
     p.out = out;
     p.q = q;
@@ -217,13 +245,60 @@ pa_status pa_decode(void *out, const void *q, const void *k_cache, const void *v
     p.block_size = block_size;
     p.window = window;
     p.max_blocks_per_seq = max_blocks_per_seq;
-    p.max_len = static_cast<int>(std::min<long long>(static_cast<long long>(max_blocks_per_seq) * block_size, 0x7fffffffLL));
+    p.max_len = static_cast<int>(std::min<long long>(static_cast<long long>(max_blocks_per_seq) * block_size, INT_MAX));
     p.num_blocks = num_blocks;
     p.bpp = plan.bpp;
     p.max_parts = plan.max_parts;
     p.out_dtype = out_dtype;
-    p.stages = S;
+    p.stages = 0;
     p.scale_log2 = scale * 1.4426950408889634f;
+
+    const int row = head_dim * elt_bytes(dtype);
+    const int tile = block_size * row;
+    const long long tiles = static_cast<long long>(num_blocks) * num_kv_heads;
+    // MHA takes the TMA-tensor kernel; its 3-D tensor map addresses tiles with
+    // a 32-bit coordinate, so very large pools use the general kernel.
+    const bool mha = (G == 1 && tiles <= INT_MAX);
+    const void *fn;
+    size_t smem;
+    int threads;
+    CUtensorMap tmk, tmv;
+    if (mha) {
+        fn = dtype == PA_F32   ? decode_mha_kernel_f32(head_dim, block_size)
+             : dtype == PA_F16 ? decode_mha_kernel_f16(head_dim, block_size)
+                               : decode_mha_kernel_bf16(head_dim, block_size);
+        int S = kMhaStageBudget / (2 * tile);
+        S = S < 4 ? 4 : (S > 16 ? 16 : S);
+        p.stages = S;
+        smem = mha_smem_layout(S, tile, row, head_dim).total;
+        threads = kMhaThreads;
+        pa_status ts = kv_tensor_map(&tmk, k_cache, dtype, head_dim, block_size, tiles);
+        if (ts == PA_OK)
+            ts = kv_tensor_map(&tmv, v_cache, dtype, head_dim, block_size, tiles);
+        if (ts != PA_OK)
+            return ts;
+    } else {
+        fn = dtype == PA_F32   ? decode_kernel_f32(head_dim, G)
+             : dtype == PA_F16 ? decode_kernel_f16(head_dim, G)
+                               : decode_kernel_bf16(head_dim, G);
+        int S = kStageBudget / (2 * tile);
+        S = S < 2 ? 2 : (S > 8 ? 8 : S);
+        p.stages = S;
+        smem = decode_smem_layout(S, tile, row, G, head_dim).total;
+        threads = kDecodeThreads;
+    }
+    if (!fn)
+        return fail(PA_ERR_UNSUPPORTED, "no decode kernel for this dtype / head_dim / group / block size");
+
+    int dev = 0, sms = 0, per_sm = 0;
+    cudaError_t e = device_sms(&dev, &sms);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "device query");
+    e = prepare_kernel(dev, fn, smem, threads, &per_sm);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "decode kernel set-up");
+    if (per_sm < 1)
+        return fail(PA_ERR_UNSUPPORTED, "decode kernel does not fit on an SM");
 
     const long long items_max = static_cast<long long>(num_seqs) * num_kv_heads * plan.max_parts;
     long long grid = static_cast<long long>(sms) * per_sm;
@@ -231,9 +306,10 @@ pa_status pa_decode(void *out, const void *q, const void *k_cache, const void *v
         grid = items_max;
     if (grid < 1)
         grid = 1;
-    void *args[] = {&p};
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-    e = cudaLaunchKernel(fn, dim3(static_cast<unsigned>(grid)), dim3(kDecodeThreads), args, smem, cs);
+    void *args_mha[] = {&p, &tmk, &tmv};
+    void *args[] = {&p};
+    e = cudaLaunchKernel(fn, dim3(static_cast<unsigned>(grid)), dim3(threads), mha ? args_mha : args, smem, cs);
     if (e != cudaSuccess)
         return cuda_fail(e, "decode launch");
     if (plan.max_parts > 1) {

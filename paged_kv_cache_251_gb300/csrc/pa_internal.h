@@ -15,6 +15,12 @@ const void *decode_kernel_f16(int head_dim, int group);
 const void *decode_kernel_bf16(int head_dim, int group);
 const void *reduce_kernel(int head_dim);
 
+// MHA (one query head per kv head) decode kernels fed by TMA tensor copies,
+// per element type, head_dim and block size; nullptr if not built.
+const void *decode_mha_kernel_f32(int head_dim, int block_size);
+const void *decode_mha_kernel_f16(int head_dim, int block_size);
+const void *decode_mha_kernel_bf16(int head_dim, int block_size);
+
 cudaError_t launch_append(const void *k, const void *v, const int64_t *slots, void *k_cache, void *v_cache,
                           int num_tokens, int num_kv_heads, int row_bytes, int block_size, int num_blocks,
                           uint32_t *err, int num_sms, cudaStream_t stream);

@@ -25,6 +25,12 @@ EDGE_CASES = [
     ("gqa8", 3, 16, 2, 128, 16, [90, 400, 1], 0, 0),
     ("gqa2_d64", 4, 8, 4, 64, 32, [65, 66, 700, 2], 0, 0),
     ("empty_seq", 3, 4, 2, 64, 16, [0, 33, 0], 0, 0),
+    # one query head per kv head at every block size (the TMA-tensor kernel)
+    ("mha_bs8_d128", 4, 6, 6, 128, 8, [9, 700, 1, 255], 0, 0),
+    ("mha_bs32_d64", 4, 4, 4, 64, 32, [33, 31, 1100, 64], 0, 0),
+    ("mha_bs16_parts", 3, 5, 5, 128, 16, [2000, 100, 513], 0, 64),
+    ("mha_window", 3, 4, 4, 128, 16, [1000, 20, 777], 100, 0),
+    ("mha_empty", 3, 2, 2, 64, 8, [0, 5, 0], 0, 0),
 ]
 
 
@@ -56,8 +62,9 @@ def test_tiny_config():
     compare(got, oracle_decode(inp), torch.float32)
 
 
-def test_invalid_table_entries_are_skipped_and_flagged():
-    sh = shape("bad", 3, 4, 2, 64, 16, torch.float16, seed=8)
+@pytest.mark.parametrize("hkv", [4, 2])
+def test_invalid_table_entries_are_skipped_and_flagged(hkv):
+    sh = shape("bad", 3, 4, hkv, 64, 16, torch.float16, seed=8)
     inp = make_inputs(sh, [70, 40, 33])
     bt = inp.block_tables.clone()
     bt[0, 1] = inp.num_blocks + 5        # out of the pool
@@ -80,9 +87,10 @@ def test_context_beyond_table_row_is_clamped_and_flagged():
     compare(got, ref, torch.float32)
 
 
-def test_table_entries_outside_the_window_are_never_read():
+@pytest.mark.parametrize("hkv", [8, 2])
+def test_table_entries_outside_the_window_are_never_read(hkv):
     """A sliding window touches only its own table entries: poison the rest."""
-    sh = shape("win", 2, 8, 2, 128, 16, torch.bfloat16, window=256, seed=10)
+    sh = shape("win", 2, 8, hkv, 128, 16, torch.bfloat16, window=256, seed=10)
     inp = make_inputs(sh, [1000, 900])
     bt = inp.block_tables.clone()
     for s, L in enumerate([1000, 900]):
