@@ -51,7 +51,8 @@ def parse_args(argv=None):
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
-    ap.add_argument("--workload", choices=["opt13b", "gqa"], default="opt13b")
+    ap.add_argument("--workload", choices=["opt13b", "gqa", "window", "prefix_bs8", "prefix_bs16",
+                                           "prefix_bs32"], default="opt13b")
     ap.add_argument("--partition", type=int, default=0, help="pa_decode partition_size (0 = default)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU baseline budget")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -171,59 +172,281 @@ def _isnum(s):
 
 
 # ---------------------------------------------------------------------------
-# workload
+# workloads: each defines one step on the GPU, its bytes, its end-to-end form
+# (host buffers) and the oracle's version of the same step
 
 
-def build_workload(name: str, device):
-    """Inputs of one step, resident on `device`, plus host copies where needed."""
-    from paged_kv_cache_251_gb300 import workloads as wl
-    from paged_kv_cache_251_gb300.blocks import BlockManager
+class Step:
+    """One workload's step.  Tensors the step reads are resident on the GPU;
+    `host` holds pinned host copies of the per-step inputs for the end-to-end
+    measurement."""
 
-    if name == "opt13b":
-        inp = wl.decode_inputs(wl.SHAPES["opt13b"], device=device)
-    else:
-        inp = wl.decode_inputs(wl.SHAPES["gqa"], device=device, room_for_append=True, fill=0.95)
-    s = inp.shape
-    # slots of the appended token (position L of every sequence): the host
-    # block manager replays each sequence's blocks in table order
-    held = inp.blocks_held.tolist()
-    order = [b for row, n in zip(inp.block_tables.tolist(), held) for b in row[:n]]
-    used = set(order)
-    rest = [b for b in range(inp.num_blocks) if b not in used]
-    bm = BlockManager(inp.num_blocks, s.block_size, s.num_seqs, inp.block_tables.shape[1],
-                      free_order=order + rest)
-    slots = torch.empty(s.num_seqs, dtype=torch.int64)
-    for i in range(s.num_seqs):
-        bm.add_sequence(i)
-        sl, _ = bm.extend(i, int(inp.context_lens[i]) + 1)
-        slots[i] = sl[-1]
-    tables, _ = bm.tables()
-    assert torch.equal(tables, inp.block_tables), "block manager replay disagrees with the generated tables"
-    return inp, slots
+    name = ""
+    description = ""
+
+    def __init__(self, device, partition):
+        self.device = device
+        self.partition = partition
+        self.err = torch.zeros(1, dtype=torch.int32, device=device)
+
+    # the parts of a step, enqueued on `stream`
+    def pre(self, stream):
+        pass
+
+    def decode(self, stream):
+        raise NotImplementedError
+
+    def post(self, stream):
+        pass
+
+    append_first = False   # prefix sharing writes the new tokens before it decodes
+
+    def run(self, stream, events=None):
+        """One step; `events` (start, end) bracket the decode call."""
+        self.pre(stream)
+        if self.append_first:
+            self.post(stream)
+        if events:
+            events[0].record(stream)
+        self.decode(stream)
+        if events:
+            events[1].record(stream)
+        if not self.append_first:
+            self.post(stream)
 
 
-def step_bytes(inp):
-    from paged_kv_cache_251_gb300 import accounting as acc
-    s = inp.shape
-    elt = torch.tensor([], dtype=s.dtype).element_size()
-    dec = acc.decode_bytes(inp.context_lens.cpu(), s.num_heads, s.num_kv_heads, s.head_dim, s.block_size, elt,
-                           out_elt_bytes=4, window=s.window)
-    app = acc.append_bytes(s.num_seqs, s.num_kv_heads, s.head_dim, elt)
-    return dec, app
+def _elt(dtype):
+    return torch.tensor([], dtype=dtype).element_size()
 
 
-def traffic_from_profile(kernel_hash: str):
-    """dram bytes per decode launch from the committed ncu summary, if it was
-    taken on the current kernel source; else None."""
-    path = os.path.join(ROOT, "profiles", "pa_decode_opt13b.md")
+class DecodeAppendStep(Step):
+    """pa_decode over every sequence's L tokens, then pa_append_kv of token L
+    (the slot the host block manager assigns); idempotent step."""
+
+    def __init__(self, name, device, partition):
+        super().__init__(device, partition)
+        from paged_kv_cache_251_gb300 import pa
+        from paged_kv_cache_251_gb300 import workloads as wl
+        from paged_kv_cache_251_gb300.blocks import BlockManager
+        self.pa = pa
+        self.name = name
+        if name == "opt13b":
+            inp = wl.decode_inputs(wl.SHAPES["opt13b"], device=device)
+            self.description = ("opt13b: 64 seqs x 40 MHA heads, head_dim 128, block 16, fp16, context ~ U[512, 2048], "
+                                "exact-need pool shuffled; step = pa_decode + pa_append_kv (1 token/seq)")
+        else:
+            inp = wl.decode_inputs(wl.SHAPES["gqa"], device=device, room_for_append=True, fill=0.95)
+            self.description = ("gqa: 256 seqs, 32 q / 8 kv heads, head_dim 128, block 16, bf16, lognormal context "
+                                "(median 1024, sigma 1) clipped to [16, 8192], 95%-full shuffled pool; "
+                                "step = pa_decode + pa_append_kv (1 token/seq)")
+        s = self.shape = inp.shape
+        # the host block manager replays each sequence's blocks in table order and
+        # assigns the slot of the appended token (position L)
+        held = inp.blocks_held.tolist()
+        order = [b for row, n in zip(inp.block_tables.tolist(), held) for b in row[:n]]
+        used = set(order)
+        rest = [b for b in range(inp.num_blocks) if b not in used]
+        bm = BlockManager(inp.num_blocks, s.block_size, s.num_seqs, inp.block_tables.shape[1],
+                          free_order=order + rest)
+        slots = torch.empty(s.num_seqs, dtype=torch.int64)
+        for i in range(s.num_seqs):
+            bm.add_sequence(i)
+            sl, _ = bm.extend(i, int(inp.context_lens[i]) + 1)
+            slots[i] = sl[-1]
+        tables, _ = bm.tables()
+        assert torch.equal(tables, inp.block_tables), "block manager replay disagrees with the generated tables"
+        self.inp = inp
+        self.q, self.k_cache, self.v_cache = inp.q, inp.k_cache, inp.v_cache
+        self.k_new, self.v_new = inp.k_new, inp.v_new
+        self.bt, self.cl, self.slots = inp.block_tables.to(device), inp.context_lens.to(device), slots.to(device)
+        self.host = {"q": inp.q, "k_new": inp.k_new, "v_new": inp.v_new, "slots": slots,
+                     "context_lens": inp.context_lens, "block_tables": inp.block_tables}
+        self.out = torch.empty(inp.q.shape, dtype=torch.float32, device=device)
+        self.window = 0
+        self.ws = pa.workspace_for(inp.q, s.block_size, self.bt.shape[1], 0, partition)
+        elt = _elt(s.dtype)
+        from paged_kv_cache_251_gb300 import accounting as acc
+        self.dec_bytes = acc.decode_bytes(inp.context_lens, s.num_heads, s.num_kv_heads, s.head_dim,
+                                          s.block_size, elt, out_elt_bytes=4)
+        self.kv_bytes = self.dec_bytes["kv"]
+        self.roof_bytes = self.dec_bytes["total"]
+        self.launches = (2 if self.ws is not None else 1) + 1
+
+    def decode(self, stream, q=None, bt=None, cl=None):
+        s = self.shape
+        self.pa.pa_decode(self.out, self.q if q is None else q, self.k_cache, self.v_cache,
+                          self.bt if bt is None else bt, self.cl if cl is None else cl, num_kv_heads=s.num_kv_heads,
+                          window=self.window, partition_size=self.partition, workspace=self.ws, err_word=self.err,
+                          stream=stream)
+
+    def post(self, stream, k_new=None, v_new=None, slots=None):
+        self.pa.pa_append_kv(self.k_new if k_new is None else k_new, self.v_new if v_new is None else v_new,
+                             self.slots if slots is None else slots, self.k_cache, self.v_cache, err_word=self.err,
+                             stream=stream)
+
+    def e2e(self, stream, dev):
+        """The step through the public API from host buffers (dev: device
+        staging tensors filled here)."""
+        for k in ("q", "k_new", "v_new", "slots", "context_lens", "block_tables"):
+            dev[k].copy_(self.host_pinned[k], non_blocking=True)
+        self.decode(stream, q=dev["q"], bt=dev["block_tables"], cl=dev["context_lens"])
+        self.post(stream, k_new=dev["k_new"], v_new=dev["v_new"], slots=dev["slots"])
+        self.out_host.copy_(self.out, non_blocking=True)
+
+    def oracle_step(self, threads, rows=None):
+        """The same step on the CPU oracle (host copies made on first use);
+        rows limits the decode to the first `rows` sequences."""
+        import oracle
+        if not hasattr(self, "_h"):
+            self._h = [t.cpu() for t in (self.q, self.k_cache, self.v_cache, self.k_new, self.v_new)]
+        q, k, v, kn, vn = self._h
+        s = self.shape
+        n = s.num_seqs if rows is None else rows
+        oracle.paged_attention(q[:n], k, v, self.inp.block_tables[:n], self.inp.context_lens[:n],
+                               num_kv_heads=s.num_kv_heads, scale=1.0 / math.sqrt(s.head_dim), threads=threads)
+        oracle.append_kv(k, v, kn, vn, self.host["slots"])
+        return int(self.inp.context_lens[:n].to(torch.int64).sum()) * 2 * s.num_kv_heads * s.head_dim * _elt(s.dtype)
+
+
+class WindowStep(DecodeAppendStep):
+    """Sliding window: pa_decode with window 32768 (512-token partitions +
+    reduce) over 4 x 131072-token sequences held in rings of 2049 blocks, then
+    pa_append_kv of token L (a ring table rewrite on the host)."""
+
+    def __init__(self, device, partition):
+        Step.__init__(self, device, partition or 512)
+        from paged_kv_cache_251_gb300 import pa, scenarios
+        from paged_kv_cache_251_gb300 import accounting as acc
+        self.pa = pa
+        self.name = "window"
+        self.description = ("window: 4 seqs x 131072 logical tokens, 32 q / 8 kv heads, head_dim 128, bf16, block 16, "
+                            "window 32768 over rings of 2049 physical blocks (table rewrite, no K/V movement), "
+                            "512-token partitions + LSE reduce; step = pa_decode + pa_append_kv (1 token/seq)")
+        st = scenarios.window_state(device=device)
+        s = self.shape = st.shape
+        self.window = s.window
+        tables0, lens0 = st.block_tables, st.context_lens
+        slots, _ = st.manager.append(list(range(s.num_seqs)))   # token L of every sequence
+        # decode over L tokens with the tables as they were before token L
+        self.inp = type("I", (), {"block_tables": tables0, "context_lens": lens0})
+        self.q, self.k_cache, self.v_cache, self.k_new, self.v_new = st.q, st.k_cache, st.v_cache, st.k_new, st.v_new
+        self.bt, self.cl, self.slots = tables0.to(device), lens0.to(device), slots.to(device)
+        self.host = {"q": st.q, "k_new": st.k_new, "v_new": st.v_new, "slots": slots, "context_lens": lens0,
+                     "block_tables": tables0}
+        self.out = torch.empty(st.q.shape, dtype=torch.float32, device=device)
+        self.ws = pa.workspace_for(st.q, s.block_size, self.bt.shape[1], self.window, self.partition)
+        self.dec_bytes = acc.decode_bytes(lens0, s.num_heads, s.num_kv_heads, s.head_dim, s.block_size,
+                                          _elt(s.dtype), out_elt_bytes=4, window=self.window)
+        self.kv_bytes = self.dec_bytes["kv"]
+        self.roof_bytes = self.dec_bytes["total"]
+        self.launches = 3
+
+    def oracle_step(self, threads, rows=None):
+        import oracle
+        if not hasattr(self, "_h"):
+            self._h = [t.cpu() for t in (self.q, self.k_cache, self.v_cache, self.k_new, self.v_new)]
+        q, k, v, kn, vn = self._h
+        s = self.shape
+        n = s.num_seqs if rows is None else rows
+        oracle.paged_attention(q[:n], k, v, self.inp.block_tables[:n], self.inp.context_lens[:n],
+                               num_kv_heads=s.num_kv_heads, scale=1.0 / math.sqrt(s.head_dim), window=self.window,
+                               threads=threads)
+        oracle.append_kv(k, v, kn, vn, self.host["slots"])
+        return n * self.window * 2 * s.num_kv_heads * s.head_dim * _elt(s.dtype)
+
+
+class PrefixStep(DecodeAppendStep):
+    """Prefix sharing: pa_copy_blocks (copy-on-write of the partly filled last
+    prompt block, block 32 only), pa_append_kv of every sample's 1-256 new
+    tokens, pa_decode over all 256 samples; idempotent step."""
+
+    append_first = True
+
+    def __init__(self, device, partition, block_size=16):
+        Step.__init__(self, device, partition)
+        from paged_kv_cache_251_gb300 import pa, scenarios
+        from paged_kv_cache_251_gb300 import accounting as acc
+        self.pa = pa
+        self.name = f"prefix_bs{block_size}"
+        st = scenarios.prefix_state(block_size, device=device)
+        s = self.shape = st.shape
+        self.description = (f"prefix: 32 prompts x 2000 tokens shared by 8 samples each (256 samples), U{{1..256}} new "
+                            f"tokens per sample ({st.slots.numel()} in all), 40 MHA heads, head_dim 128, fp16, "
+                            f"block {block_size}, {st.pairs.shape[0]} copy-on-write pairs; step = pa_copy_blocks + "
+                            f"pa_append_kv + pa_decode")
+        self.window = 0
+        self.inp = type("I", (), {"block_tables": st.block_tables, "context_lens": st.context_lens})
+        self.q, self.k_cache, self.v_cache, self.k_new, self.v_new = st.q, st.k_cache, st.v_cache, st.k_new, st.v_new
+        self.bt, self.cl, self.slots = st.block_tables.to(device), st.context_lens.to(device), st.slots.to(device)
+        self.pairs = st.pairs.to(device)
+        self.host = {"q": st.q, "k_new": st.k_new, "v_new": st.v_new, "slots": st.slots,
+                     "context_lens": st.context_lens, "block_tables": st.block_tables, "pairs": st.pairs}
+        self.out = torch.empty(st.q.shape, dtype=torch.float32, device=device)
+        self.ws = pa.workspace_for(st.q, s.block_size, self.bt.shape[1], 0, partition)
+        elt = _elt(s.dtype)
+        self.dec_bytes = acc.decode_bytes(st.context_lens, s.num_heads, s.num_kv_heads, s.head_dim, s.block_size, elt,
+                                          out_elt_bytes=4)
+        # logical bytes (every sample reads its own context) and unique bytes
+        # (a prompt's shared blocks once): the roofline uses the unique bytes
+        shared_blocks = st.prompts * (st.prompt_len // block_size)
+        per_tok = 2 * s.num_kv_heads * s.head_dim * elt
+        self.kv_bytes = self.dec_bytes["kv"]
+        self.unique_kv = self.kv_bytes - (st.samples - 1) * shared_blocks * block_size * per_tok
+        self.roof_bytes = self.dec_bytes["total"] - (self.kv_bytes - self.unique_kv)
+        self.launches = (1 if st.pairs.shape[0] else 0) + 1 + (2 if self.ws is not None else 1)
+        self.T = st.slots.numel()
+
+    def pre(self, stream, pairs=None):
+        self.pa.pa_copy_blocks(self.pairs if pairs is None else pairs, self.k_cache, self.v_cache,
+                               err_word=self.err, stream=stream)
+
+    def e2e(self, stream, dev):
+        for k in ("q", "k_new", "v_new", "slots", "context_lens", "block_tables", "pairs"):
+            dev[k].copy_(self.host_pinned[k], non_blocking=True)
+        self.pre(stream, pairs=dev["pairs"])
+        self.post(stream, k_new=dev["k_new"], v_new=dev["v_new"], slots=dev["slots"])
+        self.decode(stream, q=dev["q"], bt=dev["block_tables"], cl=dev["context_lens"])
+        self.out_host.copy_(self.out, non_blocking=True)
+
+    def oracle_step(self, threads, rows=None):
+        import oracle
+        if not hasattr(self, "_h"):
+            self._h = [t.cpu() for t in (self.q, self.k_cache, self.v_cache, self.k_new, self.v_new)]
+        q, k, v, kn, vn = self._h
+        s = self.shape
+        n = s.num_seqs if rows is None else rows
+        oracle.copy_blocks(k, v, self.host["pairs"])
+        oracle.append_kv(k, v, kn, vn, self.host["slots"])
+        oracle.paged_attention(q[:n], k, v, self.inp.block_tables[:n], self.inp.context_lens[:n],
+                               num_kv_heads=s.num_kv_heads, scale=1.0 / math.sqrt(s.head_dim), threads=threads)
+        return int(self.inp.context_lens[:n].to(torch.int64).sum()) * 2 * s.num_kv_heads * s.head_dim * _elt(s.dtype)
+
+
+WORKLOADS = ["opt13b", "gqa", "window", "prefix_bs8", "prefix_bs16", "prefix_bs32"]
+
+
+def make_step(name, device, partition):
+    if name in ("opt13b", "gqa"):
+        return DecodeAppendStep(name, device, partition)
+    if name == "window":
+        return WindowStep(device, partition)
+    if name.startswith("prefix_bs"):
+        return PrefixStep(device, partition, int(name[len("prefix_bs"):]))
+    raise ValueError(name)
+
+
+def traffic_from_profile(name: str, kernel_hash: str):
+    """dram bytes per decode launch from the committed ncu summary of this
+    workload, if it was taken on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", f"pa_decode_{name}.md")
     try:
         text = open(path).read()
     except OSError:
-        return None
+        return None, None
     m = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)\s+source_hash:\s*([0-9a-f]+)", text)
     if m and m.group(2) == kernel_hash:
-        return int(m.group(1))
-    return None
+        return int(m.group(1)), os.path.relpath(path, ROOT)
+    return None, None
 
 
 def kernel_source_hash() -> str:
@@ -238,31 +461,6 @@ def kernel_source_hash() -> str:
 
 
 # ---------------------------------------------------------------------------
-# CPU oracle timing
-
-
-def time_oracle(inp, slots, budget_s: float, threads: int, full_first: bool = True):
-    """Run the oracle step (decode of all (seq, head) rows + append) on host
-    copies; repeat while within budget.  Returns (seconds per step, reps, rows)."""
-    import oracle
-    s = inp.shape
-    q, k, v = inp.q.cpu(), inp.k_cache.cpu(), inp.v_cache.cpu()
-    bt, cl = inp.block_tables.cpu(), inp.context_lens.cpu()
-    kn, vn = inp.k_new.cpu(), inp.v_new.cpu()
-    scale = 1.0 / math.sqrt(s.head_dim)
-    times = []
-    t_start = time.perf_counter()
-    while True:
-        t0 = time.perf_counter()
-        oracle.paged_attention(q, k, v, bt, cl, num_kv_heads=s.num_kv_heads, scale=scale, threads=threads)
-        oracle.append_kv(k, v, kn, vn, slots)
-        times.append(time.perf_counter() - t0)
-        if time.perf_counter() - t_start + times[-1] > budget_s or len(times) >= 20:
-            break
-    return statistics.median(times), len(times), s.num_seqs * s.num_heads
-
-
-# ---------------------------------------------------------------------------
 # arms
 
 
@@ -273,36 +471,14 @@ def run_native(args):
         raise SystemExit("bench.py needs a CUDA GPU for the native arm")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    from paged_kv_cache_251_gb300 import pa
-
-    inp, slots_h = build_workload(args.workload, dev)
-    s = inp.shape
-    bt = inp.block_tables.to(dev)
-    cl = inp.context_lens.to(dev)
-    slots = slots_h.to(dev)
-    out = torch.empty(inp.q.shape, dtype=torch.float32, device=dev)
-    ws = pa.workspace_for(inp.q, s.block_size, bt.shape[1], s.window, args.partition)
-    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    st = make_step(args.workload, dev, args.partition)
+    s = st.shape
     stream = torch.cuda.current_stream(dev)
-    scale = 1.0 / math.sqrt(s.head_dim)
-    dec_b, app_b = step_bytes(inp)
-    kv_bytes = dec_b["kv"]
-    max_parts_gt1 = pa.pa_decode_workspace_size(s.num_seqs, s.num_heads, s.head_dim, s.block_size, bt.shape[1],
-                                                s.window, args.partition) > 0
-    launches_per_step = (2 if max_parts_gt1 else 1) + 1
-
-    def decode():
-        pa.pa_decode(out, inp.q, inp.k_cache, inp.v_cache, bt, cl, num_kv_heads=s.num_kv_heads, scale=scale,
-                     window=s.window, partition_size=args.partition, workspace=ws, err_word=err, stream=stream)
-
-    def append():
-        pa.pa_append_kv(inp.k_new, inp.v_new, slots, inp.k_cache, inp.v_cache, err_word=err, stream=stream)
 
     for _ in range(max(args.warmup, 0)):
-        decode()
-        append()
+        st.run(stream)
     torch.cuda.synchronize(dev)
-    assert err.item() == 0, f"device error word {err.item()}"
+    assert st.err.item() == 0, f"device error word {st.err.item()}"
 
     K = args.steps
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -313,10 +489,7 @@ def run_native(args):
     with ClockSampler(local) as clocks:
         ev0.record(stream)
         for i in range(K):
-            ds[i].record(stream)
-            decode()
-            de[i].record(stream)
-            append()
+            st.run(stream, (ds[i], de[i]))
         ev1.record(stream)
         torch.cuda.synchronize(dev)
     barrier(world)
@@ -324,7 +497,7 @@ def run_native(args):
     ms_step = ev0.elapsed_time(ev1) / K
     ms_dec = statistics.mean(ds[i].elapsed_time(de[i]) for i in range(K))
     ms_step_max = max_over_ranks(ms_step, world, dev)
-    assert err.item() == 0, f"device error word {err.item()}"
+    assert st.err.item() == 0, f"device error word {st.err.item()}"
 
     # spot parity of the benchmarked output against the oracle
     parity = None
@@ -333,39 +506,27 @@ def run_native(args):
         from paged_kv_cache_251_gb300 import workloads as wl
         idx = wl.permutation(4242, 1, s.num_seqs * s.num_heads)[:16]
         pairs = torch.stack([idx // s.num_heads, idx % s.num_heads], 1).to(torch.int32)
-        # the cache now also holds the appended token; the decode attended L tokens
-        ref = oracle.paged_attention(inp.q.cpu(), inp.k_cache.cpu(), inp.v_cache.cpu(), inp.block_tables,
-                                     inp.context_lens, num_kv_heads=s.num_kv_heads, scale=scale, pairs=pairs,
+        ref = oracle.paged_attention(st.q.cpu(), st.k_cache.cpu(), st.v_cache.cpu(), st.inp.block_tables,
+                                     st.inp.context_lens, num_kv_heads=s.num_kv_heads,
+                                     scale=1.0 / math.sqrt(s.head_dim), window=st.window, pairs=pairs,
                                      threads=os.cpu_count() or 1)
-        got = out.cpu()[pairs[:, 0].long(), pairs[:, 1].long()].double().numpy()
+        got = st.out.cpu()[pairs[:, 0].long(), pairs[:, 1].long()].double().numpy()
         parity = float(abs(got - ref).max())
 
     # end to end through the public API with host buffers
-    pin = lambda t: t.cpu().pin_memory()  # noqa: E731
-    q_h, kn_h, vn_h = pin(inp.q), pin(inp.k_new), pin(inp.v_new)
-    sl_h, cl_h, bt_h = pin(slots_h), pin(inp.context_lens), pin(inp.block_tables)
-    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    q_d, kn_d, vn_d = torch.empty_like(inp.q), torch.empty_like(inp.k_new), torch.empty_like(inp.v_new)
-    sl_d, cl_d, bt_d = torch.empty_like(slots), torch.empty_like(cl), torch.empty_like(bt)
-    h2d = sum(t.numel() * t.element_size() for t in (q_h, kn_h, vn_h, sl_h, cl_h, bt_h))
-    d2h = out_h.numel() * out_h.element_size()
-
-    def e2e_step():
-        for dst, src in ((q_d, q_h), (kn_d, kn_h), (vn_d, vn_h), (sl_d, sl_h), (cl_d, cl_h), (bt_d, bt_h)):
-            dst.copy_(src, non_blocking=True)
-        pa.pa_decode(out, q_d, inp.k_cache, inp.v_cache, bt_d, cl_d, num_kv_heads=s.num_kv_heads, scale=scale,
-                     window=s.window, partition_size=args.partition, workspace=ws, err_word=err, stream=stream)
-        pa.pa_append_kv(kn_d, vn_d, sl_d, inp.k_cache, inp.v_cache, err_word=err, stream=stream)
-        out_h.copy_(out, non_blocking=True)
-
+    st.host_pinned = {k: v.cpu().pin_memory() for k, v in st.host.items()}
+    dev_in = {k: torch.empty(v.shape, dtype=v.dtype, device=dev) for k, v in st.host.items()}
+    st.out_host = torch.empty(st.out.shape, dtype=st.out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in st.host_pinned.values())
+    d2h = st.out_host.numel() * st.out_host.element_size()
     for _ in range(max(args.warmup, 0)):
-        e2e_step()
+        st.e2e(stream, dev_in)
     torch.cuda.synchronize(dev)
     barrier(world)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(K):
-        e2e_step()
+        st.e2e(stream, dev_in)
     e1.record(stream)
     torch.cuda.synchronize(dev)
     barrier(world)
@@ -374,17 +535,25 @@ def run_native(args):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         threads = os.cpu_count() or 1
-        t_step, reps, rows = time_oracle(inp, slots_h, args.cpu_seconds, threads)
-        cpu = {"value": kv_bytes / t_step / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
-               "sample": f"the full step ({rows} (seq, head) rows of fp64 decode + the append), "
-                         f"median of {reps} runs on {threads} host threads",
+        times, reps, kv_done = [], 0, 0
+        t_start = time.perf_counter()
+        while True:
+            t0 = time.perf_counter()
+            kv_done = st.oracle_step(threads)
+            times.append(time.perf_counter() - t0)
+            if time.perf_counter() - t_start + times[-1] > args.cpu_seconds or len(times) >= 20:
+                break
+        t_step = statistics.median(times)
+        cpu = {"value": kv_done / t_step / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+               "sample": f"the full step ({s.num_seqs * s.num_heads} (seq, head) rows of fp64 decode plus the "
+                         f"cache ops), median of {len(times)} runs on {threads} host threads",
                "seconds_per_step": t_step}
 
     peak, peak_kind = hbm_peak()
-    achieved = dec_b["total"] / (ms_dec * 1e-3) / 1e9
+    achieved = st.roof_bytes / (ms_dec * 1e-3) / 1e9
     khash = kernel_source_hash()
-    traffic = traffic_from_profile(khash)
-    value = world * kv_bytes / (ms_step_max * 1e-3) / 1e9
+    traffic, traffic_src = traffic_from_profile(args.workload, khash)
+    value = world * st.kv_bytes / (ms_step_max * 1e-3) / 1e9
     line = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -399,16 +568,12 @@ def run_native(args):
         "dtype": {torch.float16: "f16", torch.bfloat16: "bf16", torch.float32: "f32"}[s.dtype],
         "data": "synthetic (seeded SplitMix64 / Box-Muller N(0,1) q, K, V; seeded shuffle of the block pool)",
         "config": {
-            "workload": ("opt13b: 64 seqs x 40 MHA heads, head_dim 128, block 16, fp16, context ~ U[512, 2048], "
-                         "exact-need pool shuffled; step = pa_decode + pa_append_kv (1 token/seq)"
-                         if args.workload == "opt13b" else
-                         "gqa: 256 seqs, 32 q / 8 kv heads, head_dim 128, block 16, bf16, lognormal context "
-                         "(median 1024, sigma 1) clipped to [16, 8192], 95%-full shuffled pool; "
-                         "step = pa_decode + pa_append_kv"),
+            "workload": st.description,
             "num_seqs": s.num_seqs, "num_heads": s.num_heads, "num_kv_heads": s.num_kv_heads,
-            "head_dim": s.head_dim, "block_size": s.block_size, "context_tokens": dec_b["attended_tokens"],
-            "partition_size": args.partition or 512, "accumulate": "f32", "out_dtype": "f32",
-            "l2": f"no flush: the K/V read per step ({kv_bytes / 1e9:.2f} GB) is larger than L2 (129 MB)",
+            "head_dim": s.head_dim, "block_size": s.block_size, "window": st.window,
+            "context_tokens": st.dec_bytes["attended_tokens"],
+            "partition_size": st.partition or 512, "accumulate": "f32", "out_dtype": "f32",
+            "l2": f"no flush: the K/V read per step ({st.kv_bytes / 1e9:.2f} GB) is larger than L2 (129 MB)",
             "parallelism": f"replicas x{world} (each rank its own batch)",
         },
         "seq_layer_steps_per_s": round(world * s.num_seqs / (ms_step_max * 1e-3), 1),
@@ -417,18 +582,20 @@ def run_native(args):
         "roofline": {"bound": "hbm", "kernel": "pa_decode (decode + partition reduce)",
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_kind": f"{peak_kind} (hbm_gbs, STREAM-style copy)",
-                     "algorithmic_bytes_per_launch": dec_b["total"], "traffic": traffic,
-                     "traffic_source": "profiles/pa_decode_opt13b.md" if traffic else None,
-                     "source_hash": khash},
+                     "algorithmic_bytes_per_launch": st.roof_bytes, "traffic": traffic,
+                     "traffic_source": traffic_src, "source_hash": khash},
         "cpu_baseline": cpu,
-        "e2e": {"value": round(world * kv_bytes / (ms_e2e * 1e-3) / 1e9, 2), "unit": "GB/s",
+        "e2e": {"value": round(world * st.kv_bytes / (ms_e2e * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms_e2e, 5),
                 "api": "paged_kv_cache_251_gb300.pa (ctypes binding of libpa)"},
-        "gpu_launches": K * launches_per_step,
+        "gpu_launches": K * st.launches,
         "clocks": clk,
         "parity_sampled_max_abs": parity,
         "impl": "native",
     }
+    if hasattr(st, "unique_kv"):
+        line["config"]["unique_kv_bytes"] = st.unique_kv
+        line["roofline"]["bytes_note"] = "unique K/V bytes (each shared prompt block counted once)"
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -439,45 +606,33 @@ def run_reference(args):
     world, rank, _ = dist_env()
     if rank != 0:
         return  # the reference arm runs on rank 0 only
-    from paged_kv_cache_251_gb300 import workloads as wl
-    import oracle
-    s = wl.SHAPES[args.workload]
-    if args.workload == "opt13b":
-        inp = wl.decode_inputs(s)
-    else:
-        inp = wl.decode_inputs(s, room_for_append=True, fill=0.95)
+    st = make_step(args.workload, "cpu", args.partition)
+    s = st.shape
     threads = os.cpu_count() or 1
-    scale = 1.0 / math.sqrt(s.head_dim)
     # size the per-step sample so the whole run stays within a few minutes
     total_steps = max(1, args.steps + args.warmup)
-    probe_n = min(4, s.num_seqs)
+    probe = min(2, s.num_seqs)
     t0 = time.perf_counter()
-    oracle.paged_attention(inp.q[:probe_n], inp.k_cache, inp.v_cache, inp.block_tables[:probe_n],
-                           inp.context_lens[:probe_n], num_kv_heads=s.num_kv_heads, scale=scale, threads=threads)
-    per_seq = (time.perf_counter() - t0) / probe_n
+    st.oracle_step(threads, rows=probe)
+    per_seq = (time.perf_counter() - t0) / probe
     budget = 150.0 / total_steps
     n = max(1, min(s.num_seqs, int(budget / max(per_seq, 1e-9))))
-    q, bt, cl = inp.q[:n].contiguous(), inp.block_tables[:n].contiguous(), inp.context_lens[:n].contiguous()
-    dec_b, _ = step_bytes(inp)
-    from paged_kv_cache_251_gb300 import accounting as acc
-    elt = inp.k_cache.element_size()
-    kv = acc.decode_bytes(cl, s.num_heads, s.num_kv_heads, s.head_dim, s.block_size, elt)["kv"]
     for _ in range(args.warmup):
-        oracle.paged_attention(q, inp.k_cache, inp.v_cache, bt, cl, num_kv_heads=s.num_kv_heads, scale=scale,
-                               threads=threads)
-    t0 = time.perf_counter()
+        st.oracle_step(threads, rows=n)
+    times, kv = [], 0
     for _ in range(args.steps):
-        oracle.paged_attention(q, inp.k_cache, inp.v_cache, bt, cl, num_kv_heads=s.num_kv_heads, scale=scale,
-                               threads=threads)
-    dt = (time.perf_counter() - t0) / max(args.steps, 1)
+        t0 = time.perf_counter()
+        kv = st.oracle_step(threads, rows=n)
+        times.append(time.perf_counter() - t0)
+    dt = statistics.mean(times) if times else float("nan")
     value = kv / dt / 1e9
-    sample = (f"{n} of {s.num_seqs} sequences ({n * s.num_heads} (seq, head) rows, {int(cl.sum())} context tokens) "
-              f"per step, fp64 oracle on {threads} host threads")
+    sample = (f"{n} of {s.num_seqs} sequences ({n * s.num_heads} (seq, head) rows) of fp64 decode plus the step's "
+              f"cache ops per step, on {threads} host threads")
     line = {
         "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (same seeded workload as the native arm)",
-        "config": {"workload": args.workload, "num_seqs_sampled": n, "num_heads": s.num_heads,
+        "config": {"workload": st.description, "num_seqs_sampled": n, "num_heads": s.num_heads,
                    "num_kv_heads": s.num_kv_heads, "head_dim": s.head_dim, "block_size": s.block_size},
         "impl": "reference",
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
