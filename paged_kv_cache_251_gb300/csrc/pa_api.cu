@@ -15,6 +15,7 @@
 
 #include "pa.h"
 #include "pa_decode.cuh"
+#include "pa_decode_gqa.cuh"
 #include "pa_decode_mha.cuh"
 #include "pa_internal.h"
 
@@ -138,8 +139,30 @@ pa_status kv_tensor_map(CUtensorMap *map, const void *base, int dtype, int head_
     return PA_OK;
 }
 
+// 2-D view of q [num_seqs * num_heads][head_dim] with a box of one 128-byte
+// row segment x `group` rows (the query heads of one kv head), 128-byte swizzle.
+pa_status q_tensor_map(CUtensorMap *map, const void *base, int dtype, int head_dim, long long rows, int group) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
+    cudaError_t e = tensor_map_encoder(&enc);
+    if (e != cudaSuccess || !enc)
+        return cuda_fail(e == cudaSuccess ? cudaErrorSymbolNotFound : e, "cuTensorMapEncodeTiled lookup");
+    const int elt = elt_bytes(dtype);
+    const CUtensorMapDataType dt = dtype == PA_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(head_dim) * elt};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / elt), static_cast<cuuint32_t>(group)};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, dt, 2, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(PA_ERR_INVALID_ARGUMENT,
+                    "cuTensorMapEncodeTiled rejected the query layout (code " + std::to_string(static_cast<int>(r)) + ")");
+    return PA_OK;
+}
+
 constexpr int kDefaultPartition = 512;
 constexpr int kMhaStageBudget = 64 * 1024;
+constexpr int kGqaStages = 3;
 constexpr int kStageBudget = 48 * 1024;
 
 struct DecodePlan {
@@ -259,11 +282,26 @@ pa_status pa_decode(void *out, const void *q, const void *k_cache, const void *v
     // MHA takes the TMA-tensor kernel; its 3-D tensor map addresses tiles with
     // a 32-bit coordinate, so very large pools use the general kernel.
     const bool mha = (G == 1 && tiles <= INT_MAX);
+    // Grouped heads with 16-bit K/V and head_dim 128 take the tensor-core kernel.
+    const bool gqa_tc = (G > 1 && head_dim == 128 && dtype != PA_F32 && tiles <= INT_MAX &&
+                         static_cast<long long>(num_seqs) * num_heads <= INT_MAX);
     const void *fn;
     size_t smem;
     int threads;
-    CUtensorMap tmk, tmv;
-    if (mha) {
+    CUtensorMap tmk, tmv, tmq;
+    if (gqa_tc) {
+        fn = dtype == PA_F16 ? decode_gqa_kernel_f16(block_size, G) : decode_gqa_kernel_bf16(block_size, G);
+        p.stages = kGqaStages;
+        smem = gqa_smem_layout(kGqaStages).total;
+        threads = kGqaThreads;
+        pa_status ts = kv_tensor_map(&tmk, k_cache, dtype, head_dim, block_size, tiles);
+        if (ts == PA_OK)
+            ts = kv_tensor_map(&tmv, v_cache, dtype, head_dim, block_size, tiles);
+        if (ts == PA_OK)
+            ts = q_tensor_map(&tmq, q, dtype, head_dim, static_cast<long long>(num_seqs) * num_heads, G);
+        if (ts != PA_OK)
+            return ts;
+    } else if (mha) {
         fn = dtype == PA_F32   ? decode_mha_kernel_f32(head_dim, block_size)
              : dtype == PA_F16 ? decode_mha_kernel_f16(head_dim, block_size)
                                : decode_mha_kernel_bf16(head_dim, block_size);
@@ -307,9 +345,11 @@ pa_status pa_decode(void *out, const void *q, const void *k_cache, const void *v
     if (grid < 1)
         grid = 1;
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    void *args_gqa[] = {&p, &tmk, &tmv, &tmq};
     void *args_mha[] = {&p, &tmk, &tmv};
     void *args[] = {&p};
-    e = cudaLaunchKernel(fn, dim3(static_cast<unsigned>(grid)), dim3(threads), mha ? args_mha : args, smem, cs);
+    e = cudaLaunchKernel(fn, dim3(static_cast<unsigned>(grid)), dim3(threads),
+                         gqa_tc ? args_gqa : (mha ? args_mha : args), smem, cs);
     if (e != cudaSuccess)
         return cuda_fail(e, "decode launch");
     if (plan.max_parts > 1) {

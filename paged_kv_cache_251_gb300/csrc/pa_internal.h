@@ -21,6 +21,11 @@ const void *decode_mha_kernel_f32(int head_dim, int block_size);
 const void *decode_mha_kernel_f16(int head_dim, int block_size);
 const void *decode_mha_kernel_bf16(int head_dim, int block_size);
 
+// Tensor-core (tcgen05) decode kernels for grouped-query heads: 16-bit K/V,
+// head_dim 128, per block size and group 2/4/8; nullptr if not built.
+const void *decode_gqa_kernel_f16(int block_size, int group);
+const void *decode_gqa_kernel_bf16(int block_size, int group);
+
 cudaError_t launch_append(const void *k, const void *v, const int64_t *slots, void *k_cache, void *v_cache,
                           int num_tokens, int num_kv_heads, int row_bytes, int block_size, int num_blocks,
                           uint32_t *err, int num_sms, cudaStream_t stream);

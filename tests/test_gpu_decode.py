@@ -31,6 +31,11 @@ EDGE_CASES = [
     ("mha_bs16_parts", 3, 5, 5, 128, 16, [2000, 100, 513], 0, 64),
     ("mha_window", 3, 4, 4, 128, 16, [1000, 20, 777], 100, 0),
     ("mha_empty", 3, 2, 2, 64, 8, [0, 5, 0], 0, 0),
+    # grouped heads, head_dim 128 (the tensor-core kernel for 16-bit K/V)
+    ("tc_g2_bs32", 4, 4, 2, 128, 32, [129, 31, 1000, 257], 0, 0),
+    ("tc_g4_parts", 3, 8, 2, 128, 16, [700, 129, 2049], 0, 64),
+    ("tc_g8_bs8_window", 3, 16, 2, 128, 8, [5000, 77, 1300], 1000, 0),
+    ("tc_empty", 3, 8, 1, 128, 8, [0, 300, 0], 0, 0),
 ]
 
 
@@ -62,9 +67,9 @@ def test_tiny_config():
     compare(got, oracle_decode(inp), torch.float32)
 
 
-@pytest.mark.parametrize("hkv", [4, 2])
-def test_invalid_table_entries_are_skipped_and_flagged(hkv):
-    sh = shape("bad", 3, 4, hkv, 64, 16, torch.float16, seed=8)
+@pytest.mark.parametrize("hkv,d", [(4, 64), (2, 64), (2, 128)])
+def test_invalid_table_entries_are_skipped_and_flagged(hkv, d):
+    sh = shape("bad", 3, 4, hkv, d, 16, torch.float16, seed=8)
     inp = make_inputs(sh, [70, 40, 33])
     bt = inp.block_tables.clone()
     bt[0, 1] = inp.num_blocks + 5        # out of the pool
