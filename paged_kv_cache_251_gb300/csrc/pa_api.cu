@@ -139,6 +139,29 @@ pa_status kv_tensor_map(CUtensorMap *map, const void *base, int dtype, int head_
     return PA_OK;
 }
 
+// 5-D view of a 16-bit K or V cache with head_dim 128 for the tensor-core
+// kernel: [tile = block * H_kv + head][row / 8][half][row % 8][64 elements];
+// one box is a whole (block, head) tile and lands in shared memory as 8-row
+// groups of both 128-byte halves (128-byte swizzle).
+pa_status kv_tensor_map_groups(CUtensorMap *map, const void *base, int dtype, int block_size, long long tiles) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
+    cudaError_t e = tensor_map_encoder(&enc);
+    if (e != cudaSuccess || !enc)
+        return cuda_fail(e == cudaSuccess ? cudaErrorSymbolNotFound : e, "cuTensorMapEncodeTiled lookup");
+    const CUtensorMapDataType dt = dtype == PA_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const cuuint64_t row = 256;  // bytes per token row (128 x 2 bytes)
+    cuuint64_t dims[5] = {64, 8, 2, static_cast<cuuint64_t>(block_size / 8), static_cast<cuuint64_t>(tiles)};
+    cuuint64_t strides[4] = {row, 128, 8 * row, row * block_size};
+    cuuint32_t box[5] = {64, 8, 2, static_cast<cuuint32_t>(block_size / 8), 1};
+    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    CUresult r = enc(map, dt, 5, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(PA_ERR_INVALID_ARGUMENT, "cuTensorMapEncodeTiled rejected the grouped cache view (code " +
+                                                 std::to_string(static_cast<int>(r)) + ")");
+    return PA_OK;
+}
+
 // 2-D view of q [num_seqs * num_heads][head_dim] with a box of one 128-byte
 // row segment x `group` rows (the query heads of one kv head), 128-byte swizzle.
 pa_status q_tensor_map(CUtensorMap *map, const void *base, int dtype, int head_dim, long long rows, int group) {
@@ -294,9 +317,9 @@ pa_status pa_decode(void *out, const void *q, const void *k_cache, const void *v
         p.stages = kGqaStages;
         smem = gqa_smem_layout(kGqaStages).total;
         threads = kGqaThreads;
-        pa_status ts = kv_tensor_map(&tmk, k_cache, dtype, head_dim, block_size, tiles);
+        pa_status ts = kv_tensor_map_groups(&tmk, k_cache, dtype, block_size, tiles);
         if (ts == PA_OK)
-            ts = kv_tensor_map(&tmv, v_cache, dtype, head_dim, block_size, tiles);
+            ts = kv_tensor_map_groups(&tmv, v_cache, dtype, block_size, tiles);
         if (ts == PA_OK)
             ts = q_tensor_map(&tmq, q, dtype, head_dim, static_cast<long long>(num_seqs) * num_heads, G);
         if (ts != PA_OK)

@@ -19,8 +19,9 @@
 // (sequence, kv head, partition)):
 //   warp 0      producer: item ring (+ the item's G query rows by TMA),
 //               block-table slice into shared memory (range-checked), K and V
-//               of each 128-token tile by 3-D TMA tensor copies (128-byte
-//               swizzle) into a ring of stages;
+//               of each 128-token tile by 5-D TMA tensor copies (one per block
+//               and operand, issued by one lane per block; 128-byte swizzle)
+//               into a ring of stages;
 //   warp 1      tensor-memory allocation and the single thread that issues
 //               the MMAs and their commits; tile g's S = K . Q^T is issued
 //               before tile g-1's P V, so scoring overlaps the P V product;
@@ -51,9 +52,12 @@ template <typename T, int BS, int G> struct GqaCfg {
     static constexpr int kElt = 2;
     static constexpr int kRow = kD * kElt;               // 256 bytes
     static constexpr int kBpt = kTileTokens / BS;        // blocks per tile
-    static constexpr int kBoxBytes = kTileTokens * 128;  // one 64-column box of a 128-token tile
-    static constexpr int kTile = 2 * kBoxBytes;          // K (or V) of one tile: 32 KB
-    static constexpr int kBlockBox = BS * 128;           // one block's rows inside a box
+    // K (or V) of one tile: [token / 8][half of head_dim][token % 8][128 B],
+    // i.e. 8-row groups of 2 KB, each holding both 64-column halves
+    static constexpr int kGroupBytes = 2048;
+    static constexpr int kHalfBytes = 1024;
+    static constexpr int kTile = kTileTokens / 8 * kGroupBytes;  // 32 KB
+    static constexpr int kBlockBytes = BS * kRow;                // one block: all rows, both halves
     static constexpr int kOpBytes = 2 * 16 * 128;        // Q or P operand: 2 boxes x 16 rows x 128 B
     static_assert(sizeof(T) == 2, "tensor-core path takes 16-bit K/V");
     static_assert(G == 2 || G == 4 || G == 8, "query group");
@@ -179,6 +183,17 @@ template <> __device__ inline void tmem_ld<16>(uint32_t taddr, float *v) {
         v[i] = __uint_as_float(r[i]);
 }
 __device__ inline void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// One block of one kv head through the 5-D view [tile][row / 8][half][row % 8][64]
+// (box = the whole block), landing as 8-row groups of both halves.
+__device__ inline void tma_load_5d(void *dst, const CUtensorMap *map, int z, uint64_t *bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint "
+        "[%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(0), "r"(0), "r"(0), "r"(z), "r"(smem_addr(bar)),
+        "l"(policy)
+        : "memory");
+}
 
 __device__ inline void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y, uint64_t *bar) {
     asm volatile(
@@ -345,33 +360,23 @@ __device__ inline void gqa_producer(const DecodeParams &p, const CUtensorMap *tm
                 ok = false;
                 break;
             }
+            // lane j issues block j of the tile: one copy for K, one for V
+            const int bj = ti * C::kBpt + lane;
+            const bool mine = lane < C::kBpt && bj < nb && tbl[bj] >= 0;
+            const uint32_t mask = __ballot_sync(0xffffffffu, mine);
             if (lane == 0) {
-                uint32_t mask = 0;
-                for (int j = 0; j < C::kBpt; ++j) {
-                    const int b = ti * C::kBpt + j;
-                    if (b < nb && tbl[b] >= 0)
-                        mask |= 1u << j;
-                }
                 meta[stage] = mask;
-                if (mask) {
-                    mbar_arrive_expect_tx(&full[stage], __popc(mask) * 4 * C::kBlockBox);
-                    char *dk = stage_buf + static_cast<size_t>(stage) * 2 * C::kTile;
-                    char *dv = dk + C::kTile;
-                    for (int j = 0; j < C::kBpt; ++j) {
-                        if (!(mask >> j & 1u))
-                            continue;
-                        const int z = tbl[ti * C::kBpt + j] * p.num_kv_heads + kvh;
-#pragma unroll
-                        for (int bx = 0; bx < 2; ++bx) {
-                            tma_load_3d(dk + bx * C::kBoxBytes + j * C::kBlockBox, tmk, bx * 64, 0, z, &full[stage],
-                                        policy);
-                            tma_load_3d(dv + bx * C::kBoxBytes + j * C::kBlockBox, tmv, bx * 64, 0, z, &full[stage],
-                                        policy);
-                        }
-                    }
-                } else {
+                if (mask)
+                    mbar_arrive_expect_tx(&full[stage], __popc(mask) * 2 * C::kBlockBytes);
+                else
                     mbar_arrive(&full[stage]);
-                }
+            }
+            __syncwarp();
+            if (mine) {
+                char *dk = stage_buf + static_cast<size_t>(stage) * 2 * C::kTile + lane * C::kBlockBytes;
+                const int z = tbl[bj] * p.num_kv_heads + kvh;
+                tma_load_5d(dk, tmk, z, &full[stage], policy);
+                tma_load_5d(dk + C::kTile, tmv, z, &full[stage], policy);
             }
             __syncwarp();
         }
@@ -427,7 +432,10 @@ __device__ inline bool gqa_mma(const DecodeParams &p, char *smem, const GqaLayou
 #pragma unroll
             for (int kk = 0; kk < 2; ++kk) {
                 const int t0 = 32 * w + 16 * kk;  // first token of this K step
-                const uint64_t ad = sdesc(vt + t0 * 128, C::kBoxBytes, 1024);
+                // V^T, MN-major: head_dim halves C::kHalfBytes apart, 8-token groups
+                // C::kGroupBytes apart (read either way round, every address stays
+                // inside this tile)
+                const uint64_t ad = sdesc(vt + (t0 >> 3) * C::kGroupBytes, C::kHalfBytes, C::kGroupBytes);
                 const uint64_t bd = sdesc(pb + (t0 >> 6) * 16 * 128 + (t0 & 63) * 2, 16, 1024);
                 tc_mma(tmem + 32 + b * 64 + w * 16, ad, bd, kIdPV, kk > 0);
             }
@@ -465,7 +473,7 @@ __device__ inline bool gqa_mma(const DecodeParams &p, char *smem, const GqaLayou
             // S = K . Q^T: A = K tile (K-major), B = Q (K-major); 8 steps of 16 along head_dim
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
-                const uint64_t ad = sdesc(kt + (kk >> 2) * C::kBoxBytes + (kk & 3) * 32, 16, 1024);
+                const uint64_t ad = sdesc(kt + (kk >> 2) * C::kHalfBytes + (kk & 3) * 32, 16, C::kGroupBytes);
                 const uint64_t bd = sdesc(qs + (kk >> 2) * 16 * 128 + (kk & 3) * 32, 16, 1024);
                 tc_mma(tmem + b * 16, ad, bd, kIdQK, kk > 0);
             }
@@ -692,7 +700,8 @@ __device__ inline bool gqa_softmax(const DecodeParams &p, char *smem, const GqaL
                 char *vt = stage_buf + static_cast<size_t>(stage) * 2 * C::kTile + C::kTile;
 #pragma unroll
                 for (int bx = 0; bx < 2; ++bx) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(vt + bx * C::kBoxBytes + row * 128);
+                    uint4 *dst = reinterpret_cast<uint4 *>(vt + (row >> 3) * C::kGroupBytes + bx * C::kHalfBytes +
+                                                           (row & 7) * 128);
 #pragma unroll
                     for (int c = 0; c < 8; ++c)
                         dst[c] = make_uint4(0, 0, 0, 0);
