@@ -377,7 +377,7 @@ pa_status pa_decode(void *out, const void *q, const void *k_cache, const void *v
         return cuda_fail(e, "decode launch");
     if (plan.max_parts > 1) {
         const long long rows = static_cast<long long>(num_seqs) * num_heads;
-        e = cudaLaunchKernel(reduce_kernel(head_dim), dim3(static_cast<unsigned>((rows + 3) / 4)), dim3(128), args, 0,
+        e = cudaLaunchKernel(reduce_kernel(head_dim), dim3(static_cast<unsigned>(rows)), dim3(kReduceThreads), args, 0,
                              cs);
         if (e != cudaSuccess)
             return cuda_fail(e, "reduce launch");

@@ -516,48 +516,98 @@ __global__ void __launch_bounds__(kDecodeThreads) pa_decode_kernel(const DecodeP
 
 // Merge the partitions of every multi-partition (sequence, head):
 //   M = max_p m_p,  out = sum_p 2^(m_p - M) acc_p / sum_p 2^(m_p - M) l_p
-// One warp per (sequence, head); single-partition rows were written by the
-// decode kernel and are left alone.
+// One CTA of kReduceThreads per (sequence, head) row: the (m, l) pairs are
+// read by all threads at once (block max and sum), then the warps take
+// partitions round-robin, each lane a contiguous slice of head_dim, and sum
+// their slices through shared memory.  Single-partition rows were written by
+// the decode kernel and are left alone.
+constexpr int kReduceThreads = 128;
+
 template <int D>
-__global__ void __launch_bounds__(128) pa_reduce_kernel(const DecodeParams p) {
-    const long long wid = static_cast<long long>(blockIdx.x) * 4 + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
-    if (wid >= static_cast<long long>(p.num_seqs) * p.num_heads)
-        return;
-    const int s = static_cast<int>(wid / p.num_heads);
+__global__ void __launch_bounds__(kReduceThreads) pa_reduce_kernel(const DecodeParams p) {
+    constexpr int kWarps = kReduceThreads / 32;
+    constexpr int kPer = D / 32;  // head_dim slice per lane (4 or 2)
+    __shared__ float red[kWarps];
+    __shared__ float accs[kWarps][D];
+    const long long rowi = blockIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int s = static_cast<int>(rowi / p.num_heads);
     const SeqSpan sp = seq_span(p.context_lens[s], p.max_len, p.window, p.block_size, p.bpp);
     if (sp.nparts <= 1)
         return;
-    const long long base = wid * p.max_parts;
-    const float *ml = p.part_ml + base * 2;
+    const int np = sp.nparts;
+    const long long base = rowi * p.max_parts;
+    const float2 *ml = reinterpret_cast<const float2 *>(p.part_ml + base * 2);
+
+    // row max over the partitions' running maxima
     float M = -INFINITY;
-    for (int q = lane; q < sp.nparts; q += 32)
-        M = fmaxf(M, ml[2 * q]);
+    for (int q = tid; q < np; q += kReduceThreads)
+        M = fmaxf(M, ml[q].x);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1)
         M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    constexpr int kPer = D / 32;
+    if (lane == 0)
+        red[warp] = M;
+    __syncthreads();
+    M = red[0];
+#pragma unroll
+    for (int w = 1; w < kWarps; ++w)
+        M = fmaxf(M, red[w]);
+    __syncthreads();
+
+    // denominator
+    float den = 0.f;
+    if (M != -INFINITY)
+        for (int q = tid; q < np; q += kReduceThreads) {
+            const float2 v = ml[q];
+            if (v.x != -INFINITY)
+                den = fmaf(v.y, exp2f(v.x - M), den);
+        }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        den += __shfl_xor_sync(0xffffffffu, den, o);
+    if (lane == 0)
+        red[warp] = den;
+
+    // numerator: warp w takes partitions w, w + kWarps, ...
     float num[kPer];
 #pragma unroll
     for (int i = 0; i < kPer; ++i)
         num[i] = 0.f;
-    float den = 0.f;
     if (M != -INFINITY) {
-        for (int q = 0; q < sp.nparts; ++q) {
-            const float mq = ml[2 * q];
-            if (mq == -INFINITY)
-                continue;
-            const float sc = exp2f(mq - M);
-            den = fmaf(ml[2 * q + 1], sc, den);
-            const float *a = p.part_acc + (base + q) * D;
+#pragma unroll 4
+        for (int q = warp; q < np; q += kWarps) {
+            const float mq = ml[q].x;
+            const float sc = mq == -INFINITY ? 0.f : exp2f(mq - M);
+            const float *a = p.part_acc + (base + q) * D + lane * kPer;
+            if (kPer == 4) {
+                const float4 v = *reinterpret_cast<const float4 *>(a);
+                num[0] = fmaf(v.x, sc, num[0]);
+                num[1] = fmaf(v.y, sc, num[1]);
+                num[2] = fmaf(v.z, sc, num[2]);
+                num[3] = fmaf(v.w, sc, num[3]);
+            } else {
 #pragma unroll
-            for (int i = 0; i < kPer; ++i)
-                num[i] = fmaf(a[lane + 32 * i], sc, num[i]);
+                for (int i = 0; i < kPer; ++i)
+                    num[i] = fmaf(a[i], sc, num[i]);
+            }
         }
     }
 #pragma unroll
     for (int i = 0; i < kPer; ++i)
-        store_out(p.out, p.out_dtype, wid * D + lane + 32 * i, den > 0.f ? num[i] / den : 0.f);
+        accs[warp][lane * kPer + i] = num[i];
+    __syncthreads();
+    float dsum = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w)
+        dsum += red[w];
+    for (int d = tid; d < D; d += kReduceThreads) {
+        float v = 0.f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w)
+            v += accs[w][d];
+        store_out(p.out, p.out_dtype, rowi * D + d, dsum > 0.f ? v / dsum : 0.f);
+    }
 }
 
 }  // namespace pa
