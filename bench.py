@@ -104,7 +104,8 @@ def hbm_peak():
 
 
 class ClockSampler:
-    """nvidia-smi clocks / throttle reasons sampled every 200 ms while active."""
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms while active
+    (the bench keeps the GPU busy with the timed step for the whole window)."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -484,9 +485,16 @@ def run_native(args):
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ds = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     de = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    barrier(world)
-    torch.cuda.synchronize(dev)
     with ClockSampler(local) as clocks:
+        # untimed soak of the same step (>= 0.6 s) so the 200 ms clock samples
+        # see the GPU under this load; the timed region follows immediately
+        t_soak = time.perf_counter()
+        while time.perf_counter() - t_soak < 0.6:
+            for _ in range(50):
+                st.run(stream)
+            torch.cuda.synchronize(dev)
+        barrier(world)
+        torch.cuda.synchronize(dev)
         ev0.record(stream)
         for i in range(K):
             st.run(stream, (ds[i], de[i]))
