@@ -54,6 +54,8 @@ def parse_args(argv=None):
     ap.add_argument("--workload", choices=["opt13b", "gqa", "window", "prefix_bs8", "prefix_bs16",
                                            "prefix_bs32"], default="opt13b")
     ap.add_argument("--partition", type=int, default=0, help="pa_decode partition_size (0 = default)")
+    ap.add_argument("--table", choices=["shuffled", "identity"], default="shuffled",
+                    help="block hand-out order (identity: each sequence's blocks adjacent in memory)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU baseline budget")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args(argv)
@@ -224,7 +226,7 @@ class DecodeAppendStep(Step):
     """pa_decode over every sequence's L tokens, then pa_append_kv of token L
     (the slot the host block manager assigns); idempotent step."""
 
-    def __init__(self, name, device, partition):
+    def __init__(self, name, device, partition, shuffle=True):
         super().__init__(device, partition)
         from paged_kv_cache_251_gb300 import pa
         from paged_kv_cache_251_gb300 import workloads as wl
@@ -232,11 +234,12 @@ class DecodeAppendStep(Step):
         self.pa = pa
         self.name = name
         if name == "opt13b":
-            inp = wl.decode_inputs(wl.SHAPES["opt13b"], device=device)
+            inp = wl.decode_inputs(wl.SHAPES["opt13b"], device=device, shuffle=shuffle)
             self.description = ("opt13b: 64 seqs x 40 MHA heads, head_dim 128, block 16, fp16, context ~ U[512, 2048], "
                                 "exact-need pool shuffled; step = pa_decode + pa_append_kv (1 token/seq)")
         else:
-            inp = wl.decode_inputs(wl.SHAPES["gqa"], device=device, room_for_append=True, fill=0.95)
+            inp = wl.decode_inputs(wl.SHAPES["gqa"], device=device, room_for_append=True, fill=0.95,
+                                   shuffle=shuffle)
             self.description = ("gqa: 256 seqs, 32 q / 8 kv heads, head_dim 128, block 16, bf16, lognormal context "
                                 "(median 1024, sigma 1) clipped to [16, 8192], 95%-full shuffled pool; "
                                 "step = pa_decode + pa_append_kv (1 token/seq)")
@@ -426,9 +429,9 @@ class PrefixStep(DecodeAppendStep):
 WORKLOADS = ["opt13b", "gqa", "window", "prefix_bs8", "prefix_bs16", "prefix_bs32"]
 
 
-def make_step(name, device, partition):
+def make_step(name, device, partition, table="shuffled"):
     if name in ("opt13b", "gqa"):
-        return DecodeAppendStep(name, device, partition)
+        return DecodeAppendStep(name, device, partition, shuffle=(table == "shuffled"))
     if name == "window":
         return WindowStep(device, partition)
     if name.startswith("prefix_bs"):
@@ -472,7 +475,7 @@ def run_native(args):
         raise SystemExit("bench.py needs a CUDA GPU for the native arm")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    st = make_step(args.workload, dev, args.partition)
+    st = make_step(args.workload, dev, args.partition, args.table)
     s = st.shape
     stream = torch.cuda.current_stream(dev)
 
@@ -581,6 +584,7 @@ def run_native(args):
             "head_dim": s.head_dim, "block_size": s.block_size, "window": st.window,
             "context_tokens": st.dec_bytes["attended_tokens"],
             "partition_size": st.partition or 512, "accumulate": "f32", "out_dtype": "f32",
+            "block_order": args.table,
             "l2": f"no flush: the K/V read per step ({st.kv_bytes / 1e9:.2f} GB) is larger than L2 (129 MB)",
             "parallelism": f"replicas x{world} (each rank its own batch)",
         },
@@ -614,7 +618,7 @@ def run_reference(args):
     world, rank, _ = dist_env()
     if rank != 0:
         return  # the reference arm runs on rank 0 only
-    st = make_step(args.workload, "cpu", args.partition)
+    st = make_step(args.workload, "cpu", args.partition, args.table)
     s = st.shape
     threads = os.cpu_count() or 1
     # size the per-step sample so the whole run stays within a few minutes

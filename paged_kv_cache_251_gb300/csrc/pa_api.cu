@@ -113,8 +113,10 @@ cudaError_t tensor_map_encoder(PFN_cuTensorMapEncodeTiled_v12000 *fn) {
     return g_encode_err;
 }
 
-// 3-D view of a K or V cache [num_blocks * H_kv][block_size][head_dim] with a
-// box of one 128-byte row segment x block_size rows, 128-byte swizzle.
+// 4-D view of a K or V cache [num_blocks * H_kv][block_size][head_dim] as
+// [tile][128-byte segment of the row][row][elements of the segment]; one box is
+// a whole (block, head) tile and lands in shared memory as one 128-byte-wide,
+// block_size-row box per segment (128-byte swizzle).
 pa_status kv_tensor_map(CUtensorMap *map, const void *base, int dtype, int head_dim, int block_size,
                         long long tiles) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
@@ -125,13 +127,14 @@ pa_status kv_tensor_map(CUtensorMap *map, const void *base, int dtype, int head_
     const CUtensorMapDataType dt = dtype == PA_F32   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
                                    : dtype == PA_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
                                                      : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-    cuuint64_t dims[3] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(block_size),
+    const cuuint64_t row = static_cast<cuuint64_t>(head_dim) * elt;
+    const cuuint32_t segs = static_cast<cuuint32_t>(row / 128);
+    cuuint64_t dims[4] = {static_cast<cuuint64_t>(128 / elt), static_cast<cuuint64_t>(block_size), segs,
                           static_cast<cuuint64_t>(tiles)};
-    cuuint64_t strides[2] = {static_cast<cuuint64_t>(head_dim) * elt,
-                             static_cast<cuuint64_t>(head_dim) * elt * block_size};
-    cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / elt), static_cast<cuuint32_t>(block_size), 1};
-    cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = enc(map, dt, 3, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+    cuuint64_t strides[3] = {row, 128, row * block_size};
+    cuuint32_t box[4] = {static_cast<cuuint32_t>(128 / elt), static_cast<cuuint32_t>(block_size), segs, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = enc(map, dt, 4, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS)
         return fail(PA_ERR_INVALID_ARGUMENT, "cuTensorMapEncodeTiled rejected the cache layout (code " +

@@ -7,8 +7,8 @@
 // 案例 2), split into context partitions merged by the log-sum-exp reduce.
 //
 // What differs is the data path, shaped for HBM bandwidth on sm_103a:
-//  - K and V tiles of one (block, kv head) arrive by 3-D TMA tensor copies
-//    (cp.async.bulk.tensor) in 128-byte-swizzled shared-memory layout: a tile
+//  - K and V tiles of one (block, kv head) arrive by one 4-D TMA tensor copy
+//    each (cp.async.bulk.tensor) in 128-byte-swizzled shared-memory layout: a tile
 //    row of d * elt bytes is split into 128-byte boxes whose 16-byte chunks
 //    are XOR-permuted by row, so both access patterns below are free of bank
 //    conflicts.
@@ -110,12 +110,14 @@ __host__ __device__ inline MhaLayout mha_smem_layout(int S, int tile_bytes, int 
 // ---------------------------------------------------------------------------
 // PTX helpers specific to this kernel
 
-__device__ inline void tma_load_3d(void *dst, const CUtensorMap *map, int x, int y, int z, uint64_t *bar,
-                                   uint64_t policy) {
+// One whole (block, head) tile through the 4-D view
+// [tile][128-byte segment][row][segment elements]: kBoxes boxes of block_size
+// rows x 128 bytes, back to back.
+__device__ inline void tma_load_4d(void *dst, const CUtensorMap *map, int z, uint64_t *bar, uint64_t policy) {
     asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint "
-        "[%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_addr(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_addr(bar)), "l"(policy)
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint "
+        "[%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(0), "r"(0), "r"(z), "r"(smem_addr(bar)), "l"(policy)
         : "memory");
 }
 
@@ -366,11 +368,8 @@ __device__ inline void mha_producer(const DecodeParams &p, const CUtensorMap *tm
                     char *dk = stage_buf + static_cast<size_t>(stage) * 2 * C::kTile;
                     char *dv = dk + C::kTile;
                     const int z = pb * p.num_kv_heads + kvh;
-#pragma unroll
-                    for (int b = 0; b < C::kBoxes; ++b) {
-                        tma_load_3d(dk + b * C::kBoxBytes, tmk, b * C::kBoxElems, 0, z, &full[stage], policy);
-                        tma_load_3d(dv + b * C::kBoxBytes, tmv, b * C::kBoxElems, 0, z, &full[stage], policy);
-                    }
+                    tma_load_4d(dk, tmk, z, &full[stage], policy);
+                    tma_load_4d(dv, tmv, z, &full[stage], policy);
                 } else {
                     mbar_arrive(&full[stage]);
                 }

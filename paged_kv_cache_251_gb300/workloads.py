@@ -175,9 +175,11 @@ def _ceil_div(a, b):
 
 
 def pool_and_tables(shape: Shape, lens: torch.Tensor, room_for_append: bool,
-                    num_blocks: int | None = None, fill: float = 1.0):
-    """Hand out a seeded shuffle of the pool's block ids, sequence by
-    sequence, each sequence taking the blocks its tokens occupy.
+                    num_blocks: int | None = None, fill: float = 1.0, shuffle: bool = True):
+    """Hand out a seeded shuffle of the pool's block ids (or, with
+    shuffle=False, the ids in order, so each sequence's blocks are adjacent in
+    memory), sequence by sequence, each sequence taking the blocks its tokens
+    occupy.
 
     Returns (block_tables int32 [N, M], blocks_held int32 [N], num_blocks).
     """
@@ -189,7 +191,8 @@ def pool_and_tables(shape: Shape, lens: torch.Tensor, room_for_append: bool,
         num_blocks = need if fill >= 1.0 else int(_ceil_div(need * 100, int(round(fill * 100))))
     if need > num_blocks:
         raise ValueError("pool too small for the requested lengths")
-    perm = permutation(shape.seed, _S_PERM, num_blocks).to(torch.int32)
+    perm = (permutation(shape.seed, _S_PERM, num_blocks) if shuffle
+            else torch.arange(num_blocks)).to(torch.int32)
     width = max(1, int(held.max()))
     tables = torch.full((shape.num_seqs, width), -1, dtype=torch.int32)
     at = 0
@@ -202,12 +205,12 @@ def pool_and_tables(shape: Shape, lens: torch.Tensor, room_for_append: bool,
 
 def decode_inputs(shape: Shape, device="cpu", lens: torch.Tensor | None = None,
                   room_for_append: bool = True, num_blocks: int | None = None,
-                  fill: float = 1.0, with_append: bool = True) -> DecodeInputs:
+                  fill: float = 1.0, with_append: bool = True, shuffle: bool = True) -> DecodeInputs:
     """Pool, tables, queries and K/V values for a decode (+ append) step."""
     s = shape
     if lens is None:
         lens = context_lengths(s)
-    tables, held, nb = pool_and_tables(s, lens, room_for_append, num_blocks, fill)
+    tables, held, nb = pool_and_tables(s, lens, room_for_append, num_blocks, fill, shuffle)
     kv_shape = (nb, s.num_kv_heads, s.block_size, s.head_dim)
     q = normal_tensor(s.seed, _S_Q, (s.num_seqs, s.num_heads, s.head_dim), device, s.dtype)
     k = normal_tensor(s.seed, _S_K, kv_shape, device, s.dtype)
