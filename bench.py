@@ -43,6 +43,7 @@ import torch  # noqa: E402
 METRIC = "paged decode attention KV GB/s (% of GB300 HBM peak) and seq-layer steps/s"
 FALLBACK_HBM_GBS = 6800.0
 L2_BYTES = 129 * 1024 * 1024
+L2_FLUSH_BYTES = 256 * 1024 * 1024
 
 
 def parse_args(argv=None):
@@ -52,7 +53,7 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--workload", choices=["opt13b", "gqa", "window", "prefix_bs8", "prefix_bs16",
-                                           "prefix_bs32"], default="opt13b")
+                                           "prefix_bs32", "tiny", "tiny_scaled"], default="opt13b")
     ap.add_argument("--partition", type=int, default=0, help="pa_decode partition_size (0 = default)")
     ap.add_argument("--table", choices=["shuffled", "identity"], default="shuffled",
                     help="block hand-out order (identity: each sequence's blocks adjacent in memory)")
@@ -233,7 +234,15 @@ class DecodeAppendStep(Step):
         from paged_kv_cache_251_gb300.blocks import BlockManager
         self.pa = pa
         self.name = name
-        if name == "opt13b":
+        if name == "tiny":
+            inp = wl.decode_inputs(wl.SHAPES["tiny"], device=device, num_blocks=64, shuffle=shuffle)
+            self.description = ("tiny: 4 seqs x 4 MHA heads, head_dim 64, block 16, fp32, context ~ U[1, 100], "
+                                "64-block pool shuffled; step = pa_decode + pa_append_kv (launch-bound by size)")
+        elif name == "tiny_scaled":
+            inp = wl.decode_inputs(wl.SHAPES["tiny_scaled"], device=device, shuffle=shuffle)
+            self.description = ("tiny_scaled: the tiny shape (4 MHA heads, head_dim 64, block 16, fp32) with 4096 "
+                                "seqs, context ~ U[1, 2048], exact-need pool shuffled; step = pa_decode + pa_append_kv")
+        elif name == "opt13b":
             inp = wl.decode_inputs(wl.SHAPES["opt13b"], device=device, shuffle=shuffle)
             self.description = ("opt13b: 64 seqs x 40 MHA heads, head_dim 128, block 16, fp16, context ~ U[512, 2048], "
                                 "exact-need pool shuffled; step = pa_decode + pa_append_kv (1 token/seq)")
@@ -426,11 +435,11 @@ class PrefixStep(DecodeAppendStep):
         return int(self.inp.context_lens[:n].to(torch.int64).sum()) * 2 * s.num_kv_heads * s.head_dim * _elt(s.dtype)
 
 
-WORKLOADS = ["opt13b", "gqa", "window", "prefix_bs8", "prefix_bs16", "prefix_bs32"]
+WORKLOADS = ["opt13b", "gqa", "window", "prefix_bs8", "prefix_bs16", "prefix_bs32", "tiny", "tiny_scaled"]
 
 
 def make_step(name, device, partition, table="shuffled"):
-    if name in ("opt13b", "gqa"):
+    if name in ("opt13b", "gqa", "tiny", "tiny_scaled"):
         return DecodeAppendStep(name, device, partition, shuffle=(table == "shuffled"))
     if name == "window":
         return WindowStep(device, partition)
@@ -488,6 +497,10 @@ def run_native(args):
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ds = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     de = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    es = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ee = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    flush = (torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+             if int(st.kv_bytes) < 2 * L2_BYTES else None)
     with ClockSampler(local) as clocks:
         # untimed soak of the same step (>= 0.6 s) so the 200 ms clock samples
         # see the GPU under this load; the timed region follows immediately
@@ -498,14 +511,26 @@ def run_native(args):
             torch.cuda.synchronize(dev)
         barrier(world)
         torch.cuda.synchronize(dev)
-        ev0.record(stream)
-        for i in range(K):
-            st.run(stream, (ds[i], de[i]))
-        ev1.record(stream)
+        if flush is None:
+            ev0.record(stream)
+            for i in range(K):
+                st.run(stream, (ds[i], de[i]))
+            ev1.record(stream)
+        else:
+            # the step's K/V would stay in L2: overwrite a buffer larger than L2
+            # before every step and time each step on its own
+            for i in range(K):
+                flush.add_(1)
+                es[i].record(stream)
+                st.run(stream, (ds[i], de[i]))
+                ee[i].record(stream)
         torch.cuda.synchronize(dev)
     barrier(world)
     clk = clocks.summary()
-    ms_step = ev0.elapsed_time(ev1) / K
+    if flush is None:
+        ms_step = ev0.elapsed_time(ev1) / K
+    else:
+        ms_step = statistics.mean(es[i].elapsed_time(ee[i]) for i in range(K))
     ms_dec = statistics.mean(ds[i].elapsed_time(de[i]) for i in range(K))
     ms_step_max = max_over_ranks(ms_step, world, dev)
     assert st.err.item() == 0, f"device error word {st.err.item()}"
@@ -585,7 +610,10 @@ def run_native(args):
             "context_tokens": st.dec_bytes["attended_tokens"],
             "partition_size": st.partition or 512, "accumulate": "f32", "out_dtype": "f32",
             "block_order": args.table,
-            "l2": f"no flush: the K/V read per step ({st.kv_bytes / 1e9:.2f} GB) is larger than L2 (129 MB)",
+            "l2": (f"no flush: the K/V read per step ({st.kv_bytes / 1e9:.2f} GB) is larger than L2 (129 MB)"
+                   if flush is None else
+                   f"L2 flushed before every timed step (a 256 MB buffer is overwritten); the K/V read per step "
+                   f"({st.kv_bytes / 1e6:.2f} MB) would otherwise stay in L2; steps timed one by one"),
             "parallelism": f"replicas x{world} (each rank its own batch)",
         },
         "seq_layer_steps_per_s": round(world * s.num_seqs / (ms_step_max * 1e-3), 1),

@@ -128,6 +128,8 @@ SHAPES = {
     "window": Shape("window", 4, 32, 8, 128, 16, torch.bfloat16, window=32768,
                     partition_size=512, seed=251004),
     "prefix": Shape("prefix", 256, 40, 40, 128, 16, torch.float16, seed=251005),
+    # the tiny shape scaled up so that it is not launch-bound: 4096 sequences
+    "tiny_scaled": Shape("tiny_scaled", 4096, 4, 4, 64, 16, torch.float32, seed=251006),
 }
 
 # streams
@@ -141,6 +143,8 @@ def context_lengths(shape: Shape) -> torch.Tensor:
         return randint(s.seed, _S_LENS, s.num_seqs, 1, 100).to(torch.int32)
     if s.name == "opt13b":
         return randint(s.seed, _S_LENS, s.num_seqs, 512, 2048).to(torch.int32)
+    if s.name == "tiny_scaled":
+        return randint(s.seed, _S_LENS, s.num_seqs, 1, 2048).to(torch.int32)
     if s.name == "gqa":
         g = normal(s.seed, _S_LENS, s.num_seqs, dtype=torch.float64)
         lens = torch.round(torch.exp(torch.log(torch.tensor(1024.0, dtype=torch.float64)) + g))

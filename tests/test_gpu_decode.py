@@ -111,11 +111,18 @@ def _sample_pairs(N, H, count, seed):
     return torch.stack([idx // H, idx % H], dim=1).to(torch.int32)
 
 
-@pytest.mark.parametrize("name", ["opt13b", "gqa"])
+@pytest.mark.parametrize("name", ["opt13b", "gqa", "tiny_scaled"])
 def test_full_size_config_sampled(name):
-    """Full-size workloads in the launch configuration the benchmark times;
-    every output is finite and a sample of rows matches the oracle."""
-    inp = wl.opt13b() if name == "opt13b" else wl.gqa()
+    """Full-size workloads in the launch configuration the benchmark times
+    (inputs generated on the GPU); every output is finite and a sample of rows
+    matches the oracle."""
+    if name == "opt13b":
+        inp = wl.decode_inputs(wl.SHAPES["opt13b"], device="cuda")
+    elif name == "gqa":
+        inp = wl.decode_inputs(wl.SHAPES["gqa"], device="cuda", room_for_append=False, fill=0.95,
+                               with_append=False)
+    else:
+        inp = wl.decode_inputs(wl.SHAPES["tiny_scaled"], device="cuda")
     got, err = run_decode(inp)
     assert err == 0
     s = inp.shape
