@@ -53,7 +53,7 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--workload", choices=["opt13b", "gqa", "window", "prefix_bs8", "prefix_bs16",
-                                           "prefix_bs32", "tiny", "tiny_scaled"], default="opt13b")
+                                           "prefix_bs32", "tiny", "tiny_scaled", "swap"], default="opt13b")
     ap.add_argument("--partition", type=int, default=0, help="pa_decode partition_size (0 = default)")
     ap.add_argument("--table", choices=["shuffled", "identity"], default="shuffled",
                     help="block hand-out order (identity: each sequence's blocks adjacent in memory)")
@@ -642,6 +642,52 @@ def run_native(args):
         torch.distributed.destroy_process_group()
 
 
+def run_swap(args):
+    """Block swap between HBM and pinned host memory (the OPT-13B pool's
+    blocks, 2048 of them = 655 MB of K+V, out to host and back in)."""
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    from paged_kv_cache_251_gb300 import pa
+    from paged_kv_cache_251_gb300 import workloads as wl
+    inp = wl.decode_inputs(wl.SHAPES["opt13b"], device=dev)
+    nblk = 2048
+    hk = torch.empty((nblk,) + tuple(inp.k_cache.shape[1:]), dtype=inp.k_cache.dtype).pin_memory()
+    hv = torch.empty_like(hk).pin_memory()
+    src = wl.permutation(77, 1, inp.num_blocks)[:nblk]
+    out_pairs = torch.stack([src, torch.arange(nblk)], 1).contiguous().to(dev)
+    in_pairs = torch.stack([torch.arange(nblk), src], 1).contiguous().to(dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    bytes_dir = 2 * nblk * hk[0].numel() * hk.element_size()
+    for _ in range(max(args.warmup, 3)):
+        pa.pa_swap_blocks(out_pairs, inp.k_cache, inp.v_cache, hk, hv, err_word=err)
+        pa.pa_swap_blocks(in_pairs, hk, hv, inp.k_cache, inp.v_cache, err_word=err)
+    torch.cuda.synchronize(dev)
+    K = args.steps
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3 * K)]
+    for i in range(K):
+        ev[3 * i].record(stream)
+        pa.pa_swap_blocks(out_pairs, inp.k_cache, inp.v_cache, hk, hv, err_word=err)
+        ev[3 * i + 1].record(stream)
+        pa.pa_swap_blocks(in_pairs, hk, hv, inp.k_cache, inp.v_cache, err_word=err)
+        ev[3 * i + 2].record(stream)
+    torch.cuda.synchronize(dev)
+    assert err.item() == 0
+    t_out = statistics.mean(ev[3 * i].elapsed_time(ev[3 * i + 1]) for i in range(K))
+    t_in = statistics.mean(ev[3 * i + 1].elapsed_time(ev[3 * i + 2]) for i in range(K))
+    line = {"metric": "KV block swap GB/s (HBM <-> pinned host memory)", "value": round(
+        2 * bytes_dir / ((t_out + t_in) * 1e-3) / 1e9, 2), "unit": "GB/s", "n_gpus": 1, "steps": K,
+        "warmup": max(args.warmup, 3), "higher_is_better": True, "dtype": "f16", "data": "synthetic",
+        "config": {"workload": f"swap: {nblk} OPT-13B-shaped blocks (K+V {bytes_dir / 1e6:.0f} MB) out to pinned "
+                               "host memory and back, pa_swap_blocks", "blocks": nblk},
+        "swap_out_gbs": round(bytes_dir / (t_out * 1e-3) / 1e9, 2),
+        "swap_in_gbs": round(bytes_dir / (t_in * 1e-3) / 1e9, 2),
+        "ms_out": round(t_out, 4), "ms_in": round(t_in, 4), "gpu_launches": 2 * K, "impl": "native"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def run_reference(args):
     world, rank, _ = dist_env()
     if rank != 0:
@@ -687,6 +733,8 @@ def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload == "swap":
+        run_swap(args)
     else:
         run_native(args)
 

@@ -8,7 +8,9 @@
  *                   table;
  *   pa_append_kv    store each new token's key/value rows into its slot;
  *   pa_copy_blocks  copy whole blocks, the copy-on-write step for blocks that
- *                   several sequences share.
+ *                   several sequences share;
+ *   pa_swap_blocks  copy whole blocks between two pools (GPU memory and host
+ *                   memory), the swap step of residency changes.
  *
  * Sources (web pages on PagedAttention):
  *   [A] "PagedAttention: From Operating System Virtual Memory to Large
@@ -197,6 +199,25 @@ PA_API pa_status pa_copy_blocks(const int64_t *src_dst_pairs, int num_pairs, voi
                          void *v_cache, int num_kv_heads, int head_dim, int block_size,
                          int num_blocks, pa_dtype dtype, uint32_t *err_word,
                          pa_stream_t stream);
+
+/*
+ * Block swap between two pools [B 踩过的坑: swap (or recompute) is the fallback
+ * when GPU memory runs short; "PagedAttention的终极用途": pages move between GPU
+ * and CPU memory].  For each pair (src, dst) copy block src of the source pool
+ * onto block dst of the destination pool, K and V, all kv heads: a bit-exact
+ * copy.  Either pool may be device memory or host memory the GPU can address
+ * (pinned, mapped host allocations; on GB300 they are reached over the
+ * NVLink-C2C host link).  The pairs array must be readable by the GPU too.
+ * Both pools share the cache layout, dtype, num_kv_heads, head_dim and
+ * block_size.  A pair outside either pool is skipped and flagged
+ * (PA_DEVERR_BAD_PAIR).  The pools must not overlap; a destination named
+ * twice is order-dependent: callers must not do this.  num_pairs == 0 returns
+ * PA_OK without launching.
+ */
+PA_API pa_status pa_swap_blocks(const int64_t *src_dst_pairs, int num_pairs, const void *src_k,
+                                const void *src_v, void *dst_k, void *dst_v, int src_num_blocks,
+                                int dst_num_blocks, int num_kv_heads, int head_dim, int block_size,
+                                pa_dtype dtype, uint32_t *err_word, pa_stream_t stream);
 
 /* Static text for a status code. */
 PA_API const char *pa_status_string(pa_status status);

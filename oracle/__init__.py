@@ -47,6 +47,8 @@ def _bind(lib):
     lib.orc_append_kv.restype = I64
     lib.orc_copy_blocks.argtypes = [P, P, P, I64, I, I, I, I, I]
     lib.orc_copy_blocks.restype = I64
+    lib.orc_swap_blocks.argtypes = [P, P, P, P, P, I64, I, I, I, I, I, I]
+    lib.orc_swap_blocks.restype = I64
     lib.orc_element_to_double.argtypes = [P, I, I64]
     lib.orc_element_to_double.restype = D
     return lib
@@ -145,4 +147,21 @@ def copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor, src_dst_pairs, lib
                              hkv, d, bs, nb, k_cache.element_size())
     if rc < 0:
         raise ValueError(f"oracle copy_blocks refused the input (code {rc})")
+    return int(rc)
+
+
+def swap_blocks(src_k: torch.Tensor, src_v: torch.Tensor, dst_k: torch.Tensor, dst_v: torch.Tensor,
+                src_dst_pairs, lib=None) -> int:
+    """Copy block src of the source pool onto block dst of the destination
+    pool (K and V), in place on CPU tensors.  Returns the out-of-range pairs."""
+    lib = lib or load()
+    assert dst_k.device.type == "cpu" and dst_k.is_contiguous() and dst_v.is_contiguous()
+    src_k, src_v = _cpu(src_k), _cpu(src_v)
+    pr = _cpu(torch.as_tensor(src_dst_pairs)).to(torch.int64).reshape(-1, 2).contiguous()
+    snb, hkv, bs, d = src_k.shape
+    dnb = dst_k.shape[0]
+    rc = lib.orc_swap_blocks(src_k.data_ptr(), src_v.data_ptr(), dst_k.data_ptr(), dst_v.data_ptr(), pr.data_ptr(),
+                             pr.shape[0], snb, dnb, hkv, d, bs, src_k.element_size())
+    if rc < 0:
+        raise ValueError(f"oracle swap_blocks refused the input (code {rc})")
     return int(rc)

@@ -353,3 +353,31 @@ int64_t orc_copy_blocks(void *k_cache, void *v_cache, const int64_t *pairs, int6
     }
     return bad;
 }
+
+/* ------------------------------------------------------------------ */
+/* Swap: the block copy between two pools (one of them in host memory on the
+ * GPU side).  pairs: int64 [num_pairs][2] = (src block of the source pool,
+ * dst block of the destination pool).  A pair outside either pool is skipped
+ * and counted; a destination named twice is refused (-2).
+ */
+int64_t orc_swap_blocks(const void *src_k, const void *src_v, void *dst_k, void *dst_v, const int64_t *pairs,
+                        int64_t num_pairs, int src_num_blocks, int dst_num_blocks, int num_kv_heads,
+                        int head_dim, int block_size, int elt_bytes)
+{
+    for (int64_t i = 0; i < num_pairs; ++i)
+        for (int64_t j = 0; j < i; ++j)
+            if (pairs[2 * i + 1] == pairs[2 * j + 1])
+                return -2;
+    const size_t block_bytes = (size_t)num_kv_heads * block_size * head_dim * elt_bytes;
+    int64_t bad = 0;
+    for (int64_t i = 0; i < num_pairs; ++i) {
+        const int64_t src = pairs[2 * i], dst = pairs[2 * i + 1];
+        if (src < 0 || src >= src_num_blocks || dst < 0 || dst >= dst_num_blocks) {
+            ++bad;
+            continue;
+        }
+        memcpy((char *)dst_k + dst * block_bytes, (const char *)src_k + src * block_bytes, block_bytes);
+        memcpy((char *)dst_v + dst * block_bytes, (const char *)src_v + src * block_bytes, block_bytes);
+    }
+    return bad;
+}

@@ -452,6 +452,39 @@ pa_status pa_copy_blocks(const int64_t *src_dst_pairs, int num_pairs, void *k_ca
     return PA_OK;
 }
 
+pa_status pa_swap_blocks(const int64_t *src_dst_pairs, int num_pairs, const void *src_k, const void *src_v,
+                         void *dst_k, void *dst_v, int src_num_blocks, int dst_num_blocks, int num_kv_heads,
+                         int head_dim, int block_size, pa_dtype dtype, uint32_t *err_word, pa_stream_t stream) {
+    g_detail.clear();
+    if (num_pairs < 0 || num_kv_heads <= 0 || src_num_blocks <= 0 || dst_num_blocks <= 0)
+        return fail(PA_ERR_INVALID_ARGUMENT, "num_pairs, num_kv_heads or a pool size out of range");
+    if (!block_size_ok(block_size))
+        return fail(PA_ERR_UNSUPPORTED, "block_size must be 8, 16 or 32");
+    if (!head_dim_ok(head_dim))
+        return fail(PA_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
+    if (!dtype_ok(dtype))
+        return fail(PA_ERR_INVALID_ARGUMENT, "unknown dtype");
+    if (num_pairs == 0)
+        return PA_OK;
+    if (!src_dst_pairs || !src_k || !src_v || !dst_k || !dst_v)
+        return fail(PA_ERR_INVALID_ARGUMENT, "null pointer");
+    if (!aligned16(src_k) || !aligned16(src_v) || !aligned16(dst_k) || !aligned16(dst_v))
+        return fail(PA_ERR_INVALID_ARGUMENT, "the pools must be 16-byte aligned");
+    if ((reinterpret_cast<uintptr_t>(src_dst_pairs) & 7u) != 0)
+        return fail(PA_ERR_INVALID_ARGUMENT, "src_dst_pairs must be 8-byte aligned");
+    int dev = 0, sms = 0;
+    cudaError_t e = device_sms(&dev, &sms);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "device query");
+    const long long block_bytes =
+        static_cast<long long>(num_kv_heads) * block_size * head_dim * elt_bytes(dtype);
+    e = launch_swap_blocks(src_dst_pairs, num_pairs, src_k, src_v, dst_k, dst_v, block_bytes, src_num_blocks,
+                           dst_num_blocks, err_word, sms, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+        return cuda_fail(e, "swap_blocks launch");
+    return PA_OK;
+}
+
 const char *pa_status_string(pa_status status) {
     switch (status) {
     case PA_OK:

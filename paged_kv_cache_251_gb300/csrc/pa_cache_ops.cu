@@ -6,7 +6,9 @@
 //   cache[slot / block_size][h][slot % block_size][:].
 // Block copy (same page, 案例 3: copy-on-write, one whole block is the copy
 // unit): for each (src, dst) pair the block's tiles of every kv head, K and V.
-// Both are bit-exact 16-byte vector copies; bad slots / pairs are skipped and
+// Swap (same page, 踩过的坑: swap is the fallback when memory runs short): the
+// block copy between two pools, one of which may be host memory.
+// All are bit-exact 16-byte vector copies; bad slots / pairs are skipped and
 // flagged in the error word.
 #include <cuda_runtime.h>
 
@@ -96,7 +98,66 @@ __global__ void __launch_bounds__(256) copy_blocks_kernel(const int64_t *__restr
     }
 }
 
+// Swap: the same block copy between two pools (device memory, or host memory
+// the GPU can address).  grid.x: chunks, grid.y: pairs (strided), grid.z: K / V.
+__global__ void __launch_bounds__(256) swap_blocks_kernel(const int64_t *__restrict__ pairs, int num_pairs,
+                                                          const uint4 *src_k, const uint4 *src_v, uint4 *dst_k,
+                                                          uint4 *dst_v, long long chunks_per_block,
+                                                          long long src_blocks, long long dst_blocks, uint32_t *err) {
+    const uint4 *src_pool = blockIdx.z == 0 ? src_k : src_v;
+    uint4 *dst_pool = blockIdx.z == 0 ? dst_k : dst_v;
+    for (int pi = blockIdx.y; pi < num_pairs; pi += gridDim.y) {
+        const long long src = pairs[2 * pi], dst = pairs[2 * pi + 1];
+        if (src < 0 || src >= src_blocks || dst < 0 || dst >= dst_blocks) {
+            if (err && blockIdx.x == 0 && threadIdx.x == 0)
+                atomicOr(err, PA_DEVERR_BAD_PAIR);
+            continue;
+        }
+        const uint4 *s = src_pool + src * chunks_per_block;
+        uint4 *d = dst_pool + dst * chunks_per_block;
+        const long long step = static_cast<long long>(gridDim.x) * blockDim.x * kCopyUnroll;
+        for (long long base = static_cast<long long>(blockIdx.x) * blockDim.x * kCopyUnroll + threadIdx.x;
+             base < chunks_per_block; base += step) {
+            uint4 r[kCopyUnroll];
+#pragma unroll
+            for (int u = 0; u < kCopyUnroll; ++u) {
+                const long long c = base + static_cast<long long>(u) * blockDim.x;
+                if (c < chunks_per_block)
+                    r[u] = ld_stream(s + c);
+            }
+#pragma unroll
+            for (int u = 0; u < kCopyUnroll; ++u) {
+                const long long c = base + static_cast<long long>(u) * blockDim.x;
+                if (c < chunks_per_block)
+                    d[c] = r[u];
+            }
+        }
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_swap_blocks(const int64_t *pairs, int num_pairs, const void *src_k, const void *src_v,
+                               void *dst_k, void *dst_v, long long block_bytes, int src_blocks, int dst_blocks,
+                               uint32_t *err, int num_sms, cudaStream_t stream) {
+    const long long chunks = block_bytes / 16;
+    const long long per_cta = 256LL * kCopyUnroll;
+    const long long gx = (chunks + per_cta - 1) / per_cta;
+    long long gy = num_pairs;
+    const long long cap = static_cast<long long>(num_sms) * 8;  // CTAs in flight for either link's latency
+    if (gx * gy * 2 > cap) {
+        gy = cap / (2 * gx);
+        if (gy < 1)
+            gy = 1;
+    }
+    if (gy > 65535)
+        gy = 65535;
+    dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(gy), 2);
+    swap_blocks_kernel<<<grid, 256, 0, stream>>>(pairs, num_pairs, static_cast<const uint4 *>(src_k),
+                                                 static_cast<const uint4 *>(src_v), static_cast<uint4 *>(dst_k),
+                                                 static_cast<uint4 *>(dst_v), chunks, src_blocks, dst_blocks, err);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_append(const void *k, const void *v, const int64_t *slots, void *k_cache, void *v_cache,
                           int num_tokens, int num_kv_heads, int row_bytes, int block_size, int num_blocks,

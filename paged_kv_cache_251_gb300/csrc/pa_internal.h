@@ -34,6 +34,10 @@ cudaError_t launch_copy_blocks(const int64_t *pairs, int num_pairs, void *k_cach
                                long long block_bytes, int num_blocks, uint32_t *err, int num_sms,
                                cudaStream_t stream);
 
+cudaError_t launch_swap_blocks(const int64_t *pairs, int num_pairs, const void *src_k, const void *src_v,
+                               void *dst_k, void *dst_v, long long block_bytes, int src_blocks, int dst_blocks,
+                               uint32_t *err, int num_sms, cudaStream_t stream);
+
 // Text returned by pa_last_error_detail() on the calling thread.
 void set_last_error_detail(const char *why);
 

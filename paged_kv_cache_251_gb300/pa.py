@@ -45,6 +45,8 @@ def _load():
     lib.pa_append_kv.restype = I
     lib.pa_copy_blocks.argtypes = [P, I, P, P, I, I, I, I, I, P, P]
     lib.pa_copy_blocks.restype = I
+    lib.pa_swap_blocks.argtypes = [P, I, P, P, P, P, I, I, I, I, I, I, P, P]
+    lib.pa_swap_blocks.restype = I
     lib.pa_status_string.argtypes = [I]
     lib.pa_status_string.restype = ctypes.c_char_p
     lib.pa_last_error_detail.argtypes = []
@@ -174,6 +176,29 @@ def pa_copy_blocks(src_dst_pairs: torch.Tensor, k_cache: torch.Tensor, v_cache: 
     nb, hkv, bs, d = k_cache.shape
     _check(_lib.pa_copy_blocks(_ptr(src_dst_pairs), src_dst_pairs.numel() // 2, _ptr(k_cache),
                                _ptr(v_cache), hkv, d, bs, nb, DTYPE_CODE[k_cache.dtype],
+                               _ptr(err_word), _stream(stream)))
+
+
+def pa_swap_blocks(src_dst_pairs: torch.Tensor, src_k: torch.Tensor, src_v: torch.Tensor, dst_k: torch.Tensor,
+                   dst_v: torch.Tensor, err_word: torch.Tensor | None = None, stream=None) -> None:
+    """Copy block src of (src_k, src_v) onto block dst of (dst_k, dst_v) for
+    every pair.  Pools and pairs may be CUDA tensors or pinned host tensors
+    (the GPU reads / writes host memory directly)."""
+    for t in (src_dst_pairs, src_k, src_v, dst_k, dst_v):
+        if not t.is_contiguous() or not (t.is_cuda or t.is_pinned()):
+            raise ValueError("pools and pairs must be contiguous CUDA tensors or pinned host tensors")
+    if err_word is not None:
+        _cuda(err_word)
+    if src_dst_pairs.dtype != torch.int64:
+        raise TypeError("src_dst_pairs must be int64")
+    if src_k.dtype != dst_k.dtype or src_v.dtype != src_k.dtype or dst_v.dtype != src_k.dtype:
+        raise TypeError("both pools must share one dtype")
+    snb, hkv, bs, d = src_k.shape
+    dnb, hkv2, bs2, d2 = dst_k.shape
+    if (hkv, bs, d) != (hkv2, bs2, d2) or src_v.shape != src_k.shape or dst_v.shape != dst_k.shape:
+        raise ValueError("both pools must share the block layout")
+    _check(_lib.pa_swap_blocks(_ptr(src_dst_pairs), src_dst_pairs.numel() // 2, _ptr(src_k), _ptr(src_v),
+                               _ptr(dst_k), _ptr(dst_v), snb, dnb, hkv, d, bs, DTYPE_CODE[src_k.dtype],
                                _ptr(err_word), _stream(stream)))
 
 

@@ -102,3 +102,36 @@ def test_copy_blocks_bad_pair_flagged_and_empty_list():
     assert err.item() & 4
     k[5], v[5] = k[3], v[3]
     assert torch.equal(_bits(kg.cpu()), _bits(k)) and torch.equal(_bits(vg.cpu()), _bits(v))
+
+
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16, torch.float32])
+def test_swap_out_to_pinned_host_and_back_bit_exact(dtype):
+    """Swap blocks GPU -> pinned host -> GPU (other slots); pools compared byte
+    for byte with the oracle after each direction."""
+    from paged_kv_cache_251_gb300 import pa
+    nb, hb, hkv, bs, d = 40, 24, 8, 16, 128
+    k, v = _pool(nb, hkv, bs, d, dtype, seed=11)
+    kg, vg = k.cuda(), v.cuda()
+    hk = torch.zeros((hb, hkv, bs, d), dtype=dtype).pin_memory()
+    hv = torch.zeros_like(hk).pin_memory()
+    ok_, ov_ = torch.zeros_like(hk), torch.zeros_like(hv)
+    perm = wl.permutation(12, 1, nb)
+    out_pairs = torch.stack([perm[:20], wl.permutation(13, 1, hb)[:20]], 1).contiguous()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pa.pa_swap_blocks(out_pairs.cuda(), kg, vg, hk, hv, err_word=err)
+    oracle.swap_blocks(k, v, ok_, ov_, out_pairs)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    assert torch.equal(_bits(hk), _bits(ok_)) and torch.equal(_bits(hv), _bits(ov_))
+    # swap back in to other device blocks; the pairs live in pinned host memory
+    in_pairs = torch.stack([out_pairs[:, 1], perm[20:40]], 1).contiguous().pin_memory()
+    pa.pa_swap_blocks(in_pairs, hk, hv, kg, vg, err_word=err)
+    oracle.swap_blocks(ok_, ov_, k, v, in_pairs)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    assert torch.equal(_bits(kg.cpu()), _bits(k)) and torch.equal(_bits(vg.cpu()), _bits(v))
+    # a pair outside a pool is skipped and flagged
+    pa.pa_swap_blocks(torch.tensor([[0, hb]], dtype=torch.int64).cuda(), kg, vg, hk, hv, err_word=err)
+    torch.cuda.synchronize()
+    assert err.item() & 4
+    assert torch.equal(_bits(hk), _bits(ok_))

@@ -136,3 +136,25 @@ def test_ring_window_moves_no_data_and_keeps_the_window():
     # stale entries are the logical blocks the ring has recycled
     last = (L - 1) // bs
     assert all(m.table[lb] == -1 for lb in range(0, last - R + 1))
+
+
+def test_swap_round_trip_restores_the_blocks_and_touches_nothing_else():
+    bs, hkv, d = 16, 4, 64
+    dk, dv = _pool(12, hkv, bs, d, torch.bfloat16, seed=5)
+    hk = torch.zeros((5,) + tuple(dk.shape[1:]), dtype=torch.bfloat16)
+    hv = torch.zeros_like(hk)
+    d0k, d0v = dk.clone(), dv.clone()
+    out = [[3, 0], [7, 4], [11, 2]]
+    assert oracle.swap_blocks(dk, dv, hk, hv, out) == 0
+    for src, dst in out:
+        assert torch.equal(hk[dst].view(torch.int16), dk[src].view(torch.int16))
+        assert torch.equal(hv[dst].view(torch.int16), dv[src].view(torch.int16))
+    assert torch.count_nonzero(hk[[1, 3]].view(torch.int16)) == 0      # untouched host blocks
+    dk[3].zero_(), dv[3].zero_(), dk[7].zero_()
+    assert oracle.swap_blocks(hk, hv, dk, dv, [[0, 3], [4, 7], [2, 11]]) == 0
+    assert torch.equal(dk[[3, 11]].view(torch.int16), d0k[[3, 11]].view(torch.int16))
+    assert torch.equal(dv[3].view(torch.int16), d0v[3].view(torch.int16))
+    assert torch.equal(dk[7].view(torch.int16), d0k[7].view(torch.int16))
+    assert oracle.swap_blocks(dk, dv, hk, hv, [[12, 0], [0, 5], [-1, 1]]) == 3
+    with pytest.raises(ValueError):
+        oracle.swap_blocks(dk, dv, hk, hv, [[1, 2], [3, 2]])
