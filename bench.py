@@ -55,6 +55,8 @@ def parse_args(argv=None):
     ap.add_argument("--workload", choices=["opt13b", "gqa", "window", "prefix_bs8", "prefix_bs16",
                                            "prefix_bs32", "tiny", "tiny_scaled", "swap"], default="opt13b")
     ap.add_argument("--partition", type=int, default=0, help="pa_decode partition_size (0 = default)")
+    ap.add_argument("--shared-prefix", action="store_true",
+                    help="prefix workloads: decode with pa_decode_shared_prefix (shared blocks read once per group)")
     ap.add_argument("--table", choices=["shuffled", "identity"], default="shuffled",
                     help="block hand-out order (identity: each sequence's blocks adjacent in memory)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU baseline budget")
@@ -375,8 +377,9 @@ class PrefixStep(DecodeAppendStep):
 
     append_first = True
 
-    def __init__(self, device, partition, block_size=16):
+    def __init__(self, device, partition, block_size=16, shared=False):
         Step.__init__(self, device, partition)
+        self.shared = shared
         from paged_kv_cache_251_gb300 import pa, scenarios
         from paged_kv_cache_251_gb300 import accounting as acc
         self.pa = pa
@@ -408,6 +411,26 @@ class PrefixStep(DecodeAppendStep):
         self.roof_bytes = self.dec_bytes["total"] - (self.kv_bytes - self.unique_kv)
         self.launches = (1 if st.pairs.shape[0] else 0) + 1 + (2 if self.ws is not None else 1)
         self.T = st.slots.numel()
+        if shared:
+            self.name += "_shared"
+            self.description += "; decode by pa_decode_shared_prefix (each prompt's whole blocks read once per group)"
+            self.group = st.samples
+            self.shared_lens = torch.full((st.prompts,), st.prompt_len // block_size * block_size,
+                                          dtype=torch.int32, device=device)
+            n = pa.pa_decode_shared_prefix_workspace_size(s.num_seqs, s.num_heads, s.head_dim, block_size,
+                                                          self.bt.shape[1], partition, self.group, s.dtype)
+            self.ws_shared = torch.empty(n, dtype=torch.uint8, device=device)
+            self.launches = (1 if st.pairs.shape[0] else 0) + 1 + 4
+
+    def decode(self, stream, q=None, bt=None, cl=None):
+        if not self.shared:
+            return DecodeAppendStep.decode(self, stream, q, bt, cl)
+        s = self.shape
+        self.pa.pa_decode_shared_prefix(self.out, self.q if q is None else q, self.k_cache, self.v_cache,
+                                        self.bt if bt is None else bt, self.cl if cl is None else cl,
+                                        self.shared_lens, self.group, num_kv_heads=s.num_kv_heads,
+                                        partition_size=self.partition, workspace=self.ws_shared, err_word=self.err,
+                                        stream=stream)
 
     def pre(self, stream, pairs=None):
         self.pa.pa_copy_blocks(self.pairs if pairs is None else pairs, self.k_cache, self.v_cache,
@@ -438,13 +461,13 @@ class PrefixStep(DecodeAppendStep):
 WORKLOADS = ["opt13b", "gqa", "window", "prefix_bs8", "prefix_bs16", "prefix_bs32", "tiny", "tiny_scaled"]
 
 
-def make_step(name, device, partition, table="shuffled"):
+def make_step(name, device, partition, table="shuffled", shared=False):
     if name in ("opt13b", "gqa", "tiny", "tiny_scaled"):
         return DecodeAppendStep(name, device, partition, shuffle=(table == "shuffled"))
     if name == "window":
         return WindowStep(device, partition)
     if name.startswith("prefix_bs"):
-        return PrefixStep(device, partition, int(name[len("prefix_bs"):]))
+        return PrefixStep(device, partition, int(name[len("prefix_bs"):]), shared=shared)
     raise ValueError(name)
 
 
@@ -484,7 +507,7 @@ def run_native(args):
         raise SystemExit("bench.py needs a CUDA GPU for the native arm")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    st = make_step(args.workload, dev, args.partition, args.table)
+    st = make_step(args.workload, dev, args.partition, args.table, args.shared_prefix)
     s = st.shape
     stream = torch.cuda.current_stream(dev)
 

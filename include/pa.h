@@ -144,6 +144,39 @@ PA_API pa_status pa_decode(void *out, const void *q, const void *k_cache, const 
                     size_t workspace_bytes, uint32_t *err_word, pa_stream_t stream);
 
 /*
+ * Decode attention for groups of sequences that share a prompt prefix [B
+ * 核心要点 and 案例 3: parallel samples of one prompt share its blocks].  Same
+ * result as pa_decode (window 0) for every sequence; the shared blocks are
+ * read once per group instead of once per sequence.
+ *   Sequences come in consecutive groups of group_size (num_seqs a multiple
+ *   of it).  Group g's members share their first shared_lens[g] tokens: their
+ *   block tables agree on the first shared_lens[g] / block_size entries (as a
+ *   fork produces).  The shared blocks are read through the first member's
+ *   table row.  shared_lens is a device int32 [num_seqs / group_size]; each
+ *   value is used rounded down to whole blocks and to at most every member's
+ *   context (PA_DEVERR_BAD_LEN flags a change).
+ *   Supported: fp16 / bf16 K/V, head_dim 128, group_size * (num_heads /
+ *   num_kv_heads) in {2, 4, 8} (the grouped queries of one kv head go
+ *   through the tensor-core kernel together).
+ *   workspace: at least pa_decode_shared_prefix_workspace_size() bytes,
+ *   16-byte aligned (regrouped queries, lengths, two sets of partials).
+ * Other arguments as pa_decode.
+ */
+PA_API pa_status pa_decode_shared_prefix(void *out, const void *q, const void *k_cache, const void *v_cache,
+                                         const int32_t *block_tables, const int32_t *context_lens,
+                                         const int32_t *shared_lens, int group_size, int num_seqs,
+                                         int num_heads, int num_kv_heads, int head_dim, int block_size,
+                                         float scale, pa_dtype dtype, pa_dtype out_dtype,
+                                         int max_blocks_per_seq, int num_blocks, int partition_size,
+                                         void *workspace, size_t workspace_bytes, uint32_t *err_word,
+                                         pa_stream_t stream);
+
+/* Bytes of workspace pa_decode_shared_prefix needs (0 for bad arguments). */
+PA_API size_t pa_decode_shared_prefix_workspace_size(int num_seqs, int num_heads, int head_dim,
+                                                     int block_size, int max_blocks_per_seq,
+                                                     int partition_size, int group_size, pa_dtype dtype);
+
+/*
  * pa_decode without any allocation.  No page describes this call: it exists
  * for callers that cannot allocate device memory (a plugin whose host
  * framework owns all device allocations, a runtime with a fixed memory

@@ -227,6 +227,86 @@ pa_status plan_decode(int num_seqs, int num_heads, int head_dim, int block_size,
 
 void set_last_error_detail(const char *why) { g_detail = why; }
 
+pa_status launch_decode_kernel(DecodeParams &p, int dtype, int head_dim, int G, cudaStream_t cs) {
+    const int block_size = p.block_size;
+    const int row = head_dim * elt_bytes(dtype);
+    const int tile = block_size * row;
+    const long long tiles = static_cast<long long>(p.num_blocks) * p.num_kv_heads;
+    // MHA takes the TMA-tensor kernel; its 3-D tensor map addresses tiles with
+    // a 32-bit coordinate, so very large pools use the general kernel.
+    const bool mha = (G == 1 && tiles <= INT_MAX);
+    // Grouped heads with 16-bit K/V and head_dim 128 take the tensor-core kernel.
+    const bool gqa_tc = (G > 1 && head_dim == 128 && dtype != PA_F32 && tiles <= INT_MAX &&
+                         static_cast<long long>(p.num_seqs) * p.num_heads <= INT_MAX);
+    const void *fn;
+    size_t smem;
+    int threads;
+    CUtensorMap tmk, tmv, tmq;
+    if (gqa_tc) {
+        fn = dtype == PA_F16 ? decode_gqa_kernel_f16(block_size, G) : decode_gqa_kernel_bf16(block_size, G);
+        p.stages = kGqaStages;
+        smem = gqa_smem_layout(kGqaStages).total;
+        threads = kGqaThreads;
+        pa_status ts = kv_tensor_map_groups(&tmk, p.k_cache, dtype, block_size, tiles);
+        if (ts == PA_OK)
+            ts = kv_tensor_map_groups(&tmv, p.v_cache, dtype, block_size, tiles);
+        if (ts == PA_OK)
+            ts = q_tensor_map(&tmq, p.q, dtype, head_dim, static_cast<long long>(p.num_seqs) * p.num_heads, G);
+        if (ts != PA_OK)
+            return ts;
+    } else if (mha) {
+        fn = dtype == PA_F32   ? decode_mha_kernel_f32(head_dim, block_size)
+             : dtype == PA_F16 ? decode_mha_kernel_f16(head_dim, block_size)
+                               : decode_mha_kernel_bf16(head_dim, block_size);
+        int S = kMhaStageBudget / (2 * tile);
+        S = S < 4 ? 4 : (S > 16 ? 16 : S);
+        p.stages = S;
+        smem = mha_smem_layout(S, tile, row, head_dim).total;
+        threads = kMhaThreads;
+        pa_status ts = kv_tensor_map(&tmk, p.k_cache, dtype, head_dim, block_size, tiles);
+        if (ts == PA_OK)
+            ts = kv_tensor_map(&tmv, p.v_cache, dtype, head_dim, block_size, tiles);
+        if (ts != PA_OK)
+            return ts;
+    } else {
+        fn = dtype == PA_F32   ? decode_kernel_f32(head_dim, G)
+             : dtype == PA_F16 ? decode_kernel_f16(head_dim, G)
+                               : decode_kernel_bf16(head_dim, G);
+        int S = kStageBudget / (2 * tile);
+        S = S < 2 ? 2 : (S > 8 ? 8 : S);
+        p.stages = S;
+        smem = decode_smem_layout(S, tile, row, G, head_dim).total;
+        threads = kDecodeThreads;
+    }
+    if (!fn)
+        return fail(PA_ERR_UNSUPPORTED, "no decode kernel for this dtype / head_dim / group / block size");
+
+    int dev = 0, sms = 0, per_sm = 0;
+    cudaError_t e = device_sms(&dev, &sms);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "device query");
+    e = prepare_kernel(dev, fn, smem, threads, &per_sm);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "decode kernel set-up");
+    if (per_sm < 1)
+        return fail(PA_ERR_UNSUPPORTED, "decode kernel does not fit on an SM");
+
+    const long long items_max = static_cast<long long>(p.num_seqs) * p.num_kv_heads * p.max_parts;
+    long long grid = static_cast<long long>(sms) * per_sm;
+    if (grid > items_max)
+        grid = items_max;
+    if (grid < 1)
+        grid = 1;
+    void *args_gqa[] = {&p, &tmk, &tmv, &tmq};
+    void *args_mha[] = {&p, &tmk, &tmv};
+    void *args[] = {&p};
+    e = cudaLaunchKernel(fn, dim3(static_cast<unsigned>(grid)), dim3(threads),
+                         gqa_tc ? args_gqa : (mha ? args_mha : args), smem, cs);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "decode launch");
+    return PA_OK;
+}
+
 }  // namespace pa
 
 using namespace pa;
@@ -301,83 +381,15 @@ pa_status pa_decode(void *out, const void *q, const void *k_cache, const void *v
     p.out_dtype = out_dtype;
     p.stages = 0;
     p.scale_log2 = scale * 1.4426950408889634f;
+    p.start_tok = nullptr;
+    p.force_partial = 0;
 
-    const int row = head_dim * elt_bytes(dtype);
-    const int tile = block_size * row;
-    const long long tiles = static_cast<long long>(num_blocks) * num_kv_heads;
-    // MHA takes the TMA-tensor kernel; its 3-D tensor map addresses tiles with
-    // a 32-bit coordinate, so very large pools use the general kernel.
-    const bool mha = (G == 1 && tiles <= INT_MAX);
-    // Grouped heads with 16-bit K/V and head_dim 128 take the tensor-core kernel.
-    const bool gqa_tc = (G > 1 && head_dim == 128 && dtype != PA_F32 && tiles <= INT_MAX &&
-                         static_cast<long long>(num_seqs) * num_heads <= INT_MAX);
-    const void *fn;
-    size_t smem;
-    int threads;
-    CUtensorMap tmk, tmv, tmq;
-    if (gqa_tc) {
-        fn = dtype == PA_F16 ? decode_gqa_kernel_f16(block_size, G) : decode_gqa_kernel_bf16(block_size, G);
-        p.stages = kGqaStages;
-        smem = gqa_smem_layout(kGqaStages).total;
-        threads = kGqaThreads;
-        pa_status ts = kv_tensor_map_groups(&tmk, k_cache, dtype, block_size, tiles);
-        if (ts == PA_OK)
-            ts = kv_tensor_map_groups(&tmv, v_cache, dtype, block_size, tiles);
-        if (ts == PA_OK)
-            ts = q_tensor_map(&tmq, q, dtype, head_dim, static_cast<long long>(num_seqs) * num_heads, G);
-        if (ts != PA_OK)
-            return ts;
-    } else if (mha) {
-        fn = dtype == PA_F32   ? decode_mha_kernel_f32(head_dim, block_size)
-             : dtype == PA_F16 ? decode_mha_kernel_f16(head_dim, block_size)
-                               : decode_mha_kernel_bf16(head_dim, block_size);
-        int S = kMhaStageBudget / (2 * tile);
-        S = S < 4 ? 4 : (S > 16 ? 16 : S);
-        p.stages = S;
-        smem = mha_smem_layout(S, tile, row, head_dim).total;
-        threads = kMhaThreads;
-        pa_status ts = kv_tensor_map(&tmk, k_cache, dtype, head_dim, block_size, tiles);
-        if (ts == PA_OK)
-            ts = kv_tensor_map(&tmv, v_cache, dtype, head_dim, block_size, tiles);
-        if (ts != PA_OK)
-            return ts;
-    } else {
-        fn = dtype == PA_F32   ? decode_kernel_f32(head_dim, G)
-             : dtype == PA_F16 ? decode_kernel_f16(head_dim, G)
-                               : decode_kernel_bf16(head_dim, G);
-        int S = kStageBudget / (2 * tile);
-        S = S < 2 ? 2 : (S > 8 ? 8 : S);
-        p.stages = S;
-        smem = decode_smem_layout(S, tile, row, G, head_dim).total;
-        threads = kDecodeThreads;
-    }
-    if (!fn)
-        return fail(PA_ERR_UNSUPPORTED, "no decode kernel for this dtype / head_dim / group / block size");
-
-    int dev = 0, sms = 0, per_sm = 0;
-    cudaError_t e = device_sms(&dev, &sms);
-    if (e != cudaSuccess)
-        return cuda_fail(e, "device query");
-    e = prepare_kernel(dev, fn, smem, threads, &per_sm);
-    if (e != cudaSuccess)
-        return cuda_fail(e, "decode kernel set-up");
-    if (per_sm < 1)
-        return fail(PA_ERR_UNSUPPORTED, "decode kernel does not fit on an SM");
-
-    const long long items_max = static_cast<long long>(num_seqs) * num_kv_heads * plan.max_parts;
-    long long grid = static_cast<long long>(sms) * per_sm;
-    if (grid > items_max)
-        grid = items_max;
-    if (grid < 1)
-        grid = 1;
+    const pa_status ls = launch_decode_kernel(p, dtype, head_dim, G, reinterpret_cast<cudaStream_t>(stream));
+    if (ls != PA_OK)
+        return ls;
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-    void *args_gqa[] = {&p, &tmk, &tmv, &tmq};
-    void *args_mha[] = {&p, &tmk, &tmv};
     void *args[] = {&p};
-    e = cudaLaunchKernel(fn, dim3(static_cast<unsigned>(grid)), dim3(threads),
-                         gqa_tc ? args_gqa : (mha ? args_mha : args), smem, cs);
-    if (e != cudaSuccess)
-        return cuda_fail(e, "decode launch");
+    cudaError_t e;
     if (plan.max_parts > 1) {
         const long long rows = static_cast<long long>(num_seqs) * num_heads;
         e = cudaLaunchKernel(reduce_kernel(head_dim), dim3(static_cast<unsigned>(rows)), dim3(kReduceThreads), args, 0,

@@ -57,6 +57,8 @@ struct DecodeParams {
     int max_blocks_per_seq, num_blocks, bpp, max_parts, out_dtype, stages;
     int max_len;       // max_blocks_per_seq * block_size
     float scale_log2;  // scale * log2(e): scores are kept in base-2 units
+    const int32_t *start_tok;  // per-sequence first attended token (nullable)
+    int force_partial;         // 1: always write partials, even for one partition
 };
 
 struct StageMeta {
@@ -155,7 +157,7 @@ __device__ inline void decode_producer(const DecodeParams &p, char *smem, const 
     // Sequences are scanned 32 at a time: lane j holds sequence chunk_base + j.
     int chunk_base = 0;
     long long chunk_prefix = 0;  // partitions of all sequences before chunk_base
-    int my_len = 0, my_np = 0, my_incl = 0, chunk_total = 0;
+    int my_len = 0, my_start = 0, my_np = 0, my_incl = 0, chunk_total = 0;
     bool chunk_ready = false;
 
     uint32_t t = 0;  // stages issued
@@ -166,7 +168,7 @@ __device__ inline void decode_producer(const DecodeParams &p, char *smem, const 
     for (long long w = blockIdx.x; ok; w += gridDim.x) {
         const long long f = w / hkv;
         const int kvh = static_cast<int>(w % hkv);
-        int s = -1, part = 0, len = 0, nparts = 1;
+        int s = -1, part = 0, len = 0, start = 0, nparts = 1;
         for (;;) {
             if (!chunk_ready) {
                 if (chunk_base >= p.num_seqs)
@@ -175,7 +177,8 @@ __device__ inline void decode_producer(const DecodeParams &p, char *smem, const 
                 my_len = sq < p.num_seqs ? ld_nc_i32(p.context_lens + sq) : 0;
                 if (sq < p.num_seqs && my_len > p.max_len && p.err)
                     atomicOr(p.err, PA_DEVERR_BAD_LEN);
-                my_np = sq < p.num_seqs ? seq_span(my_len, p.max_len, p.window, bs, p.bpp).nparts : 0;
+                my_start = (sq < p.num_seqs && p.start_tok) ? ld_nc_i32(p.start_tok + sq) : 0;
+                my_np = sq < p.num_seqs ? seq_span(my_len, p.max_len, p.window, bs, p.bpp, my_start).nparts : 0;
                 my_incl = my_np;
 #pragma unroll
                 for (int o = 1; o < 32; o <<= 1) {
@@ -193,6 +196,7 @@ __device__ inline void decode_producer(const DecodeParams &p, char *smem, const 
                 const int incl_j = __shfl_sync(0xffffffffu, my_incl, j);
                 nparts = __shfl_sync(0xffffffffu, my_np, j);
                 len = __shfl_sync(0xffffffffu, my_len, j);
+                start = __shfl_sync(0xffffffffu, my_start, j);
                 part = static_cast<int>(f - (chunk_prefix + incl_j - nparts));
                 break;
             }
@@ -203,7 +207,7 @@ __device__ inline void decode_producer(const DecodeParams &p, char *smem, const 
         if (s < 0)
             break;  // no more items for this CTA
 
-        const SeqSpan sp = seq_span(len, p.max_len, p.window, bs, p.bpp);
+        const SeqSpan sp = seq_span(len, p.max_len, p.window, bs, p.bpp, start);
         const int blk_lo = sp.b0 + part * p.bpp;
         const int nb = max(0, min(p.bpp, sp.nblk - part * p.bpp));
         const int tok_lo = max(sp.start, blk_lo * bs);
@@ -461,7 +465,7 @@ __device__ inline void decode_consumer(const DecodeParams &p, char *smem, const 
                 }
                 const int h = cur.kvh * G + g;
                 const long long row = static_cast<long long>(cur.s) * p.num_heads + h;
-                if (cur.nparts == 1) {
+                if (cur.nparts == 1 && !p.force_partial) {
                     store_out(p.out, p.out_dtype, row * D + dd, den > 0.f ? num / den : 0.f);
                 } else {
                     const long long pr = row * p.max_parts + cur.part;
@@ -532,7 +536,8 @@ __global__ void __launch_bounds__(kReduceThreads) pa_reduce_kernel(const DecodeP
     const long long rowi = blockIdx.x;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int s = static_cast<int>(rowi / p.num_heads);
-    const SeqSpan sp = seq_span(p.context_lens[s], p.max_len, p.window, p.block_size, p.bpp);
+    const SeqSpan sp = seq_span(p.context_lens[s], p.max_len, p.window, p.block_size, p.bpp,
+                                p.start_tok ? p.start_tok[s] : 0);
     if (sp.nparts <= 1)
         return;
     const int np = sp.nparts;

@@ -260,7 +260,7 @@ __device__ inline void gqa_producer(const DecodeParams &p, const CUtensorMap *tm
     }
     int chunk_base = 0;
     long long chunk_prefix = 0;
-    int my_len = 0, my_np = 0, my_incl = 0, chunk_total = 0;
+    int my_len = 0, my_start = 0, my_np = 0, my_incl = 0, chunk_total = 0;
     bool chunk_ready = false;
     uint32_t t = 0;
     bool ok = true;
@@ -269,7 +269,7 @@ __device__ inline void gqa_producer(const DecodeParams &p, const CUtensorMap *tm
     for (long long w = blockIdx.x, k = 0;; w += gridDim.x, ++k) {
         const long long f = w / hkv;
         const int kvh = static_cast<int>(w % hkv);
-        int s = -1, part = 0, len = 0, nparts = 1;
+        int s = -1, part = 0, len = 0, start = 0, nparts = 1;
         for (;;) {
             if (!chunk_ready) {
                 if (chunk_base >= p.num_seqs)
@@ -278,7 +278,8 @@ __device__ inline void gqa_producer(const DecodeParams &p, const CUtensorMap *tm
                 my_len = sq < p.num_seqs ? ld_nc_i32(p.context_lens + sq) : 0;
                 if (sq < p.num_seqs && my_len > p.max_len && p.err)
                     atomicOr(p.err, PA_DEVERR_BAD_LEN);
-                my_np = sq < p.num_seqs ? seq_span(my_len, p.max_len, p.window, BS, p.bpp).nparts : 0;
+                my_start = (sq < p.num_seqs && p.start_tok) ? ld_nc_i32(p.start_tok + sq) : 0;
+                my_np = sq < p.num_seqs ? seq_span(my_len, p.max_len, p.window, BS, p.bpp, my_start).nparts : 0;
                 my_incl = my_np;
 #pragma unroll
                 for (int o = 1; o < 32; o <<= 1) {
@@ -296,6 +297,7 @@ __device__ inline void gqa_producer(const DecodeParams &p, const CUtensorMap *tm
                 const int incl_j = __shfl_sync(0xffffffffu, my_incl, j);
                 nparts = __shfl_sync(0xffffffffu, my_np, j);
                 len = __shfl_sync(0xffffffffu, my_len, j);
+                start = __shfl_sync(0xffffffffu, my_start, j);
                 part = static_cast<int>(f - (chunk_prefix + incl_j - nparts));
                 break;
             }
@@ -316,7 +318,7 @@ __device__ inline void gqa_producer(const DecodeParams &p, const CUtensorMap *tm
             __syncwarp();
             break;
         }
-        const SeqSpan sp = seq_span(len, p.max_len, p.window, BS, p.bpp);
+        const SeqSpan sp = seq_span(len, p.max_len, p.window, BS, p.bpp, start);
         const int blk_lo = sp.b0 + part * p.bpp;
         const int nb = max(0, min(p.bpp, sp.nblk - part * p.bpp));
         const int ntiles = (nb + C::kBpt - 1) / C::kBpt;
@@ -617,7 +619,7 @@ __device__ inline bool gqa_softmax(const DecodeParams &p, char *smem, const GqaL
                     den = fmaf(all[w * 2 * G + G + h], sc, den);
                 }
             }
-            if (it.nparts == 1) {
+            if (it.nparts == 1 && !p.force_partial) {
                 store_out(p.out, p.out_dtype, (row0 + h) * C::kD + row, den > 0.f ? num / den : 0.f);
             } else {
                 const long long pr = (row0 + h) * p.max_parts + it.part;
@@ -645,11 +647,21 @@ __device__ inline bool gqa_softmax(const DecodeParams &p, char *smem, const GqaL
         if (it.end)
             break;
         const int ntiles = (it.nb + C::kBpt - 1) / C::kBpt;
-        if (ntiles == 0) {  // no attended token: zeros, nothing to accumulate
+        if (ntiles == 0) {  // no attended token: zeros (or an empty partial), nothing to accumulate
             const long long row0 = static_cast<long long>(it.s) * p.num_heads + static_cast<long long>(it.kvh) * G;
 #pragma unroll
-            for (int h = 0; h < G; ++h)
-                store_out(p.out, p.out_dtype, (row0 + h) * C::kD + row, 0.f);
+            for (int h = 0; h < G; ++h) {
+                if (!p.force_partial) {
+                    store_out(p.out, p.out_dtype, (row0 + h) * C::kD + row, 0.f);
+                } else {
+                    const long long pr = (row0 + h) * p.max_parts + it.part;
+                    p.part_acc[pr * C::kD + row] = 0.f;
+                    if (row == 0) {
+                        p.part_ml[pr * 2] = -INFINITY;
+                        p.part_ml[pr * 2 + 1] = 0.f;
+                    }
+                }
+            }
             continue;
         }
 #pragma unroll

@@ -260,7 +260,7 @@ __device__ inline void mha_producer(const DecodeParams &p, const CUtensorMap *tm
 
     int chunk_base = 0;
     long long chunk_prefix = 0;
-    int my_len = 0, my_np = 0, my_incl = 0, chunk_total = 0;
+    int my_len = 0, my_start = 0, my_np = 0, my_incl = 0, chunk_total = 0;
     bool chunk_ready = false;
     uint32_t t = 0;  // stages issued
     int k = 0;       // items issued
@@ -270,7 +270,7 @@ __device__ inline void mha_producer(const DecodeParams &p, const CUtensorMap *tm
     for (long long w = blockIdx.x;; w += gridDim.x) {
         const long long f = w / hkv;
         const int kvh = static_cast<int>(w % hkv);
-        int s = -1, part = 0, len = 0, nparts = 1;
+        int s = -1, part = 0, len = 0, start = 0, nparts = 1;
         for (;;) {
             if (!chunk_ready) {
                 if (chunk_base >= p.num_seqs)
@@ -279,7 +279,8 @@ __device__ inline void mha_producer(const DecodeParams &p, const CUtensorMap *tm
                 my_len = sq < p.num_seqs ? ld_nc_i32(p.context_lens + sq) : 0;
                 if (sq < p.num_seqs && my_len > p.max_len && p.err)
                     atomicOr(p.err, PA_DEVERR_BAD_LEN);
-                my_np = sq < p.num_seqs ? seq_span(my_len, p.max_len, p.window, BS, p.bpp).nparts : 0;
+                my_start = (sq < p.num_seqs && p.start_tok) ? ld_nc_i32(p.start_tok + sq) : 0;
+                my_np = sq < p.num_seqs ? seq_span(my_len, p.max_len, p.window, BS, p.bpp, my_start).nparts : 0;
                 my_incl = my_np;
 #pragma unroll
                 for (int o = 1; o < 32; o <<= 1) {
@@ -297,6 +298,7 @@ __device__ inline void mha_producer(const DecodeParams &p, const CUtensorMap *tm
                 const int incl_j = __shfl_sync(0xffffffffu, my_incl, j);
                 nparts = __shfl_sync(0xffffffffu, my_np, j);
                 len = __shfl_sync(0xffffffffu, my_len, j);
+                start = __shfl_sync(0xffffffffu, my_start, j);
                 part = static_cast<int>(f - (chunk_prefix + incl_j - nparts));
                 break;
             }
@@ -318,7 +320,7 @@ __device__ inline void mha_producer(const DecodeParams &p, const CUtensorMap *tm
             __syncwarp();
             break;
         }
-        const SeqSpan sp = seq_span(len, p.max_len, p.window, BS, p.bpp);
+        const SeqSpan sp = seq_span(len, p.max_len, p.window, BS, p.bpp, start);
         const int blk_lo = sp.b0 + part * p.bpp;
         const int nb = max(0, min(p.bpp, sp.nblk - part * p.bpp));
         if (lane == 0) {
@@ -553,7 +555,7 @@ __device__ inline void mha_consumer(const DecodeParams &p, char *smem, const Mha
 #pragma unroll
             for (int w2 = 0; w2 < kMhaWarps; ++w2)
                 num = fmaf(mscr[(b * kMhaWarps + w2) * D + dd], scl[w2], num);
-            if (it.nparts == 1) {
+            if (it.nparts == 1 && !p.force_partial) {
                 store_out(p.out, p.out_dtype, rowi * D + dd, den > 0.f ? num / den : 0.f);
             } else {
                 const long long pr = rowi * p.max_parts + it.part;

@@ -175,7 +175,9 @@ struct SeqSpan {
 
 // max_len = max_blocks_per_seq * block_size: a longer context would index past
 // the table row, so it is clamped (and the caller flags PA_DEVERR_BAD_LEN).
-__device__ inline SeqSpan seq_span(int L, int max_len, int window, int block_size, int bpp) {
+// start_min (0 normally) moves the first attended token further up: the
+// shared-prefix decode uses it for the part of a context after the prefix.
+__device__ inline SeqSpan seq_span(int L, int max_len, int window, int block_size, int bpp, int start_min = 0) {
     SeqSpan sp;
     if (L < 0)
         L = 0;
@@ -183,8 +185,10 @@ __device__ inline SeqSpan seq_span(int L, int max_len, int window, int block_siz
         L = max_len;
     sp.end = L;
     sp.start = (window > 0 && L > window) ? L - window : 0;
+    if (start_min > sp.start)
+        sp.start = start_min < L ? start_min : L;
     sp.b0 = sp.start / block_size;
-    sp.nblk = L > 0 ? (L - 1) / block_size - sp.b0 + 1 : 0;
+    sp.nblk = L > sp.start ? (L - 1) / block_size - sp.b0 + 1 : 0;
     sp.nparts = sp.nblk > 0 ? (sp.nblk + bpp - 1) / bpp : 1;
     return sp;
 }

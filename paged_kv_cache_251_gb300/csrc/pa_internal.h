@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "pa.h"
+
 namespace pa {
 
 struct DecodeParams;
@@ -37,6 +39,11 @@ cudaError_t launch_copy_blocks(const int64_t *pairs, int num_pairs, void *k_cach
 cudaError_t launch_swap_blocks(const int64_t *pairs, int num_pairs, const void *src_k, const void *src_v,
                                void *dst_k, void *dst_v, long long block_bytes, int src_blocks, int dst_blocks,
                                uint32_t *err, int num_sms, cudaStream_t stream);
+
+// Choose the decode kernel for (dtype, head_dim, group G, block size), encode
+// its tensor maps and launch it on `cs` with the filled-in parameters (the
+// stage count is set there).  The partition reduce is the caller's.
+pa_status launch_decode_kernel(DecodeParams &p, int dtype, int head_dim, int G, cudaStream_t cs);
 
 // Text returned by pa_last_error_detail() on the calling thread.
 void set_last_error_detail(const char *why);

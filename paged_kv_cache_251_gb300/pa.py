@@ -45,6 +45,10 @@ def _load():
     lib.pa_append_kv.restype = I
     lib.pa_copy_blocks.argtypes = [P, I, P, P, I, I, I, I, I, P, P]
     lib.pa_copy_blocks.restype = I
+    lib.pa_decode_shared_prefix.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, F, I, I, I, I, I, P, SZ, P, P]
+    lib.pa_decode_shared_prefix.restype = I
+    lib.pa_decode_shared_prefix_workspace_size.argtypes = [I, I, I, I, I, I, I, I]
+    lib.pa_decode_shared_prefix_workspace_size.restype = SZ
     lib.pa_swap_blocks.argtypes = [P, I, P, P, P, P, I, I, I, I, I, I, P, P]
     lib.pa_swap_blocks.restype = I
     lib.pa_status_string.argtypes = [I]
@@ -120,6 +124,47 @@ def pa_decode(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_cache
                           _ptr(context_lens), N, H, num_kv_heads, d, bs, float(scale), int(window),
                           DTYPE_CODE[q.dtype], DTYPE_CODE[out.dtype], block_tables.shape[1], nb,
                           int(partition_size), _ptr(workspace), ws_bytes, _ptr(err_word), _stream(stream)))
+    return out
+
+
+def pa_decode_shared_prefix_workspace_size(num_seqs: int, num_heads: int, head_dim: int, block_size: int,
+                                           max_blocks_per_seq: int, partition_size: int, group_size: int,
+                                           dtype: torch.dtype) -> int:
+    return int(_lib.pa_decode_shared_prefix_workspace_size(num_seqs, num_heads, head_dim, block_size,
+                                                           max_blocks_per_seq, partition_size, group_size,
+                                                           DTYPE_CODE[dtype]))
+
+
+def pa_decode_shared_prefix(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                            block_tables: torch.Tensor, context_lens: torch.Tensor, shared_lens: torch.Tensor,
+                            group_size: int, num_kv_heads: int | None = None, scale: float | None = None,
+                            partition_size: int = 0, workspace: torch.Tensor | None = None,
+                            err_word: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """pa_decode for consecutive groups of group_size sequences whose first
+    shared_lens[g] tokens are the same blocks: each shared block is read once
+    per group (see include/pa.h)."""
+    _cuda(out, q, k_cache, v_cache, block_tables, context_lens, shared_lens, workspace, err_word)
+    N, H, d = q.shape
+    nb, hkv, bs, d2 = k_cache.shape
+    if num_kv_heads is None:
+        num_kv_heads = hkv
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    for t in (block_tables, context_lens, shared_lens):
+        if t.dtype != torch.int32:
+            raise TypeError("block_tables, context_lens and shared_lens must be int32")
+    if q.dtype != k_cache.dtype or v_cache.dtype != k_cache.dtype:
+        raise TypeError("q, k_cache and v_cache must share one dtype")
+    if workspace is None:
+        n = pa_decode_shared_prefix_workspace_size(N, H, d, bs, block_tables.shape[1], partition_size, group_size,
+                                                   q.dtype)
+        workspace = torch.empty(max(n, 16), dtype=torch.uint8, device=q.device)
+    _check(_lib.pa_decode_shared_prefix(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                                        _ptr(context_lens), _ptr(shared_lens), int(group_size), N, H, num_kv_heads,
+                                        d, bs, float(scale), DTYPE_CODE[q.dtype], DTYPE_CODE[out.dtype],
+                                        block_tables.shape[1], nb, int(partition_size), _ptr(workspace),
+                                        workspace.numel() * workspace.element_size(), _ptr(err_word),
+                                        _stream(stream)))
     return out
 
 
