@@ -21,8 +21,11 @@ import torch
 from . import build as _build
 from .cow import CowModel, RingModel  # noqa: F401  (re-exported)
 
-F32, F16, BF16 = 0, 1, 2
+F32, F16, BF16, I8, E4M3 = 0, 1, 2, 3, 4
 _DTYPE_CODE = {torch.float32: F32, torch.float16: F16, torch.bfloat16: BF16}
+# 8-bit caches: the code pools are carried as int8 / float8_e4m3fn tensors
+_CODE_FMT = {torch.int8: I8, torch.float8_e4m3fn: E4M3}
+_FMT_DTYPE = {I8: torch.int8, E4M3: torch.float8_e4m3fn, "int8": torch.int8, "e4m3": torch.float8_e4m3fn}
 
 _lib = None
 
@@ -51,6 +54,17 @@ def _bind(lib):
     lib.orc_swap_blocks.restype = I64
     lib.orc_element_to_double.argtypes = [P, I, I64]
     lib.orc_element_to_double.restype = D
+    lib.orc_code_to_double.argtypes = [ctypes.c_uint8, I]
+    lib.orc_code_to_double.restype = D
+    lib.orc_e4m3_encode.argtypes = [ctypes.c_float]
+    lib.orc_e4m3_encode.restype = ctypes.c_uint8
+    lib.orc_quantize_rows.argtypes = [P, I, I64, I, I, P, P]
+    lib.orc_quantize_rows.restype = I
+    lib.orc_paged_attention_cache.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, D, I, I, I, I, I, I,
+                                              P, I64, I, P]
+    lib.orc_paged_attention_cache.restype = I
+    lib.orc_append_kv_quant.argtypes = [P, P, P, P, P, P, P, I64, I, I, I, I, I, I]
+    lib.orc_append_kv_quant.restype = I64
     return lib
 
 
@@ -85,17 +99,70 @@ def to_double(t: torch.Tensor, lib=None) -> np.ndarray:
     return out.reshape(tuple(t.shape))
 
 
+def code_to_double(code: int, fmt, lib=None) -> float:
+    """Value of one 8-bit code (fmt: "int8" / "e4m3" or I8 / E4M3)."""
+    f = {"int8": I8, "e4m3": E4M3}.get(fmt, fmt)
+    return (lib or load()).orc_code_to_double(int(code) & 0xFF, int(f))
+
+
+def e4m3_encode(x: float, lib=None) -> int:
+    """The oracle's fp32 -> E4M3 code (nearest, ties to even, saturating)."""
+    return int((lib or load()).orc_e4m3_encode(float(x)))
+
+
+def quantize_rows(x: torch.Tensor, fmt, lib=None):
+    """Quantise the last axis of x (fp32/fp16/bf16) row by row.
+
+    Returns (codes, scales): codes of x's shape as int8 ("int8") or
+    float8_e4m3fn ("e4m3") holding the oracle's bytes, scales float32 of
+    x.shape[:-1].  Dequantised row: codes * scales[..., None].
+    """
+    lib = lib or load()
+    x = _cpu(x)
+    code_dtype = _FMT_DTYPE[fmt]
+    d = x.shape[-1]
+    rows = x.numel() // d if d else 0
+    codes = torch.zeros(x.shape, dtype=torch.uint8)
+    scales = torch.zeros(x.shape[:-1], dtype=torch.float32)
+    rc = lib.orc_quantize_rows(x.data_ptr(), _DTYPE_CODE[x.dtype], rows, d, _CODE_FMT[code_dtype],
+                               codes.data_ptr(), scales.data_ptr())
+    if rc != 0:
+        raise ValueError(f"oracle quantize_rows failed with code {rc}")
+    return codes.view(code_dtype), scales
+
+
+def dequantize(codes: torch.Tensor, scales: torch.Tensor, lib=None) -> np.ndarray:
+    """fp64 values code * scale, codes decoded by the oracle's own tables."""
+    lib = lib or load()
+    codes, scales = _cpu(codes), _cpu(scales)
+    fmt = _CODE_FMT[codes.dtype]
+    table = np.array([lib.orc_code_to_double(c, fmt) for c in range(256)], dtype=np.float64)
+    vals = table[codes.view(torch.uint8).numpy().astype(np.int64)]
+    return vals * scales.numpy().astype(np.float64)[..., None]
+
+
 def paged_attention(q, k_cache, v_cache, block_tables, context_lens, *, num_kv_heads: int,
                     scale: float, window: int = 0, pairs=None, invalid_policy: int = 0,
-                    threads: int = 1, lib=None, return_skipped: bool = False):
+                    threads: int = 1, lib=None, return_skipped: bool = False,
+                    k_scale=None, v_scale=None):
     """fp64 decode attention read through the block tables.
 
     q [N, H, d]; caches [num_blocks, H_kv, bs, d]; block_tables int32 [N, M];
     context_lens int32 [N].  ``pairs`` (int32 [P, 2] of (seq, head)) limits
     the work to those rows and returns [P, d]; otherwise [N, H, d].
+    8-bit caches (int8 / float8_e4m3fn code pools) take their row scales in
+    ``k_scale`` / ``v_scale`` (float32 [num_blocks, H_kv, bs]); every cached
+    value is then code * scale.
     """
     lib = lib or load()
     q, k_cache, v_cache = _cpu(q), _cpu(k_cache), _cpu(v_cache)
+    if k_cache.dtype in _CODE_FMT:
+        if v_cache.dtype != k_cache.dtype or k_scale is None or v_scale is None:
+            raise TypeError("8-bit caches need one code dtype and both scale pools")
+        return _paged_attention_cache(q, k_cache, v_cache, _cpu(k_scale).float().contiguous(),
+                                      _cpu(v_scale).float().contiguous(), block_tables, context_lens,
+                                      num_kv_heads, scale, window, pairs, invalid_policy, threads, lib,
+                                      return_skipped)
     if not (q.dtype == k_cache.dtype == v_cache.dtype):
         raise TypeError("q, k_cache and v_cache must share one dtype")
     bt = _cpu(block_tables).to(torch.int32).contiguous()
@@ -121,6 +188,57 @@ def paged_attention(q, k_cache, v_cache, block_tables, context_lens, *, num_kv_h
     return (out, skipped.value) if return_skipped else out
 
 
+def _paged_attention_cache(q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens, num_kv_heads,
+                           scale, window, pairs, invalid_policy, threads, lib, return_skipped):
+    bt = _cpu(block_tables).to(torch.int32).contiguous()
+    cl = _cpu(context_lens).to(torch.int32).contiguous()
+    N, H, d = q.shape
+    nb, hkv, bs, d2 = k_cache.shape
+    assert d2 == d and hkv == num_kv_heads and tuple(v_cache.shape) == tuple(k_cache.shape)
+    assert tuple(k_scale.shape) == (nb, hkv, bs) and tuple(v_scale.shape) == (nb, hkv, bs)
+    M = bt.shape[1]
+    if pairs is not None:
+        pr = torch.as_tensor(pairs, dtype=torch.int32).reshape(-1, 2).contiguous()
+        out = np.zeros((pr.shape[0], d), dtype=np.float64)
+        pptr, npairs = pr.data_ptr(), pr.shape[0]
+    else:
+        out = np.zeros((N, H, d), dtype=np.float64)
+        pptr, npairs = None, 0
+    skipped = ctypes.c_int64(0)
+    rc = lib.orc_paged_attention_cache(out.ctypes.data, q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                                       k_scale.data_ptr(), v_scale.data_ptr(), bt.data_ptr(), cl.data_ptr(),
+                                       N, H, num_kv_heads, d, bs, float(scale), int(window),
+                                       _DTYPE_CODE[q.dtype], _CODE_FMT[k_cache.dtype], M, nb, invalid_policy,
+                                       pptr, npairs, threads, ctypes.byref(skipped))
+    if rc != 0:
+        raise ValueError(f"oracle paged_attention failed with code {rc}")
+    return (out, skipped.value) if return_skipped else out
+
+
+def append_kv_quant(k_codes: torch.Tensor, v_codes: torch.Tensor, k_scales: torch.Tensor,
+                    v_scales: torch.Tensor, k, v, slot_mapping, lib=None) -> int:
+    """Quantise each token's K/V rows and store codes and scales at its slot,
+    in place on CPU tensors (codes int8 / float8_e4m3fn [nb, H_kv, bs, d],
+    scales float32 [nb, H_kv, bs]).  Returns the out-of-range slots skipped."""
+    lib = lib or load()
+    for t in (k_codes, v_codes, k_scales, v_scales):
+        assert t.device.type == "cpu" and t.is_contiguous()
+    k, v = _cpu(k), _cpu(v)
+    sm = _cpu(torch.as_tensor(slot_mapping)).to(torch.int64).contiguous()
+    nb, hkv, bs, d = k_codes.shape
+    rc = lib.orc_append_kv_quant(k_codes.data_ptr(), v_codes.data_ptr(), k_scales.data_ptr(),
+                                 v_scales.data_ptr(), k.data_ptr(), v.data_ptr(), sm.data_ptr(), sm.numel(),
+                                 hkv, d, bs, nb, _DTYPE_CODE[k.dtype], _CODE_FMT[k_codes.dtype])
+    if rc < 0:
+        raise ValueError(f"oracle append_kv_quant refused the input (code {rc})")
+    return int(rc)
+
+
+def _as_pool(t: torch.Tensor) -> torch.Tensor:
+    # a scale pool [nb, H_kv, bs] is a pool of one-element rows
+    return t.unsqueeze(-1) if t.dim() == 3 else t
+
+
 def append_kv(k_cache: torch.Tensor, v_cache: torch.Tensor, k, v, slot_mapping, lib=None) -> int:
     """Byte-copy each token's K/V rows into its slot, in place on CPU tensors.
     Returns the number of out-of-range slots that were skipped."""
@@ -141,6 +259,7 @@ def copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor, src_dst_pairs, lib
     place on CPU tensors.  Returns the number of out-of-range pairs skipped."""
     lib = lib or load()
     assert k_cache.device.type == "cpu" and k_cache.is_contiguous() and v_cache.is_contiguous()
+    k_cache, v_cache = _as_pool(k_cache), _as_pool(v_cache)
     pr = _cpu(torch.as_tensor(src_dst_pairs)).to(torch.int64).reshape(-1, 2).contiguous()
     nb, hkv, bs, d = k_cache.shape
     rc = lib.orc_copy_blocks(k_cache.data_ptr(), v_cache.data_ptr(), pr.data_ptr(), pr.shape[0],
@@ -156,7 +275,8 @@ def swap_blocks(src_k: torch.Tensor, src_v: torch.Tensor, dst_k: torch.Tensor, d
     pool (K and V), in place on CPU tensors.  Returns the out-of-range pairs."""
     lib = lib or load()
     assert dst_k.device.type == "cpu" and dst_k.is_contiguous() and dst_v.is_contiguous()
-    src_k, src_v = _cpu(src_k), _cpu(src_v)
+    src_k, src_v = _as_pool(_cpu(src_k)), _as_pool(_cpu(src_v))
+    dst_k, dst_v = _as_pool(dst_k), _as_pool(dst_v)
     pr = _cpu(torch.as_tensor(src_dst_pairs)).to(torch.int64).reshape(-1, 2).contiguous()
     snb, hkv, bs, d = src_k.shape
     dnb = dst_k.shape[0]

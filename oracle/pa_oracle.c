@@ -22,7 +22,11 @@
  *    核心要点: every generated token's key/value is saved and re-read.
  *  - "KV Cache与长上下文管理", section "让 Round Robin / Sliding Window 变成 O(1)
  *    操作": a sliding window is realised by recycling pages and rewriting the
- *    page table; the attended set is the most recent tokens.
+ *    page table; the attended set is the most recent tokens.  The same page's
+ *    KV-cache quantisation passage (FP16 -> INT8 -> INT4) and the mjmagnets
+ *    article's section 4.1 mixed-precision pages (INT8 for rarely used pages):
+ *    8-bit caches, read here as symmetric per-row quantisation (one fp32
+ *    scale per cached (token, kv head) row, the codes decided in fp32).
  */
 #include <math.h>
 #include <pthread.h>
@@ -30,7 +34,7 @@
 #include <stdlib.h>
 #include <string.h>
 
-enum { ORC_F32 = 0, ORC_F16 = 1, ORC_BF16 = 2 };
+enum { ORC_F32 = 0, ORC_F16 = 1, ORC_BF16 = 2, ORC_I8 = 3, ORC_E4M3 = 4 };
 
 /* ------------------------------------------------------------------ */
 /* Exact element conversions (every fp16/bf16/fp32 value is a double). */
@@ -76,6 +80,137 @@ double orc_element_to_double(const void *base, int dtype, int64_t index)
 }
 
 /* ------------------------------------------------------------------ */
+/* 8-bit codes.
+ *
+ * INT8: two's-complement byte, value = code.
+ * E4M3 (the OCP 8-bit floating-point format, E4M3 variant): sign bit, 4
+ * exponent bits with bias 7, 3 mantissa bits; exponent field 0 encodes the
+ * subnormals m/8 * 2^-6; there are no infinities, S.1111.111 is NaN, so the
+ * largest finite value is 1.75 * 2^8 = 448.
+ */
+static double orc_i8_to_double(uint8_t c)
+{
+    return (double)(c < 128 ? (int)c : (int)c - 256);
+}
+
+static double orc_e4m3_to_double(uint8_t c)
+{
+    const int sign = c >> 7, expo = (c >> 3) & 15, mant = c & 7;
+    double v;
+    if (expo == 15 && mant == 7)
+        v = NAN;
+    else if (expo == 0)
+        v = ldexp((double)mant, -9);              /* m/8 * 2^-6 */
+    else
+        v = ldexp((double)(8 + mant), expo - 10); /* (1 + m/8) * 2^(e-7) */
+    return sign ? -v : v;
+}
+
+double orc_code_to_double(uint8_t code, int fmt)
+{
+    return fmt == ORC_I8 ? orc_i8_to_double(code) : orc_e4m3_to_double(code);
+}
+
+/* Nearest E4M3 value to a finite float, ties to the even mantissa; finite
+ * values beyond 448 saturate to +-448.  The sign of zero is kept. */
+static uint8_t orc_e4m3_from_float(float f)
+{
+    const uint8_t sign = signbit(f) ? 0x80 : 0x00;
+    double a = fabs((double)f);
+    if (a >= 448.0)
+        return sign | 0x7e;                       /* 1.75 * 2^8 */
+    /* a lies in [2^b, 2^(b+1)); below 2^-6 the subnormals share the spacing
+     * of the lowest binade.  Spacing of representable values: 2^(b-3). */
+    int e2;
+    (void)frexp(a, &e2);                          /* a = f * 2^e2, f in [0.5, 1) */
+    int b = a > 0.0 ? e2 - 1 : -6;
+    if (b < -6)
+        b = -6;
+    const double quantum = ldexp(1.0, b - 3);
+    const double r = nearbyint(a / quantum);      /* exact division; ties to even */
+    const double v = r * quantum;                 /* at most 448 here */
+    if (v == 0.0)
+        return sign;
+    (void)frexp(v, &e2);
+    const int bv = e2 - 1;
+    if (bv < -6)                                  /* subnormal: v = m * 2^-9 */
+        return sign | (uint8_t)(int)ldexp(v, 9);
+    const int m = (int)ldexp(v, 3 - bv) - 8;      /* 1.mmm -> mmm */
+    return sign | (uint8_t)((bv + 7) << 3) | (uint8_t)m;
+}
+
+uint8_t orc_e4m3_encode(float f)
+{
+    return orc_e4m3_from_float(f);
+}
+
+/* Quantise one row of d elements (row `row` of x, dtype in_dtype):
+ *   amax  = max |x_j|                      (exact: every input is an fp32 value)
+ *   scale = amax / Q in fp32, Q = 127 (INT8) or 448 (E4M3)
+ *   code_j = INT8: round-half-even(x_j / scale) clamped to [-127, 127]
+ *            E4M3: nearest E4M3 value to x_j / scale (the quotient rounded
+ *                  to fp32 first, then to E4M3)
+ * A row of zeros gets scale 0 and zero codes.  Dequantised value:
+ * code_j * scale (exact in fp64). */
+static void orc_quantize_row(const void *x, int in_dtype, int64_t row, int d, int fmt, uint8_t *codes,
+                             float *scale)
+{
+    const int64_t first = row * d;
+    float amax = 0.0f;
+    for (int j = 0; j < d; ++j) {
+        const float a = fabsf((float)orc_load(x, in_dtype, first + j));
+        if (a > amax)
+            amax = a;
+    }
+    const float q = fmt == ORC_I8 ? 127.0f : 448.0f;
+    const float s = amax / q;
+    *scale = s;
+    for (int j = 0; j < d; ++j) {
+        if (s == 0.0f) {
+            codes[j] = 0;
+            continue;
+        }
+        const float v = (float)orc_load(x, in_dtype, first + j) / s;
+        if (fmt == ORC_I8) {
+            float r = rintf(v);
+            if (r > 127.0f)
+                r = 127.0f;
+            if (r < -127.0f)
+                r = -127.0f;
+            const int c = (int)r;
+            codes[j] = (uint8_t)(c < 0 ? c + 256 : c);
+        } else {
+            codes[j] = orc_e4m3_from_float(v);
+        }
+    }
+}
+
+/* Quantise num_rows rows of d elements: codes [num_rows][d], scales [num_rows].
+ * Returns 0, or -4 for a bad format / dtype. */
+int orc_quantize_rows(const void *x, int in_dtype, int64_t num_rows, int d, int fmt, uint8_t *codes,
+                      float *scales)
+{
+    if ((fmt != ORC_I8 && fmt != ORC_E4M3) || (in_dtype != ORC_F32 && in_dtype != ORC_F16 &&
+                                               in_dtype != ORC_BF16) || d <= 0)
+        return -4;
+    for (int64_t r = 0; r < num_rows; ++r)
+        orc_quantize_row(x, in_dtype, r, d, fmt, codes + r * d, &scales[r]);
+    return 0;
+}
+
+/* Value of cache element `elem` (index into [num_blocks][H_kv][bs][d]): the
+ * element itself for fp32/fp16/bf16 caches, code * scale of its row for
+ * 8-bit caches (scales laid out [num_blocks][H_kv][bs]). */
+static double orc_cache_value(const void *cache, const float *scales, int cache_dtype, int64_t elem, int d)
+{
+    if (cache_dtype == ORC_I8 || cache_dtype == ORC_E4M3) {
+        const uint8_t c = ((const uint8_t *)cache)[elem];
+        return orc_code_to_double(c, cache_dtype) * (double)scales[elem / d];
+    }
+    return orc_load(cache, cache_dtype, elem);
+}
+
+/* ------------------------------------------------------------------ */
 /* Address translation (案例 2): logical token -> (physical block, offset). */
 
 int orc_locate(const int32_t *block_table, int table_len, int block_size,
@@ -113,6 +248,8 @@ typedef struct {
     int num_seqs, num_heads, num_kv_heads, head_dim, block_size;
     double scale;
     int window, dtype, max_blocks_per_seq, num_blocks, invalid_policy;
+    int cache_dtype;                /* element type of k_cache / v_cache */
+    const float *k_scale, *v_scale; /* row scales of 8-bit caches (else unused) */
 } orc_args;
 
 static int orc_one(const orc_args *a, int s, int h, double *out_row, int64_t *skipped)
@@ -163,7 +300,8 @@ static int orc_one(const orc_args *a, int s, int h, double *out_row, int64_t *sk
         row[i] = (((int64_t)phys * a->num_kv_heads + kvh) * a->block_size + off) * d;
         double dot = 0.0;
         for (int j = 0; j < d; ++j)
-            dot += orc_load(a->q, a->dtype, q_base + j) * orc_load(a->k_cache, a->dtype, row[i] + j);
+            dot += orc_load(a->q, a->dtype, q_base + j) *
+                   orc_cache_value(a->k_cache, a->k_scale, a->cache_dtype, row[i] + j, d);
         x[i] = a->scale * dot;
     }
 
@@ -184,7 +322,7 @@ static int orc_one(const orc_args *a, int s, int h, double *out_row, int64_t *sk
         const double w = exp(x[i] - m);
         denom += w;
         for (int j = 0; j < d; ++j)
-            out_row[j] += w * orc_load(a->v_cache, a->dtype, row[i] + j);
+            out_row[j] += w * orc_cache_value(a->v_cache, a->v_scale, a->cache_dtype, row[i] + j, d);
     }
     for (int j = 0; j < d; ++j)
         out_row[j] /= denom;
@@ -230,20 +368,26 @@ static void *orc_worker(void *p)
  * Returns 0, or a negative error; *skipped_out (nullable) receives the number
  * of tokens left out under invalid_policy 1.
  */
-int orc_paged_attention(double *out, const void *q, const void *k_cache, const void *v_cache,
-                        const int32_t *block_tables, const int32_t *context_lens,
-                        int num_seqs, int num_heads, int num_kv_heads, int head_dim,
-                        int block_size, double scale, int window, int dtype,
-                        int max_blocks_per_seq, int num_blocks, int invalid_policy,
-                        const int32_t *pairs, int64_t num_pairs, int num_threads,
-                        int64_t *skipped_out)
+/* Same, for a cache of cache_dtype (fp32/fp16/bf16, or 8-bit codes with row
+ * scales k_scale / v_scale) and queries of q_dtype. */
+int orc_paged_attention_cache(double *out, const void *q, const void *k_cache, const void *v_cache,
+                              const float *k_scale, const float *v_scale,
+                              const int32_t *block_tables, const int32_t *context_lens,
+                              int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                              int block_size, double scale, int window, int q_dtype, int cache_dtype,
+                              int max_blocks_per_seq, int num_blocks, int invalid_policy,
+                              const int32_t *pairs, int64_t num_pairs, int num_threads,
+                              int64_t *skipped_out)
 {
+    const int quant = cache_dtype == ORC_I8 || cache_dtype == ORC_E4M3;
     if (num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads != 0 || head_dim <= 0 ||
-        block_size <= 0 || (dtype != ORC_F32 && dtype != ORC_F16 && dtype != ORC_BF16))
+        block_size <= 0 || (q_dtype != ORC_F32 && q_dtype != ORC_F16 && q_dtype != ORC_BF16) ||
+        (!quant && cache_dtype != ORC_F32 && cache_dtype != ORC_F16 && cache_dtype != ORC_BF16) ||
+        (quant && (!k_scale || !v_scale)))
         return -4;
     orc_args a = {q, k_cache, v_cache, block_tables, context_lens, num_seqs, num_heads,
-                  num_kv_heads, head_dim, block_size, scale, window, dtype,
-                  max_blocks_per_seq, num_blocks, invalid_policy};
+                  num_kv_heads, head_dim, block_size, scale, window, q_dtype,
+                  max_blocks_per_seq, num_blocks, invalid_policy, cache_dtype, k_scale, v_scale};
     const int64_t items = pairs ? num_pairs : (int64_t)num_seqs * num_heads;
     if (pairs)
         for (int64_t i = 0; i < num_pairs; ++i)
@@ -283,6 +427,22 @@ int orc_paged_attention(double *out, const void *q, const void *k_cache, const v
     return status;
 }
 
+int orc_paged_attention(double *out, const void *q, const void *k_cache, const void *v_cache,
+                        const int32_t *block_tables, const int32_t *context_lens,
+                        int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                        int block_size, double scale, int window, int dtype,
+                        int max_blocks_per_seq, int num_blocks, int invalid_policy,
+                        const int32_t *pairs, int64_t num_pairs, int num_threads,
+                        int64_t *skipped_out)
+{
+    if (dtype != ORC_F32 && dtype != ORC_F16 && dtype != ORC_BF16)
+        return -4;
+    return orc_paged_attention_cache(out, q, k_cache, v_cache, NULL, NULL, block_tables, context_lens,
+                                     num_seqs, num_heads, num_kv_heads, head_dim, block_size, scale,
+                                     window, dtype, dtype, max_blocks_per_seq, num_blocks,
+                                     invalid_policy, pairs, num_pairs, num_threads, skipped_out);
+}
+
 /* ------------------------------------------------------------------ */
 /* Append: "each generated token's key/value is saved" into its slot
  * (核心要点), with slot = physical * block_size + offset (案例 2).
@@ -318,6 +478,46 @@ int64_t orc_append_kv(void *k_cache, void *v_cache, const void *k, const void *v
             const int64_t src_row = i * num_kv_heads + h;
             memcpy((char *)k_cache + dst_row * row_bytes, (const char *)k + src_row * row_bytes, row_bytes);
             memcpy((char *)v_cache + dst_row * row_bytes, (const char *)v + src_row * row_bytes, row_bytes);
+        }
+    }
+    return bad;
+}
+
+/* Quantise-on-append: token i's K and V rows (in_dtype) are quantised row by
+ * row (orc_quantize_row) and the codes and scale stored at the token's slot
+ * of the 8-bit pools: codes [num_blocks][H_kv][bs][d], scales
+ * [num_blocks][H_kv][bs].  Slots as orc_append_kv (padding, out-of-range
+ * count, duplicates refused). */
+int64_t orc_append_kv_quant(void *k_codes, void *v_codes, float *k_scales, float *v_scales, const void *k,
+                            const void *v, const int64_t *slot_mapping, int64_t num_tokens, int num_kv_heads,
+                            int head_dim, int block_size, int num_blocks, int in_dtype, int fmt)
+{
+    if ((fmt != ORC_I8 && fmt != ORC_E4M3) ||
+        (in_dtype != ORC_F32 && in_dtype != ORC_F16 && in_dtype != ORC_BF16))
+        return -4;
+    const int64_t pool_slots = (int64_t)num_blocks * block_size;
+    for (int64_t i = 0; i < num_tokens; ++i)
+        for (int64_t j = 0; j < i; ++j)
+            if (slot_mapping[i] >= 0 && slot_mapping[i] == slot_mapping[j])
+                return -2;
+    int64_t bad = 0;
+    for (int64_t i = 0; i < num_tokens; ++i) {
+        const int64_t slot = slot_mapping[i];
+        if (slot < 0)
+            continue;
+        if (slot >= pool_slots) {
+            ++bad;
+            continue;
+        }
+        const int64_t phys = slot / block_size;
+        const int64_t off = slot % block_size;
+        for (int h = 0; h < num_kv_heads; ++h) {
+            const int64_t dst_row = (phys * num_kv_heads + h) * block_size + off;
+            const int64_t src_row = i * num_kv_heads + h;
+            orc_quantize_row(k, in_dtype, src_row, head_dim, fmt, (uint8_t *)k_codes + dst_row * head_dim,
+                             &k_scales[dst_row]);
+            orc_quantize_row(v, in_dtype, src_row, head_dim, fmt, (uint8_t *)v_codes + dst_row * head_dim,
+                             &v_scales[dst_row]);
         }
     }
     return bad;

@@ -64,3 +64,94 @@ def test_planted_mistake_is_caught(name):
     assert SRC.count(old) == 1, f"mutation site for {name} not found"
     lib = oracle.load(obuild.build_from_text(SRC.replace(old, new), name))
     assert not _pins_pass(lib)
+
+
+# ---------------------------------------------------------------------------
+# 8-bit cache: mistakes in the quantiser, the code tables and the dequantised read
+
+QUANT_MUTANTS = {
+    "int8_scale_over_128": ("const float q = fmt == ORC_I8 ? 127.0f : 448.0f;",
+                            "const float q = fmt == ORC_I8 ? 128.0f : 448.0f;"),
+    "int8_truncates": ("float r = rintf(v);", "float r = truncf(v);"),
+    "e4m3_bias_off_by_one": ("v = ldexp((double)(8 + mant), expo - 10);",
+                             "v = ldexp((double)(8 + mant), expo - 9);"),
+    "e4m3_ties_away_from_zero": ("const double r = nearbyint(a / quantum);",
+                                 "const double r = floor(a / quantum + 0.5);"),
+    "e4m3_no_subnormal_floor": ("    if (b < -6)\n        b = -6;\n    const double quantum",
+                                "    const double quantum"),
+    "v_read_with_k_scale": ("orc_cache_value(a->v_cache, a->v_scale, a->cache_dtype, row[i] + j, d)",
+                            "orc_cache_value(a->v_cache, a->k_scale, a->cache_dtype, row[i] + j, d)"),
+    "scale_indexed_by_block": ("* (double)scales[elem / d];", "* (double)scales[elem / d / 16];"),
+    "append_k_codes_from_v": (
+        "orc_quantize_row(k, in_dtype, src_row, head_dim, fmt, (uint8_t *)k_codes",
+        "orc_quantize_row(v, in_dtype, src_row, head_dim, fmt, (uint8_t *)k_codes"),
+}
+
+
+def _quant_pins_pass(lib) -> bool:
+    from test_oracle_quant import _quant_identity_case, _torch_dequant
+    import torch.nn.functional as F
+    from paged_kv_cache_251_gb300 import workloads as wl
+    # code tables and the encoder against torch's float8_e4m3fn
+    for c in range(256):
+        want = torch.tensor([c], dtype=torch.uint8).view(torch.float8_e4m3fn).to(torch.float64).item()
+        got = oracle.code_to_double(c, "e4m3", lib=lib)
+        if not (math.isnan(want) and math.isnan(got)) and got != want:
+            return False
+    g = wl.uniform01(7, 1, 2000).double().numpy()
+    vals = np.concatenate([g * 464.0, g * 2.0 ** -6, -g * 3.0]).astype(np.float32)
+    want = torch.from_numpy(vals).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    ties = np.array([1.0625, 1.1875, 2.0 ** -10, 3 * 2.0 ** -10], dtype=np.float32)
+    if any(oracle.e4m3_encode(float(v), lib=lib) != w for v, w in zip(vals, want)):
+        return False
+    if [oracle.e4m3_encode(float(v), lib=lib) for v in ties] != [0x38, 0x3A, 0x00, 0x02]:
+        return False
+    # int8 rows: scale, the largest element at +-127, the rounding bound
+    x = wl.normal_tensor(21, 1, (16, 128), dtype=torch.float16)
+    codes, s = oracle.quantize_rows(x, "int8", lib=lib)
+    c, xf = codes.to(torch.int64), x.double()
+    if not torch.equal(s, xf.abs().amax(dim=1).float() / 127.0):
+        return False
+    if not torch.equal(c[torch.arange(16), xf.abs().argmax(dim=1)].abs(), torch.full((16,), 127)):
+        return False
+    if not bool(((xf - c.double() * s.double()[:, None]).abs() <= s.double()[:, None] * (0.5 + 1e-5)).all()):
+        return False
+    # attention over a quantised cache against torch SDPA on torch-decoded values
+    for fmt in ("int8", "e4m3"):
+        q, kc, vc, ks, vs, t, cl, M = _quant_identity_case(2, 4, 2, 64, 16, torch.float16, fmt, [40, 21], seed=5)
+        got = oracle.paged_attention(q, kc, vc, t, cl, num_kv_heads=2, scale=0.125, k_scale=ks, v_scale=vs, lib=lib)
+        kd = _torch_dequant(kc, ks).reshape(2, M, 2, 16, 64).permute(0, 2, 1, 3, 4).reshape(2, 2, M * 16, 64)
+        vd = _torch_dequant(vc, vs).reshape(2, M, 2, 16, 64).permute(0, 2, 1, 3, 4).reshape(2, 2, M * 16, 64)
+        for si in range(2):
+            L = int(cl[si])
+            ref = F.scaled_dot_product_attention(q[si].double().unsqueeze(1), kd[si, :, :L].repeat_interleave(2, 0),
+                                                 vd[si, :, :L].repeat_interleave(2, 0), scale=0.125).squeeze(1)
+            if not np.allclose(got[si], ref.numpy(), rtol=1e-12, atol=1e-13):
+                return False
+    # quantise-on-append stores each row's quantisation at its slot
+    kc = torch.zeros((4, 2, 16, 64), dtype=torch.int8)
+    vc = torch.zeros_like(kc)
+    ks, vs = torch.zeros(4, 2, 16), torch.zeros(4, 2, 16)
+    k = wl.normal_tensor(30, 1, (3, 2, 64), dtype=torch.float16)
+    v = wl.normal_tensor(30, 2, (3, 2, 64), dtype=torch.float16)
+    oracle.append_kv_quant(kc, vc, ks, vs, k, v, torch.tensor([5, 17, 40]), lib=lib)
+    kq, kqs = oracle.quantize_rows(k, "int8")
+    vq, vqs = oracle.quantize_rows(v, "int8")
+    for i, sl in enumerate([5, 17, 40]):
+        p_, o_ = sl // 16, sl % 16
+        if not (torch.equal(kc[p_, :, o_], kq[i]) and torch.equal(vc[p_, :, o_], vq[i])
+                and torch.equal(ks[p_, :, o_], kqs[i]) and torch.equal(vs[p_, :, o_], vqs[i])):
+            return False
+    return True
+
+
+def test_unmodified_oracle_passes_the_quant_pins():
+    assert _quant_pins_pass(oracle.load())
+
+
+@pytest.mark.parametrize("name", sorted(QUANT_MUTANTS))
+def test_planted_quantiser_mistake_is_caught(name):
+    old, new = QUANT_MUTANTS[name]
+    assert SRC.count(old) == 1, f"mutation site for {name} not found"
+    lib = oracle.load(obuild.build_from_text(SRC.replace(old, new), name))
+    assert not _quant_pins_pass(lib)
