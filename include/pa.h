@@ -83,7 +83,13 @@ typedef enum {
     PA_ERR_NO_BLOCKS = 5         /* block manager: the free list is empty */
 } pa_status;
 
-typedef enum { PA_F32 = 0, PA_F16 = 1, PA_BF16 = 2 } pa_dtype;
+typedef enum {
+    PA_F32 = 0,
+    PA_F16 = 1,
+    PA_BF16 = 2,
+    PA_I8 = 3,   /* 8-bit cache codes: two's-complement integers (with row scales) */
+    PA_E4M3 = 4  /* 8-bit cache codes: OCP FP8 E4M3 (with row scales) */
+} pa_dtype;
 
 /* Bits OR-ed into *err_word by the kernels. */
 #define PA_DEVERR_BAD_BLOCK 0x1u /* decode: table entry outside [0, num_blocks); its tokens were left out */
@@ -251,6 +257,62 @@ PA_API pa_status pa_swap_blocks(const int64_t *src_dst_pairs, int num_pairs, con
                                 const void *src_v, void *dst_k, void *dst_v, int src_num_blocks,
                                 int dst_num_blocks, int num_kv_heads, int head_dim, int block_size,
                                 pa_dtype dtype, uint32_t *err_word, pa_stream_t stream);
+
+/*
+ * 8-bit KV cache ["KV Cache与长上下文管理": KV-cache quantisation FP16 -> INT8
+ * halves the cache; the mjmagnets article, section 4.1: INT8 pages].  The
+ * pages fix no scale granularity; this library keeps one fp32 scale per
+ * cached (token, kv head) row, so an append quantises only its own rows:
+ *   amax = max_j |x_j|,  scale = amax / Q  (one fp32 division; Q = 127 for
+ *   PA_I8, 448 for PA_E4M3),
+ *   code_j = PA_I8:   round-half-even(x_j / scale) clamped to [-127, 127]
+ *            PA_E4M3: x_j / scale (fp32) rounded to the nearest E4M3 value,
+ *                     ties to even, saturating at +-448,
+ * a row of zeros storing scale 0 and zero codes.  The cached value of an
+ * element is code * scale.
+ * Pools: k_cache / v_cache hold the codes, one byte per element, in the
+ * layout of the 16-bit caches; k_scale / v_scale are fp32
+ * [num_blocks][num_kv_heads][block_size] (16-byte aligned).
+ */
+
+/*
+ * Quantise-on-append: token i's K and V rows (dtype PA_F32 / PA_F16 /
+ * PA_BF16, [num_tokens][num_kv_heads][head_dim]) are quantised row by row as
+ * above and their codes and scales written at slot_mapping[i] (padding and
+ * out-of-range slots as pa_append_kv).  cache_dtype is PA_I8 or PA_E4M3.
+ */
+PA_API pa_status pa_append_kv_quant(const void *k, const void *v, const int64_t *slot_mapping, void *k_cache,
+                                    void *v_cache, float *k_scale, float *v_scale, int num_tokens,
+                                    int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                                    pa_dtype dtype, pa_dtype cache_dtype, uint32_t *err_word,
+                                    pa_stream_t stream);
+
+/*
+ * pa_decode over an 8-bit cache: the same attention with every cached
+ * element read as code * scale of its row.  q (dtype PA_F32 / PA_F16 /
+ * PA_BF16) and out as pa_decode; cache_dtype PA_I8 or PA_E4M3; the workspace
+ * is pa_decode_workspace_size() bytes, as for pa_decode.
+ */
+PA_API pa_status pa_decode_quant(void *out, const void *q, const void *k_cache, const void *v_cache,
+                                 const float *k_scale, const float *v_scale, const int32_t *block_tables,
+                                 const int32_t *context_lens, int num_seqs, int num_heads, int num_kv_heads,
+                                 int head_dim, int block_size, float scale, int window, pa_dtype dtype,
+                                 pa_dtype cache_dtype, pa_dtype out_dtype, int max_blocks_per_seq,
+                                 int num_blocks, int partition_size, void *workspace, size_t workspace_bytes,
+                                 uint32_t *err_word, pa_stream_t stream);
+
+/* pa_copy_blocks for an 8-bit cache: codes and scales of each pair's block. */
+PA_API pa_status pa_copy_blocks_quant(const int64_t *src_dst_pairs, int num_pairs, void *k_cache, void *v_cache,
+                                      float *k_scale, float *v_scale, int num_kv_heads, int head_dim,
+                                      int block_size, int num_blocks, uint32_t *err_word, pa_stream_t stream);
+
+/* pa_swap_blocks for 8-bit pools: codes and scales (either side may be
+ * GPU-addressable host memory, as pa_swap_blocks). */
+PA_API pa_status pa_swap_blocks_quant(const int64_t *src_dst_pairs, int num_pairs, const void *src_k,
+                                      const void *src_v, const float *src_k_scale, const float *src_v_scale,
+                                      void *dst_k, void *dst_v, float *dst_k_scale, float *dst_v_scale,
+                                      int src_num_blocks, int dst_num_blocks, int num_kv_heads, int head_dim,
+                                      int block_size, uint32_t *err_word, pa_stream_t stream);
 
 /* Static text for a status code. */
 PA_API const char *pa_status_string(pa_status status);

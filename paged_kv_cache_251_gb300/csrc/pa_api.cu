@@ -17,6 +17,7 @@
 #include "pa_decode.cuh"
 #include "pa_decode_gqa.cuh"
 #include "pa_decode_mha.cuh"
+#include "pa_decode_q8.cuh"
 #include "pa_internal.h"
 
 namespace pa {
@@ -45,6 +46,7 @@ pa_status cuda_fail(cudaError_t e, const char *what) {
 
 int elt_bytes(int dtype) { return dtype == PA_F32 ? 4 : 2; }
 bool dtype_ok(int dtype) { return dtype == PA_F32 || dtype == PA_F16 || dtype == PA_BF16; }
+bool code_dtype_ok(int dtype) { return dtype == PA_I8 || dtype == PA_E4M3; }
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool block_size_ok(int bs) { return bs == 8 || bs == 16 || bs == 32; }
 bool head_dim_ok(int d) { return d == 64 || d == 128; }
@@ -307,6 +309,37 @@ pa_status launch_decode_kernel(DecodeParams &p, int dtype, int head_dim, int G, 
     return PA_OK;
 }
 
+pa_status launch_decode_q8_kernel(DecodeParams &p, int cache_dtype, int head_dim, int G, cudaStream_t cs) {
+    const void *fn = cache_dtype == PA_I8 ? decode_q8_kernel_i8(head_dim, G) : decode_q8_kernel_e4m3(head_dim, G);
+    if (!fn)
+        return fail(PA_ERR_UNSUPPORTED, "no 8-bit-cache decode kernel for this head_dim / group");
+    const int stage = static_cast<int>(q8_stage_bytes(p.block_size, head_dim));
+    int S = kStageBudget / stage;
+    S = S < 2 ? 2 : (S > 16 ? 16 : S);
+    p.stages = S;
+    const size_t smem = q8_smem_layout(S, p.block_size, G, head_dim).total;
+    int dev = 0, sms = 0, per_sm = 0;
+    cudaError_t e = device_sms(&dev, &sms);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "device query");
+    e = prepare_kernel(dev, fn, smem, kDecodeThreads, &per_sm);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "decode kernel set-up");
+    if (per_sm < 1)
+        return fail(PA_ERR_UNSUPPORTED, "decode kernel does not fit on an SM");
+    const long long items_max = static_cast<long long>(p.num_seqs) * p.num_kv_heads * p.max_parts;
+    long long grid = static_cast<long long>(sms) * per_sm;
+    if (grid > items_max)
+        grid = items_max;
+    if (grid < 1)
+        grid = 1;
+    void *args[] = {&p};
+    e = cudaLaunchKernel(fn, dim3(static_cast<unsigned>(grid)), dim3(kDecodeThreads), args, smem, cs);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "decode launch");
+    return PA_OK;
+}
+
 }  // namespace pa
 
 using namespace pa;
@@ -383,6 +416,9 @@ pa_status pa_decode(void *out, const void *q, const void *k_cache, const void *v
     p.scale_log2 = scale * 1.4426950408889634f;
     p.start_tok = nullptr;
     p.force_partial = 0;
+    p.k_scale = nullptr;
+    p.v_scale = nullptr;
+    p.q_dtype = dtype;
 
     const pa_status ls = launch_decode_kernel(p, dtype, head_dim, G, reinterpret_cast<cudaStream_t>(stream));
     if (ls != PA_OK)
@@ -492,6 +528,194 @@ pa_status pa_swap_blocks(const int64_t *src_dst_pairs, int num_pairs, const void
         static_cast<long long>(num_kv_heads) * block_size * head_dim * elt_bytes(dtype);
     e = launch_swap_blocks(src_dst_pairs, num_pairs, src_k, src_v, dst_k, dst_v, block_bytes, src_num_blocks,
                            dst_num_blocks, err_word, sms, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+        return cuda_fail(e, "swap_blocks launch");
+    return PA_OK;
+}
+
+pa_status pa_decode_quant(void *out, const void *q, const void *k_cache, const void *v_cache, const float *k_scale,
+                          const float *v_scale, const int32_t *block_tables, const int32_t *context_lens,
+                          int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size, float scale,
+                          int window, pa_dtype dtype, pa_dtype cache_dtype, pa_dtype out_dtype,
+                          int max_blocks_per_seq, int num_blocks, int partition_size, void *workspace,
+                          size_t workspace_bytes, uint32_t *err_word, pa_stream_t stream) {
+    g_detail.clear();
+    DecodePlan plan;
+    pa_status st = plan_decode(num_seqs, num_heads, head_dim, block_size, max_blocks_per_seq, window,
+                               partition_size, &plan);
+    if (st != PA_OK)
+        return st;
+    if (num_seqs == 0)
+        return PA_OK;
+    if (!out || !q || !k_cache || !v_cache || !k_scale || !v_scale || !block_tables || !context_lens)
+        return fail(PA_ERR_INVALID_ARGUMENT, "null pointer");
+    if (num_kv_heads <= 0 || num_heads % num_kv_heads != 0)
+        return fail(PA_ERR_INVALID_ARGUMENT, "num_heads must be a multiple of num_kv_heads");
+    const int G = num_heads / num_kv_heads;
+    if (G != 1 && G != 2 && G != 4 && G != 8)
+        return fail(PA_ERR_UNSUPPORTED, "num_heads / num_kv_heads must be 1, 2, 4 or 8");
+    if (!dtype_ok(dtype) || !dtype_ok(out_dtype) || !code_dtype_ok(cache_dtype))
+        return fail(PA_ERR_INVALID_ARGUMENT, "unknown dtype (q and out: PA_F32/F16/BF16; cache: PA_I8/PA_E4M3)");
+    if (num_blocks <= 0)
+        return fail(PA_ERR_INVALID_ARGUMENT, "num_blocks must be positive");
+    if (!std::isfinite(scale))
+        return fail(PA_ERR_INVALID_ARGUMENT, "scale must be finite");
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(k_scale) || !aligned16(v_scale))
+        return fail(PA_ERR_INVALID_ARGUMENT, "q, the code pools and the scale pools must be 16-byte aligned");
+    if ((reinterpret_cast<uintptr_t>(out) & (elt_bytes(out_dtype) - 1)) != 0)
+        return fail(PA_ERR_INVALID_ARGUMENT, "out is not aligned to its element size");
+    if (plan.workspace > 0 && (workspace == nullptr || workspace_bytes < plan.workspace))
+        return fail(PA_ERR_WORKSPACE_TOO_SMALL, "workspace smaller than pa_decode_workspace_size()");
+    if (plan.workspace > 0 && !aligned16(workspace))
+        return fail(PA_ERR_INVALID_ARGUMENT, "workspace must be 16-byte aligned");
+
+    DecodeParams p;
+    p.out = out;
+    p.q = q;
+    p.k_cache = k_cache;
+    p.v_cache = v_cache;
+    p.block_tables = block_tables;
+    p.context_lens = context_lens;
+    const size_t acc_floats = static_cast<size_t>(num_seqs) * num_heads * plan.max_parts * head_dim;
+    p.part_acc = plan.workspace ? static_cast<float *>(workspace) : nullptr;
+    p.part_ml = plan.workspace ? static_cast<float *>(workspace) + acc_floats : nullptr;
+    p.err = err_word;
+    p.num_seqs = num_seqs;
+    p.num_heads = num_heads;
+    p.num_kv_heads = num_kv_heads;
+    p.block_size = block_size;
+    p.window = window;
+    p.max_blocks_per_seq = max_blocks_per_seq;
+    p.max_len = static_cast<int>(std::min<long long>(static_cast<long long>(max_blocks_per_seq) * block_size, INT_MAX));
+    p.num_blocks = num_blocks;
+    p.bpp = plan.bpp;
+    p.max_parts = plan.max_parts;
+    p.out_dtype = out_dtype;
+    p.stages = 0;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.start_tok = nullptr;
+    p.force_partial = 0;
+    p.k_scale = k_scale;
+    p.v_scale = v_scale;
+    p.q_dtype = dtype;
+
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    const pa_status ls = launch_decode_q8_kernel(p, cache_dtype, head_dim, G, cs);
+    if (ls != PA_OK)
+        return ls;
+    if (plan.max_parts > 1) {
+        void *args[] = {&p};
+        const long long rows = static_cast<long long>(num_seqs) * num_heads;
+        cudaError_t e = cudaLaunchKernel(reduce_kernel(head_dim), dim3(static_cast<unsigned>(rows)),
+                                         dim3(kReduceThreads), args, 0, cs);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "reduce launch");
+    }
+    return PA_OK;
+}
+
+pa_status pa_append_kv_quant(const void *k, const void *v, const int64_t *slot_mapping, void *k_cache, void *v_cache,
+                             float *k_scale, float *v_scale, int num_tokens, int num_kv_heads, int head_dim,
+                             int block_size, int num_blocks, pa_dtype dtype, pa_dtype cache_dtype,
+                             uint32_t *err_word, pa_stream_t stream) {
+    g_detail.clear();
+    if (num_tokens < 0 || num_kv_heads <= 0 || num_blocks <= 0)
+        return fail(PA_ERR_INVALID_ARGUMENT, "num_tokens, num_kv_heads or num_blocks out of range");
+    if (!block_size_ok(block_size))
+        return fail(PA_ERR_UNSUPPORTED, "block_size must be 8, 16 or 32");
+    if (!head_dim_ok(head_dim))
+        return fail(PA_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
+    if (!dtype_ok(dtype) || !code_dtype_ok(cache_dtype))
+        return fail(PA_ERR_INVALID_ARGUMENT, "unknown dtype (rows: PA_F32/F16/BF16; cache: PA_I8/PA_E4M3)");
+    if (num_tokens == 0)
+        return PA_OK;
+    if (!k || !v || !slot_mapping || !k_cache || !v_cache || !k_scale || !v_scale)
+        return fail(PA_ERR_INVALID_ARGUMENT, "null pointer");
+    if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(k_scale) ||
+        !aligned16(v_scale))
+        return fail(PA_ERR_INVALID_ARGUMENT, "k, v, the code pools and the scale pools must be 16-byte aligned");
+    if ((reinterpret_cast<uintptr_t>(slot_mapping) & 7u) != 0)
+        return fail(PA_ERR_INVALID_ARGUMENT, "slot_mapping must be 8-byte aligned");
+    int dev = 0, sms = 0;
+    cudaError_t e = device_sms(&dev, &sms);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "device query");
+    e = launch_append_quant(k, v, slot_mapping, k_cache, v_cache, k_scale, v_scale, num_tokens, num_kv_heads,
+                            head_dim, dtype, cache_dtype, block_size, num_blocks, err_word, sms,
+                            reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+        return cuda_fail(e, "append launch");
+    return PA_OK;
+}
+
+pa_status pa_copy_blocks_quant(const int64_t *src_dst_pairs, int num_pairs, void *k_cache, void *v_cache,
+                               float *k_scale, float *v_scale, int num_kv_heads, int head_dim, int block_size,
+                               int num_blocks, uint32_t *err_word, pa_stream_t stream) {
+    g_detail.clear();
+    if (num_pairs < 0 || num_kv_heads <= 0 || num_blocks <= 0)
+        return fail(PA_ERR_INVALID_ARGUMENT, "num_pairs, num_kv_heads or num_blocks out of range");
+    if (!block_size_ok(block_size))
+        return fail(PA_ERR_UNSUPPORTED, "block_size must be 8, 16 or 32");
+    if (!head_dim_ok(head_dim))
+        return fail(PA_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
+    if (num_pairs == 0)
+        return PA_OK;
+    if (!src_dst_pairs || !k_cache || !v_cache || !k_scale || !v_scale)
+        return fail(PA_ERR_INVALID_ARGUMENT, "null pointer");
+    if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(k_scale) || !aligned16(v_scale))
+        return fail(PA_ERR_INVALID_ARGUMENT, "the code and scale pools must be 16-byte aligned");
+    if ((reinterpret_cast<uintptr_t>(src_dst_pairs) & 7u) != 0)
+        return fail(PA_ERR_INVALID_ARGUMENT, "src_dst_pairs must be 8-byte aligned");
+    int dev = 0, sms = 0;
+    cudaError_t e = device_sms(&dev, &sms);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "device query");
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    const long long code_bytes = static_cast<long long>(num_kv_heads) * block_size * head_dim;
+    const long long scale_bytes = static_cast<long long>(num_kv_heads) * block_size * 4;
+    e = launch_copy_blocks(src_dst_pairs, num_pairs, k_cache, v_cache, code_bytes, num_blocks, err_word, sms, cs);
+    if (e == cudaSuccess)
+        e = launch_copy_blocks(src_dst_pairs, num_pairs, k_scale, v_scale, scale_bytes, num_blocks, err_word, sms,
+                               cs);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "copy_blocks launch");
+    return PA_OK;
+}
+
+pa_status pa_swap_blocks_quant(const int64_t *src_dst_pairs, int num_pairs, const void *src_k, const void *src_v,
+                               const float *src_k_scale, const float *src_v_scale, void *dst_k, void *dst_v,
+                               float *dst_k_scale, float *dst_v_scale, int src_num_blocks, int dst_num_blocks,
+                               int num_kv_heads, int head_dim, int block_size, uint32_t *err_word,
+                               pa_stream_t stream) {
+    g_detail.clear();
+    if (num_pairs < 0 || num_kv_heads <= 0 || src_num_blocks <= 0 || dst_num_blocks <= 0)
+        return fail(PA_ERR_INVALID_ARGUMENT, "num_pairs, num_kv_heads or a pool size out of range");
+    if (!block_size_ok(block_size))
+        return fail(PA_ERR_UNSUPPORTED, "block_size must be 8, 16 or 32");
+    if (!head_dim_ok(head_dim))
+        return fail(PA_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
+    if (num_pairs == 0)
+        return PA_OK;
+    if (!src_dst_pairs || !src_k || !src_v || !dst_k || !dst_v || !src_k_scale || !src_v_scale || !dst_k_scale ||
+        !dst_v_scale)
+        return fail(PA_ERR_INVALID_ARGUMENT, "null pointer");
+    if (!aligned16(src_k) || !aligned16(src_v) || !aligned16(dst_k) || !aligned16(dst_v) ||
+        !aligned16(src_k_scale) || !aligned16(src_v_scale) || !aligned16(dst_k_scale) || !aligned16(dst_v_scale))
+        return fail(PA_ERR_INVALID_ARGUMENT, "the pools must be 16-byte aligned");
+    if ((reinterpret_cast<uintptr_t>(src_dst_pairs) & 7u) != 0)
+        return fail(PA_ERR_INVALID_ARGUMENT, "src_dst_pairs must be 8-byte aligned");
+    int dev = 0, sms = 0;
+    cudaError_t e = device_sms(&dev, &sms);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "device query");
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    const long long code_bytes = static_cast<long long>(num_kv_heads) * block_size * head_dim;
+    const long long scale_bytes = static_cast<long long>(num_kv_heads) * block_size * 4;
+    e = launch_swap_blocks(src_dst_pairs, num_pairs, src_k, src_v, dst_k, dst_v, code_bytes, src_num_blocks,
+                           dst_num_blocks, err_word, sms, cs);
+    if (e == cudaSuccess)
+        e = launch_swap_blocks(src_dst_pairs, num_pairs, src_k_scale, src_v_scale, dst_k_scale, dst_v_scale,
+                               scale_bytes, src_num_blocks, dst_num_blocks, err_word, sms, cs);
     if (e != cudaSuccess)
         return cuda_fail(e, "swap_blocks launch");
     return PA_OK;

@@ -131,18 +131,6 @@ __device__ inline float fast_exp2(float x) {
     return y;
 }
 
-__device__ inline uint2 ld_shared_v2(const void *p) {
-    uint2 r;
-    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(r.x), "=r"(r.y) : "r"(smem_addr(p)));
-    return r;
-}
-
-__device__ inline uint32_t ld_shared_u32(const void *p) {
-    uint32_t r;
-    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(r) : "r"(smem_addr(p)));
-    return r;
-}
-
 // acc += sum of the elementwise products of two 16-byte chunks (fp32 accumulate).
 template <typename T> struct ChunkDot;
 template <> struct ChunkDot<__half> {

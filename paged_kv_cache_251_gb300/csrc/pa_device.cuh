@@ -143,6 +143,18 @@ __device__ inline uint64_t policy_evict_first() {
     return p;
 }
 
+__device__ inline uint2 ld_shared_v2(const void *p) {
+    uint2 r;
+    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(r.x), "=r"(r.y) : "r"(smem_addr(p)));
+    return r;
+}
+
+__device__ inline uint32_t ld_shared_u32(const void *p) {
+    uint32_t r;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(r) : "r"(smem_addr(p)));
+    return r;
+}
+
 __device__ inline uint4 ld_shared_v4(const void *p) {
     uint4 r;
     asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"

@@ -28,9 +28,19 @@ const void *decode_mha_kernel_bf16(int head_dim, int block_size);
 const void *decode_gqa_kernel_f16(int block_size, int group);
 const void *decode_gqa_kernel_bf16(int block_size, int group);
 
+// General decode kernels for 8-bit caches (INT8 / E4M3 codes with row
+// scales), per head_dim and query group; nullptr if not built.
+const void *decode_q8_kernel_i8(int head_dim, int group);
+const void *decode_q8_kernel_e4m3(int head_dim, int group);
+
 cudaError_t launch_append(const void *k, const void *v, const int64_t *slots, void *k_cache, void *v_cache,
                           int num_tokens, int num_kv_heads, int row_bytes, int block_size, int num_blocks,
                           uint32_t *err, int num_sms, cudaStream_t stream);
+
+cudaError_t launch_append_quant(const void *k, const void *v, const int64_t *slots, void *k_codes, void *v_codes,
+                                float *k_scale, float *v_scale, int num_tokens, int num_kv_heads, int head_dim,
+                                int in_dtype, int cache_dtype, int block_size, int num_blocks, uint32_t *err,
+                                int num_sms, cudaStream_t stream);
 
 cudaError_t launch_copy_blocks(const int64_t *pairs, int num_pairs, void *k_cache, void *v_cache,
                                long long block_bytes, int num_blocks, uint32_t *err, int num_sms,
@@ -44,6 +54,10 @@ cudaError_t launch_swap_blocks(const int64_t *pairs, int num_pairs, const void *
 // its tensor maps and launch it on `cs` with the filled-in parameters (the
 // stage count is set there).  The partition reduce is the caller's.
 pa_status launch_decode_kernel(DecodeParams &p, int dtype, int head_dim, int G, cudaStream_t cs);
+
+// Same for an 8-bit cache of cache_dtype (PA_I8 / PA_E4M3); p.k_scale,
+// p.v_scale and p.q_dtype must be set.
+pa_status launch_decode_q8_kernel(DecodeParams &p, int cache_dtype, int head_dim, int G, cudaStream_t cs);
 
 // Text returned by pa_last_error_detail() on the calling thread.
 void set_last_error_detail(const char *why);

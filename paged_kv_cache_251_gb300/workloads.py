@@ -239,6 +239,56 @@ def gqa(device="cpu") -> DecodeInputs:
                          with_append=False)
 
 
+# 8-bit caches: random code and scale pools (raw draws, no quantisation)
+_S_KCODE, _S_VCODE, _S_KSCALE, _S_VSCALE = 9, 10, 11, 12
+CODE_DTYPES = {"int8": torch.int8, "e4m3": torch.float8_e4m3fn}
+
+
+def code_pool(seed: int, stream: int, shape, fmt: str, device="cpu") -> torch.Tensor:
+    """Random 8-bit cache codes of ``shape`` as int8 / float8_e4m3fn.
+
+    INT8: uniform in [-127, 127].  E4M3: random sign and mantissa bits, the
+    exponent field uniform in [2, 10], and one code in 16 with exponent field
+    0 (a subnormal or zero); never the NaN pattern.
+    """
+    n = 1
+    for d in shape:
+        n *= int(d)
+    out = torch.empty(n, dtype=torch.uint8, device=device)
+    for start in range(0, n, _CHUNK):
+        cnt = min(_CHUNK, n - start)
+        z = bits64(seed, stream, cnt, device=device, offset=start)
+        if fmt == "int8":
+            c = (_srl(z, 33) % 255) - 127
+            out[start:start + cnt] = (c & 0xFF).to(torch.uint8)
+        else:
+            e = 2 + _srl(z, 40) % 9
+            e = torch.where((_srl(z, 36) & 15) == 0, torch.zeros_like(e), e)
+            byte = ((_srl(z, 63) & 1) << 7) | (e << 3) | (_srl(z, 20) & 7)
+            out[start:start + cnt] = byte.to(torch.uint8)
+    return out.view(CODE_DTYPES[fmt]).reshape(tuple(shape))
+
+
+def scale_pool(seed: int, stream: int, shape, fmt: str, device="cpu") -> torch.Tensor:
+    """Random row scales (float32 of ``shape``): uniform in [0.5, 1.5) times
+    1/64 for INT8 codes or 1/5 for E4M3 codes, so code * scale is of order one."""
+    n = 1
+    for d in shape:
+        n *= int(d)
+    u = _srl(bits64(seed, stream, n, device=device), 40).to(torch.float32) * (2.0 ** -24)
+    base = 1.0 / 64 if fmt == "int8" else 0.2
+    return ((0.5 + u) * base).reshape(tuple(shape))
+
+
+def quant_pools(inp: DecodeInputs, fmt: str, device="cpu"):
+    """Random code and scale pools with the block layout of ``inp``'s caches:
+    (k_codes, v_codes, k_scale, v_scale)."""
+    s = inp.shape
+    shp = (inp.num_blocks, s.num_kv_heads, s.block_size, s.head_dim)
+    return (code_pool(s.seed, _S_KCODE, shp, fmt, device), code_pool(s.seed, _S_VCODE, shp, fmt, device),
+            scale_pool(s.seed, _S_KSCALE, shp[:3], fmt, device), scale_pool(s.seed, _S_VSCALE, shp[:3], fmt, device))
+
+
 def window_ring_blocks(shape: Shape, ring_len: int) -> torch.Tensor:
     """Physical block ids for each sequence's ring: int64 [N, ring_len], a
     seeded shuffle of the pool."""
