@@ -59,6 +59,9 @@ def parse_args(argv=None):
                     help="prefix workloads: decode with pa_decode_shared_prefix (shared blocks read once per group)")
     ap.add_argument("--table", choices=["shuffled", "identity"], default="shuffled",
                     help="block hand-out order (identity: each sequence's blocks adjacent in memory)")
+    ap.add_argument("--kv-format", choices=["native", "int8", "e4m3"], default="native",
+                    help="opt13b / gqa / tiny_scaled: 8-bit cache (codes + one fp32 scale per row), decoded by "
+                         "pa_decode_quant and appended by pa_append_kv_quant")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU baseline budget")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args(argv)
@@ -229,8 +232,11 @@ class DecodeAppendStep(Step):
     """pa_decode over every sequence's L tokens, then pa_append_kv of token L
     (the slot the host block manager assigns); idempotent step."""
 
-    def __init__(self, name, device, partition, shuffle=True):
+    kv_format = None
+
+    def __init__(self, name, device, partition, shuffle=True, kv_format="native"):
         super().__init__(device, partition)
+        self.kv_format = None if kv_format == "native" else kv_format
         from paged_kv_cache_251_gb300 import pa
         from paged_kv_cache_251_gb300 import workloads as wl
         from paged_kv_cache_251_gb300.blocks import BlockManager
@@ -281,23 +287,50 @@ class DecodeAppendStep(Step):
         self.ws = pa.workspace_for(inp.q, s.block_size, self.bt.shape[1], 0, partition)
         elt = _elt(s.dtype)
         from paged_kv_cache_251_gb300 import accounting as acc
-        self.dec_bytes = acc.decode_bytes(inp.context_lens, s.num_heads, s.num_kv_heads, s.head_dim,
-                                          s.block_size, elt, out_elt_bytes=4)
+        if self.kv_format:
+            # 8-bit pools: random codes and row scales from the seeded generator
+            # (the 16-bit pools are dropped); the new tokens are quantised on append
+            self.k_cache = self.v_cache = inp.k_cache = inp.v_cache = None
+            self.kq, self.vq, self.ks, self.vs = wl.quant_pools(inp, self.kv_format, device=device)
+            self.description += (f"; 8-bit cache: {self.kv_format.upper()} codes + one fp32 scale per "
+                                 f"(token, kv head) row, step = pa_decode_quant + pa_append_kv_quant")
+            self.dec_bytes = acc.decode_bytes(inp.context_lens, s.num_heads, s.num_kv_heads, s.head_dim,
+                                              s.block_size, 1, out_elt_bytes=4, q_elt_bytes=elt, row_scale_bytes=4)
+        else:
+            self.dec_bytes = acc.decode_bytes(inp.context_lens, s.num_heads, s.num_kv_heads, s.head_dim,
+                                              s.block_size, elt, out_elt_bytes=4)
         self.kv_bytes = self.dec_bytes["kv"]
         self.roof_bytes = self.dec_bytes["total"]
         self.launches = (2 if self.ws is not None else 1) + 1
 
     def decode(self, stream, q=None, bt=None, cl=None):
         s = self.shape
+        if self.kv_format:
+            self.pa.pa_decode_quant(self.out, self.q if q is None else q, self.kq, self.vq, self.ks, self.vs,
+                                    self.bt if bt is None else bt, self.cl if cl is None else cl,
+                                    num_kv_heads=s.num_kv_heads, window=self.window, partition_size=self.partition,
+                                    workspace=self.ws, err_word=self.err, stream=stream)
+            return
         self.pa.pa_decode(self.out, self.q if q is None else q, self.k_cache, self.v_cache,
                           self.bt if bt is None else bt, self.cl if cl is None else cl, num_kv_heads=s.num_kv_heads,
                           window=self.window, partition_size=self.partition, workspace=self.ws, err_word=self.err,
                           stream=stream)
 
     def post(self, stream, k_new=None, v_new=None, slots=None):
-        self.pa.pa_append_kv(self.k_new if k_new is None else k_new, self.v_new if v_new is None else v_new,
-                             self.slots if slots is None else slots, self.k_cache, self.v_cache, err_word=self.err,
-                             stream=stream)
+        kn = self.k_new if k_new is None else k_new
+        vn = self.v_new if v_new is None else v_new
+        sl = self.slots if slots is None else slots
+        if self.kv_format:
+            self.pa.pa_append_kv_quant(kn, vn, sl, self.kq, self.vq, self.ks, self.vs, err_word=self.err,
+                                       stream=stream)
+            return
+        self.pa.pa_append_kv(kn, vn, sl, self.k_cache, self.v_cache, err_word=self.err, stream=stream)
+
+    def cache_args(self):
+        """(k, v, extra oracle kwargs) of the cache for the oracle."""
+        if self.kv_format:
+            return self.kq, self.vq, {"k_scale": self.ks, "v_scale": self.vs}
+        return self.k_cache, self.v_cache, {}
 
     def e2e(self, stream, dev):
         """The step through the public API from host buffers (dev: device
@@ -312,11 +345,20 @@ class DecodeAppendStep(Step):
         """The same step on the CPU oracle (host copies made on first use);
         rows limits the decode to the first `rows` sequences."""
         import oracle
+        s = self.shape
+        n = s.num_seqs if rows is None else rows
+        if self.kv_format:
+            if not hasattr(self, "_h"):
+                self._h = [t.cpu() for t in (self.q, self.kq, self.vq, self.ks, self.vs, self.k_new, self.v_new)]
+            q, kq, vq, ks, vs, kn, vn = self._h
+            oracle.paged_attention(q[:n], kq, vq, self.inp.block_tables[:n], self.inp.context_lens[:n],
+                                   num_kv_heads=s.num_kv_heads, scale=1.0 / math.sqrt(s.head_dim), threads=threads,
+                                   k_scale=ks, v_scale=vs)
+            oracle.append_kv_quant(kq, vq, ks, vs, kn, vn, self.host["slots"])
+            return int(self.inp.context_lens[:n].to(torch.int64).sum()) * 2 * s.num_kv_heads * (s.head_dim + 4)
         if not hasattr(self, "_h"):
             self._h = [t.cpu() for t in (self.q, self.k_cache, self.v_cache, self.k_new, self.v_new)]
         q, k, v, kn, vn = self._h
-        s = self.shape
-        n = s.num_seqs if rows is None else rows
         oracle.paged_attention(q[:n], k, v, self.inp.block_tables[:n], self.inp.context_lens[:n],
                                num_kv_heads=s.num_kv_heads, scale=1.0 / math.sqrt(s.head_dim), threads=threads)
         oracle.append_kv(k, v, kn, vn, self.host["slots"])
@@ -461,9 +503,11 @@ class PrefixStep(DecodeAppendStep):
 WORKLOADS = ["opt13b", "gqa", "window", "prefix_bs8", "prefix_bs16", "prefix_bs32", "tiny", "tiny_scaled"]
 
 
-def make_step(name, device, partition, table="shuffled", shared=False):
+def make_step(name, device, partition, table="shuffled", shared=False, kv_format="native"):
     if name in ("opt13b", "gqa", "tiny", "tiny_scaled"):
-        return DecodeAppendStep(name, device, partition, shuffle=(table == "shuffled"))
+        return DecodeAppendStep(name, device, partition, shuffle=(table == "shuffled"), kv_format=kv_format)
+    if kv_format != "native":
+        raise SystemExit("--kv-format applies to the opt13b, gqa, tiny and tiny_scaled workloads")
     if name == "window":
         return WindowStep(device, partition)
     if name.startswith("prefix_bs"):
@@ -507,8 +551,9 @@ def run_native(args):
         raise SystemExit("bench.py needs a CUDA GPU for the native arm")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    st = make_step(args.workload, dev, args.partition, args.table, args.shared_prefix)
+    st = make_step(args.workload, dev, args.partition, args.table, args.shared_prefix, args.kv_format)
     s = st.shape
+    tag = args.workload + ("" if args.kv_format == "native" else "_" + args.kv_format)
     stream = torch.cuda.current_stream(dev)
 
     for _ in range(max(args.warmup, 0)):
@@ -565,10 +610,12 @@ def run_native(args):
         from paged_kv_cache_251_gb300 import workloads as wl
         idx = wl.permutation(4242, 1, s.num_seqs * s.num_heads)[:16]
         pairs = torch.stack([idx // s.num_heads, idx % s.num_heads], 1).to(torch.int32)
-        ref = oracle.paged_attention(st.q.cpu(), st.k_cache.cpu(), st.v_cache.cpu(), st.inp.block_tables,
+        kc, vc, extra = st.cache_args()
+        extra = {k: v.cpu() for k, v in extra.items()}
+        ref = oracle.paged_attention(st.q.cpu(), kc.cpu(), vc.cpu(), st.inp.block_tables,
                                      st.inp.context_lens, num_kv_heads=s.num_kv_heads,
                                      scale=1.0 / math.sqrt(s.head_dim), window=st.window, pairs=pairs,
-                                     threads=os.cpu_count() or 1)
+                                     threads=os.cpu_count() or 1, **extra)
         got = st.out.cpu()[pairs[:, 0].long(), pairs[:, 1].long()].double().numpy()
         parity = float(abs(got - ref).max())
 
@@ -611,7 +658,7 @@ def run_native(args):
     peak, peak_kind = hbm_peak()
     achieved = st.roof_bytes / (ms_dec * 1e-3) / 1e9
     khash = kernel_source_hash()
-    traffic, traffic_src = traffic_from_profile(args.workload, khash)
+    traffic, traffic_src = traffic_from_profile(tag, khash)
     value = world * st.kv_bytes / (ms_step_max * 1e-3) / 1e9
     line = {
         "metric": METRIC,
@@ -624,7 +671,8 @@ def run_native(args):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": {torch.float16: "f16", torch.bfloat16: "bf16", torch.float32: "f32"}[s.dtype],
+        "dtype": ({"int8": "i8", "e4m3": "e4m3"}[args.kv_format] if args.kv_format != "native" else
+                  {torch.float16: "f16", torch.bfloat16: "bf16", torch.float32: "f32"}[s.dtype]),
         "data": "synthetic (seeded SplitMix64 / Box-Muller N(0,1) q, K, V; seeded shuffle of the block pool)",
         "config": {
             "workload": st.description,
@@ -632,7 +680,7 @@ def run_native(args):
             "head_dim": s.head_dim, "block_size": s.block_size, "window": st.window,
             "context_tokens": st.dec_bytes["attended_tokens"],
             "partition_size": st.partition or 512, "accumulate": "f32", "out_dtype": "f32",
-            "block_order": args.table,
+            "block_order": args.table, "kv_format": args.kv_format,
             "l2": (f"no flush: the K/V read per step ({st.kv_bytes / 1e9:.2f} GB) is larger than L2 (129 MB)"
                    if flush is None else
                    f"L2 flushed before every timed step (a 256 MB buffer is overwritten); the K/V read per step "
@@ -715,7 +763,7 @@ def run_reference(args):
     world, rank, _ = dist_env()
     if rank != 0:
         return  # the reference arm runs on rank 0 only
-    st = make_step(args.workload, "cpu", args.partition, args.table)
+    st = make_step(args.workload, "cpu", args.partition, args.table, kv_format=args.kv_format)
     s = st.shape
     threads = os.cpu_count() or 1
     # size the per-step sample so the whole run stays within a few minutes

@@ -97,6 +97,7 @@ typedef enum {
 #define PA_DEVERR_BAD_PAIR 0x4u  /* copy: src or dst outside [0, num_blocks); the pair was skipped */
 #define PA_DEVERR_TIMEOUT 0x8u   /* a pipeline wait gave up (about 2 s); the output is not valid */
 #define PA_DEVERR_BAD_LEN 0x10u  /* decode: context_lens[s] > max_blocks_per_seq * block_size; clamped to that */
+#define PA_DEVERR_BAD_LAUNCH 0x20u /* a kernel refused its launch configuration; the output is not valid */
 
 /*
  * Bytes of scratch pa_decode needs for split-context partials (0 when no

@@ -18,6 +18,7 @@
 #include "pa_decode_gqa.cuh"
 #include "pa_decode_mha.cuh"
 #include "pa_decode_q8.cuh"
+#include "pa_decode_q8f.cuh"
 #include "pa_internal.h"
 
 namespace pa {
@@ -188,7 +189,28 @@ pa_status q_tensor_map(CUtensorMap *map, const void *base, int dtype, int head_d
     return PA_OK;
 }
 
+// 3-D view of an 8-bit code pool with head_dim 128 as [tile][row][128 bytes];
+// one box is a whole (block, head) tile (128-byte swizzle).
+pa_status code_tensor_map(CUtensorMap *map, const void *base, int block_size, long long tiles) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
+    cudaError_t e = tensor_map_encoder(&enc);
+    if (e != cudaSuccess || !enc)
+        return cuda_fail(e == cudaSuccess ? cudaErrorSymbolNotFound : e, "cuTensorMapEncodeTiled lookup");
+    cuuint64_t dims[3] = {128, static_cast<cuuint64_t>(block_size), static_cast<cuuint64_t>(tiles)};
+    cuuint64_t strides[2] = {128, 128ull * block_size};
+    cuuint32_t box[3] = {128, static_cast<cuuint32_t>(block_size), 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(PA_ERR_INVALID_ARGUMENT, "cuTensorMapEncodeTiled rejected the code pool layout (code " +
+                                                 std::to_string(static_cast<int>(r)) + ")");
+    return PA_OK;
+}
+
 constexpr int kDefaultPartition = 512;
+constexpr int kQ8fStageBudget = 48 * 1024;
 constexpr int kMhaStageBudget = 64 * 1024;
 constexpr int kGqaStages = 3;
 constexpr int kStageBudget = 48 * 1024;
@@ -260,8 +282,11 @@ pa_status launch_decode_kernel(DecodeParams &p, int dtype, int head_dim, int G, 
         fn = dtype == PA_F32   ? decode_mha_kernel_f32(head_dim, block_size)
              : dtype == PA_F16 ? decode_mha_kernel_f16(head_dim, block_size)
                                : decode_mha_kernel_bf16(head_dim, block_size);
+        // stages are owned round-robin by the consumer warps: a multiple of
+        // their count keeps each stage with one warp (no phase aliasing)
         int S = kMhaStageBudget / (2 * tile);
-        S = S < 4 ? 4 : (S > 16 ? 16 : S);
+        S -= S % kMhaWarps;
+        S = S < kMhaWarps ? kMhaWarps : (S > 16 ? 16 : S);
         p.stages = S;
         smem = mha_smem_layout(S, tile, row, head_dim).total;
         threads = kMhaThreads;
@@ -310,6 +335,51 @@ pa_status launch_decode_kernel(DecodeParams &p, int dtype, int head_dim, int G, 
 }
 
 pa_status launch_decode_q8_kernel(DecodeParams &p, int cache_dtype, int head_dim, int G, cudaStream_t cs) {
+    const long long tiles = static_cast<long long>(p.num_blocks) * p.num_kv_heads;
+    // head_dim 128, up to 4 query heads per kv head: the TMA-fed kernel (E4M3
+    // multiplies fp16 queries, so fp32 queries stay on the general kernel)
+    const bool fast = head_dim == 128 && G <= 4 && tiles <= INT_MAX &&
+                      !(cache_dtype == PA_E4M3 && p.q_dtype == PA_F32);
+    if (fast) {
+        const void *ffn = cache_dtype == PA_I8 ? decode_q8f_kernel_i8(G, p.block_size)
+                                               : decode_q8f_kernel_e4m3(G, p.block_size);
+        if (!ffn)
+            return fail(PA_ERR_UNSUPPORTED, "no 8-bit-cache decode kernel for this group / block size");
+        // stages are owned round-robin by the consumer warps: a multiple of
+        // their count keeps each stage with one warp (no phase aliasing)
+        const int stage = 2 * p.block_size * (kQ8fD + 4);
+        int S = kQ8fStageBudget / stage;
+        S -= S % kQ8fWarps;
+        S = S < kQ8fWarps ? kQ8fWarps : (S > 16 ? 16 : S);
+        p.stages = S;
+        const size_t smem = q8f_smem_layout(S, p.block_size, G).total;
+        CUtensorMap tmk, tmv;
+        pa_status ts = code_tensor_map(&tmk, p.k_cache, p.block_size, tiles);
+        if (ts == PA_OK)
+            ts = code_tensor_map(&tmv, p.v_cache, p.block_size, tiles);
+        if (ts != PA_OK)
+            return ts;
+        int dev = 0, sms = 0, per_sm = 0;
+        cudaError_t e = device_sms(&dev, &sms);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "device query");
+        e = prepare_kernel(dev, ffn, smem, kQ8fThreads, &per_sm);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "decode kernel set-up");
+        if (per_sm < 1)
+            return fail(PA_ERR_UNSUPPORTED, "decode kernel does not fit on an SM");
+        const long long items_max = static_cast<long long>(p.num_seqs) * p.num_kv_heads * p.max_parts;
+        long long grid = static_cast<long long>(sms) * per_sm;
+        if (grid > items_max)
+            grid = items_max;
+        if (grid < 1)
+            grid = 1;
+        void *args[] = {&p, &tmk, &tmv};
+        e = cudaLaunchKernel(ffn, dim3(static_cast<unsigned>(grid)), dim3(kQ8fThreads), args, smem, cs);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "decode launch");
+        return PA_OK;
+    }
     const void *fn = cache_dtype == PA_I8 ? decode_q8_kernel_i8(head_dim, G) : decode_q8_kernel_e4m3(head_dim, G);
     if (!fn)
         return fail(PA_ERR_UNSUPPORTED, "no 8-bit-cache decode kernel for this head_dim / group");

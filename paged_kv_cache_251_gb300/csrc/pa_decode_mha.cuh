@@ -570,6 +570,15 @@ __global__ void __launch_bounds__(kMhaThreads) pa_decode_mha_kernel(const Decode
     char *smem = reinterpret_cast<char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     using C = MhaCfg<T, D, BS>;
     const MhaLayout L = mha_smem_layout(p.stages, C::kTile, C::kRow, D);
+    // Stage t belongs to consumer warp t % 4.  With a stage count that is not a
+    // multiple of 4, one stage would pass between warps, and a warp running a
+    // full ring ahead could see its parity wait satisfied by an older phase of
+    // that stage.  The host never launches such a count; refuse it here too.
+    if (p.stages < kMhaWarps || p.stages % kMhaWarps != 0) {
+        if (threadIdx.x == 0 && p.err)
+            atomicOr(p.err, PA_DEVERR_BAD_LAUNCH);
+        return;
+    }
     if (threadIdx.x == 0) {
         uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.full);
         uint64_t *empty = reinterpret_cast<uint64_t *>(smem + L.empty);

@@ -264,9 +264,11 @@ __device__ inline void q8_consumer(const DecodeParams &p, char *smem, const Smem
         if (mt.flags & kFirst) {
             cur = items[mt.slot];
             if (mt.flags & kHasQ) {
+                // the item's G query rows arrived back to back at their own row size
+                const int qrow = D * (p.q_dtype == PA_F32 ? 4 : 2);
 #pragma unroll
                 for (int g = 0; g < G; ++g) {
-                    const char *qr = qbuf + (mt.slot * G + g) * C::kQRowMax;
+                    const char *qr = qbuf + mt.slot * G * C::kQRowMax + g * qrow;
 #pragma unroll
                     for (int e = 0; e < E; ++e)
                         qf[g][e] = load_elt(qr, p.q_dtype, li * E + e) * p.scale_log2;

@@ -33,6 +33,11 @@ const void *decode_gqa_kernel_bf16(int block_size, int group);
 const void *decode_q8_kernel_i8(int head_dim, int group);
 const void *decode_q8_kernel_e4m3(int head_dim, int group);
 
+// Fast decode kernels for 8-bit caches fed by TMA tensor copies: head_dim
+// 128, per query group (1, 2, 4) and block size; nullptr if not built.
+const void *decode_q8f_kernel_i8(int group, int block_size);
+const void *decode_q8f_kernel_e4m3(int group, int block_size);
+
 cudaError_t launch_append(const void *k, const void *v, const int64_t *slots, void *k_cache, void *v_cache,
                           int num_tokens, int num_kv_heads, int row_bytes, int block_size, int num_blocks,
                           uint32_t *err, int num_sms, cudaStream_t stream);

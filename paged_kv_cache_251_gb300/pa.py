@@ -17,7 +17,7 @@ LIB_PATH = Path(__file__).resolve().parent / "_lib" / "libpa.so"
 
 PA_OK, PA_ERR_INVALID_ARGUMENT, PA_ERR_UNSUPPORTED, PA_ERR_WORKSPACE_TOO_SMALL, PA_ERR_CUDA = range(5)
 PA_F32, PA_F16, PA_BF16, PA_I8, PA_E4M3 = 0, 1, 2, 3, 4
-DEVERR_BAD_BLOCK, DEVERR_BAD_SLOT, DEVERR_BAD_PAIR, DEVERR_TIMEOUT, DEVERR_BAD_LEN = 1, 2, 4, 8, 16
+DEVERR_BAD_BLOCK, DEVERR_BAD_SLOT, DEVERR_BAD_PAIR, DEVERR_TIMEOUT, DEVERR_BAD_LEN, DEVERR_BAD_LAUNCH = 1, 2, 4, 8, 16, 32
 
 DTYPE_CODE = {torch.float32: PA_F32, torch.float16: PA_F16, torch.bfloat16: PA_BF16}
 # 8-bit caches: code pools are int8 or float8_e4m3fn tensors, scales float32

@@ -151,6 +151,13 @@ QCASES = [
     ("g8_bs8_window", 3, 16, 2, 128, 8, [3000, 77, 1300], 700, 0),
     ("g4_d64", 4, 8, 2, 64, 16, [65, 66, 700, 2], 0, 0),
     ("empty", 3, 8, 2, 128, 16, [0, 300, 0], 0, 0),
+    # every (group, block size) corner of the TMA-fed kernel (head_dim 128, G <= 4)
+    ("g1_bs8", 4, 6, 6, 128, 8, [9, 700, 1, 255], 0, 0),
+    ("g2_bs16_window", 3, 8, 4, 128, 16, [1000, 5, 333], 200, 0),
+    ("g2_bs8_parts", 3, 4, 2, 128, 8, [1500, 8, 9], 0, 64),
+    ("g4_bs8", 3, 8, 2, 128, 8, [129, 1, 1000], 0, 0),
+    ("g4_bs32_window", 3, 16, 4, 128, 32, [33, 2049, 64], 100, 0),
+    ("g1_bs32_empty", 3, 2, 2, 128, 32, [0, 65, 0], 0, 0),
 ]
 
 
