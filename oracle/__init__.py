@@ -60,11 +60,13 @@ def _bind(lib):
     lib.orc_e4m3_encode.restype = ctypes.c_uint8
     lib.orc_quantize_rows.argtypes = [P, I, I64, I, I, P, P]
     lib.orc_quantize_rows.restype = I
-    lib.orc_paged_attention_cache.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, D, I, I, I, I, I, I,
+    lib.orc_paged_attention_cache.argtypes = [P, P, P, P, P, P, I, I, I, I, I, D, I, I, I, I, I, I,
                                               P, I64, I, P]
     lib.orc_paged_attention_cache.restype = I
-    lib.orc_append_kv_quant.argtypes = [P, P, P, P, P, P, P, I64, I, I, I, I, I, I]
+    lib.orc_append_kv_quant.argtypes = [P, P, P, P, P, I64, I, I, I, I, I, I]
     lib.orc_append_kv_quant.restype = I64
+    lib.orc_scale_rows.argtypes = [I, I]
+    lib.orc_scale_rows.restype = I
     return lib
 
 
@@ -131,6 +133,42 @@ def quantize_rows(x: torch.Tensor, fmt, lib=None):
     return codes.view(code_dtype), scales
 
 
+def scale_rows(block_size: int, head_dim: int) -> int:
+    """Rows of a page that hold its fp32 row scales: ceil(4 * block_size / head_dim)."""
+    return (4 * block_size + head_dim - 1) // head_dim
+
+
+def page_block_size(rows: int, head_dim: int) -> int:
+    """block_size of a page with `rows` rows (codes + scale rows)."""
+    for bs in (8, 16, 32):
+        if bs + scale_rows(bs, head_dim) == rows:
+            return bs
+    raise ValueError(f"no block size gives a {rows}-row page at head_dim {head_dim}")
+
+
+def pack_pages(codes: torch.Tensor, scales: torch.Tensor) -> torch.Tensor:
+    """8-bit pages [nb, H_kv, bs + scale_rows, d] from codes [nb, H_kv, bs, d]
+    (int8 / float8_e4m3fn) and scales float32 [nb, H_kv, bs]: the code rows,
+    then the scales' bytes, then zeros."""
+    nb, hkv, bs, d = codes.shape
+    sr = scale_rows(bs, d)
+    pages = torch.zeros((nb, hkv, bs + sr, d), dtype=torch.uint8)
+    pages[:, :, :bs] = codes.view(torch.uint8)
+    sb = scales.contiguous().view(torch.uint8).reshape(nb, hkv, 4 * bs)
+    pages[:, :, bs:].reshape(nb, hkv, sr * d)[:, :, :4 * bs] = sb
+    return pages.view(codes.dtype)
+
+
+def unpack_pages(pages: torch.Tensor):
+    """(codes [nb, H_kv, bs, d], scales float32 [nb, H_kv, bs]) of 8-bit pages."""
+    nb, hkv, rows, d = pages.shape
+    bs = page_block_size(rows, d)
+    u8 = pages.view(torch.uint8)
+    codes = u8[:, :, :bs].contiguous().view(pages.dtype)
+    scales = u8[:, :, bs:].reshape(nb, hkv, -1)[:, :, :4 * bs].contiguous().view(torch.float32)
+    return codes, scales
+
+
 def dequantize(codes: torch.Tensor, scales: torch.Tensor, lib=None) -> np.ndarray:
     """fp64 values code * scale, codes decoded by the oracle's own tables."""
     lib = lib or load()
@@ -143,26 +181,22 @@ def dequantize(codes: torch.Tensor, scales: torch.Tensor, lib=None) -> np.ndarra
 
 def paged_attention(q, k_cache, v_cache, block_tables, context_lens, *, num_kv_heads: int,
                     scale: float, window: int = 0, pairs=None, invalid_policy: int = 0,
-                    threads: int = 1, lib=None, return_skipped: bool = False,
-                    k_scale=None, v_scale=None):
+                    threads: int = 1, lib=None, return_skipped: bool = False):
     """fp64 decode attention read through the block tables.
 
     q [N, H, d]; caches [num_blocks, H_kv, bs, d]; block_tables int32 [N, M];
     context_lens int32 [N].  ``pairs`` (int32 [P, 2] of (seq, head)) limits
     the work to those rows and returns [P, d]; otherwise [N, H, d].
-    8-bit caches (int8 / float8_e4m3fn code pools) take their row scales in
-    ``k_scale`` / ``v_scale`` (float32 [num_blocks, H_kv, bs]); every cached
-    value is then code * scale.
+    8-bit caches are int8 / float8_e4m3fn pages [num_blocks, H_kv, bs +
+    scale_rows, d] (see pack_pages); every cached value is code * scale.
     """
     lib = lib or load()
     q, k_cache, v_cache = _cpu(q), _cpu(k_cache), _cpu(v_cache)
     if k_cache.dtype in _CODE_FMT:
-        if v_cache.dtype != k_cache.dtype or k_scale is None or v_scale is None:
-            raise TypeError("8-bit caches need one code dtype and both scale pools")
-        return _paged_attention_cache(q, k_cache, v_cache, _cpu(k_scale).float().contiguous(),
-                                      _cpu(v_scale).float().contiguous(), block_tables, context_lens,
-                                      num_kv_heads, scale, window, pairs, invalid_policy, threads, lib,
-                                      return_skipped)
+        if v_cache.dtype != k_cache.dtype:
+            raise TypeError("both 8-bit pools must share one code dtype")
+        return _paged_attention_cache(q, k_cache, v_cache, block_tables, context_lens, num_kv_heads, scale,
+                                      window, pairs, invalid_policy, threads, lib, return_skipped)
     if not (q.dtype == k_cache.dtype == v_cache.dtype):
         raise TypeError("q, k_cache and v_cache must share one dtype")
     bt = _cpu(block_tables).to(torch.int32).contiguous()
@@ -188,14 +222,14 @@ def paged_attention(q, k_cache, v_cache, block_tables, context_lens, *, num_kv_h
     return (out, skipped.value) if return_skipped else out
 
 
-def _paged_attention_cache(q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens, num_kv_heads,
+def _paged_attention_cache(q, k_cache, v_cache, block_tables, context_lens, num_kv_heads,
                            scale, window, pairs, invalid_policy, threads, lib, return_skipped):
     bt = _cpu(block_tables).to(torch.int32).contiguous()
     cl = _cpu(context_lens).to(torch.int32).contiguous()
     N, H, d = q.shape
-    nb, hkv, bs, d2 = k_cache.shape
+    nb, hkv, rows, d2 = k_cache.shape
+    bs = page_block_size(rows, d)
     assert d2 == d and hkv == num_kv_heads and tuple(v_cache.shape) == tuple(k_cache.shape)
-    assert tuple(k_scale.shape) == (nb, hkv, bs) and tuple(v_scale.shape) == (nb, hkv, bs)
     M = bt.shape[1]
     if pairs is not None:
         pr = torch.as_tensor(pairs, dtype=torch.int32).reshape(-1, 2).contiguous()
@@ -206,7 +240,7 @@ def _paged_attention_cache(q, k_cache, v_cache, k_scale, v_scale, block_tables, 
         pptr, npairs = None, 0
     skipped = ctypes.c_int64(0)
     rc = lib.orc_paged_attention_cache(out.ctypes.data, q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
-                                       k_scale.data_ptr(), v_scale.data_ptr(), bt.data_ptr(), cl.data_ptr(),
+                                       bt.data_ptr(), cl.data_ptr(),
                                        N, H, num_kv_heads, d, bs, float(scale), int(window),
                                        _DTYPE_CODE[q.dtype], _CODE_FMT[k_cache.dtype], M, nb, invalid_policy,
                                        pptr, npairs, threads, ctypes.byref(skipped))
@@ -215,20 +249,20 @@ def _paged_attention_cache(q, k_cache, v_cache, k_scale, v_scale, block_tables, 
     return (out, skipped.value) if return_skipped else out
 
 
-def append_kv_quant(k_codes: torch.Tensor, v_codes: torch.Tensor, k_scales: torch.Tensor,
-                    v_scales: torch.Tensor, k, v, slot_mapping, lib=None) -> int:
-    """Quantise each token's K/V rows and store codes and scales at its slot,
-    in place on CPU tensors (codes int8 / float8_e4m3fn [nb, H_kv, bs, d],
-    scales float32 [nb, H_kv, bs]).  Returns the out-of-range slots skipped."""
+def append_kv_quant(k_pages: torch.Tensor, v_pages: torch.Tensor, k, v, slot_mapping, lib=None) -> int:
+    """Quantise each token's K/V rows and store codes and scale in the slot's
+    page, in place on CPU 8-bit pages (int8 / float8_e4m3fn [nb, H_kv, bs +
+    scale_rows, d]).  Returns the out-of-range slots skipped."""
     lib = lib or load()
-    for t in (k_codes, v_codes, k_scales, v_scales):
+    for t in (k_pages, v_pages):
         assert t.device.type == "cpu" and t.is_contiguous()
     k, v = _cpu(k), _cpu(v)
     sm = _cpu(torch.as_tensor(slot_mapping)).to(torch.int64).contiguous()
-    nb, hkv, bs, d = k_codes.shape
-    rc = lib.orc_append_kv_quant(k_codes.data_ptr(), v_codes.data_ptr(), k_scales.data_ptr(),
-                                 v_scales.data_ptr(), k.data_ptr(), v.data_ptr(), sm.data_ptr(), sm.numel(),
-                                 hkv, d, bs, nb, _DTYPE_CODE[k.dtype], _CODE_FMT[k_codes.dtype])
+    nb, hkv, rows, d = k_pages.shape
+    bs = page_block_size(rows, d)
+    rc = lib.orc_append_kv_quant(k_pages.data_ptr(), v_pages.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                 sm.data_ptr(), sm.numel(), hkv, d, bs, nb, _DTYPE_CODE[k.dtype],
+                                 _CODE_FMT[k_pages.dtype])
     if rc < 0:
         raise ValueError(f"oracle append_kv_quant refused the input (code {rc})")
     return int(rc)

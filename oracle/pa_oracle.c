@@ -27,6 +27,12 @@
  *    article's section 4.1 mixed-precision pages (INT8 for rarely used pages):
  *    8-bit caches, read here as symmetric per-row quantisation (one fp32
  *    scale per cached (token, kv head) row, the codes decided in fp32).
+ *
+ * 8-bit cache pages.  A (block, kv head) page of an 8-bit pool holds the
+ * block's block_size code rows of head_dim bytes, followed by
+ * scale_rows = ceil(4 * block_size / head_dim) rows whose first
+ * 4 * block_size bytes are the rows' fp32 scales (the rest zero):
+ *   pool [num_blocks][num_kv_heads][block_size + scale_rows][head_dim] bytes.
  */
 #include <math.h>
 #include <pthread.h>
@@ -198,14 +204,25 @@ int orc_quantize_rows(const void *x, int in_dtype, int64_t num_rows, int d, int 
     return 0;
 }
 
-/* Value of cache element `elem` (index into [num_blocks][H_kv][bs][d]): the
- * element itself for fp32/fp16/bf16 caches, code * scale of its row for
- * 8-bit caches (scales laid out [num_blocks][H_kv][bs]). */
-static double orc_cache_value(const void *cache, const float *scales, int cache_dtype, int64_t elem, int d)
+int orc_scale_rows(int block_size, int head_dim)
+{
+    return (4 * block_size + head_dim - 1) / head_dim;
+}
+
+/* Value of cache element `elem` (index into [num_blocks][H_kv][bs][d], the
+ * logical element order): the element itself for fp32/fp16/bf16 caches; for
+ * 8-bit pages, code * scale of its row, both read from the row's page. */
+static double orc_cache_value(const void *cache, int cache_dtype, int64_t elem, int d, int bs)
 {
     if (cache_dtype == ORC_I8 || cache_dtype == ORC_E4M3) {
-        const uint8_t c = ((const uint8_t *)cache)[elem];
-        return orc_code_to_double(c, cache_dtype) * (double)scales[elem / d];
+        const int64_t row = elem / d;                 /* (page, r) */
+        const int64_t page = row / bs;
+        const int64_t r = row % bs;
+        const int64_t page_bytes = (int64_t)(bs + orc_scale_rows(bs, d)) * d;
+        const uint8_t *pg = (const uint8_t *)cache + page * page_bytes;
+        float sc;
+        memcpy(&sc, pg + (int64_t)bs * d + 4 * r, 4);
+        return orc_code_to_double(pg[r * d + elem % d], cache_dtype) * (double)sc;
     }
     return orc_load(cache, cache_dtype, elem);
 }
@@ -248,8 +265,7 @@ typedef struct {
     int num_seqs, num_heads, num_kv_heads, head_dim, block_size;
     double scale;
     int window, dtype, max_blocks_per_seq, num_blocks, invalid_policy;
-    int cache_dtype;                /* element type of k_cache / v_cache */
-    const float *k_scale, *v_scale; /* row scales of 8-bit caches (else unused) */
+    int cache_dtype;                /* element type of k_cache / v_cache (8-bit: pages) */
 } orc_args;
 
 static int orc_one(const orc_args *a, int s, int h, double *out_row, int64_t *skipped)
@@ -301,7 +317,7 @@ static int orc_one(const orc_args *a, int s, int h, double *out_row, int64_t *sk
         double dot = 0.0;
         for (int j = 0; j < d; ++j)
             dot += orc_load(a->q, a->dtype, q_base + j) *
-                   orc_cache_value(a->k_cache, a->k_scale, a->cache_dtype, row[i] + j, d);
+                   orc_cache_value(a->k_cache, a->cache_dtype, row[i] + j, d, a->block_size);
         x[i] = a->scale * dot;
     }
 
@@ -322,7 +338,7 @@ static int orc_one(const orc_args *a, int s, int h, double *out_row, int64_t *sk
         const double w = exp(x[i] - m);
         denom += w;
         for (int j = 0; j < d; ++j)
-            out_row[j] += w * orc_cache_value(a->v_cache, a->v_scale, a->cache_dtype, row[i] + j, d);
+            out_row[j] += w * orc_cache_value(a->v_cache, a->cache_dtype, row[i] + j, d, a->block_size);
     }
     for (int j = 0; j < d; ++j)
         out_row[j] /= denom;
@@ -368,10 +384,9 @@ static void *orc_worker(void *p)
  * Returns 0, or a negative error; *skipped_out (nullable) receives the number
  * of tokens left out under invalid_policy 1.
  */
-/* Same, for a cache of cache_dtype (fp32/fp16/bf16, or 8-bit codes with row
- * scales k_scale / v_scale) and queries of q_dtype. */
+/* Same, for a cache of cache_dtype (fp32/fp16/bf16, or 8-bit pages) and
+ * queries of q_dtype. */
 int orc_paged_attention_cache(double *out, const void *q, const void *k_cache, const void *v_cache,
-                              const float *k_scale, const float *v_scale,
                               const int32_t *block_tables, const int32_t *context_lens,
                               int num_seqs, int num_heads, int num_kv_heads, int head_dim,
                               int block_size, double scale, int window, int q_dtype, int cache_dtype,
@@ -382,12 +397,11 @@ int orc_paged_attention_cache(double *out, const void *q, const void *k_cache, c
     const int quant = cache_dtype == ORC_I8 || cache_dtype == ORC_E4M3;
     if (num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads != 0 || head_dim <= 0 ||
         block_size <= 0 || (q_dtype != ORC_F32 && q_dtype != ORC_F16 && q_dtype != ORC_BF16) ||
-        (!quant && cache_dtype != ORC_F32 && cache_dtype != ORC_F16 && cache_dtype != ORC_BF16) ||
-        (quant && (!k_scale || !v_scale)))
+        (!quant && cache_dtype != ORC_F32 && cache_dtype != ORC_F16 && cache_dtype != ORC_BF16))
         return -4;
     orc_args a = {q, k_cache, v_cache, block_tables, context_lens, num_seqs, num_heads,
                   num_kv_heads, head_dim, block_size, scale, window, q_dtype,
-                  max_blocks_per_seq, num_blocks, invalid_policy, cache_dtype, k_scale, v_scale};
+                  max_blocks_per_seq, num_blocks, invalid_policy, cache_dtype};
     const int64_t items = pairs ? num_pairs : (int64_t)num_seqs * num_heads;
     if (pairs)
         for (int64_t i = 0; i < num_pairs; ++i)
@@ -437,7 +451,7 @@ int orc_paged_attention(double *out, const void *q, const void *k_cache, const v
 {
     if (dtype != ORC_F32 && dtype != ORC_F16 && dtype != ORC_BF16)
         return -4;
-    return orc_paged_attention_cache(out, q, k_cache, v_cache, NULL, NULL, block_tables, context_lens,
+    return orc_paged_attention_cache(out, q, k_cache, v_cache, block_tables, context_lens,
                                      num_seqs, num_heads, num_kv_heads, head_dim, block_size, scale,
                                      window, dtype, dtype, max_blocks_per_seq, num_blocks,
                                      invalid_policy, pairs, num_pairs, num_threads, skipped_out);
@@ -484,13 +498,12 @@ int64_t orc_append_kv(void *k_cache, void *v_cache, const void *k, const void *v
 }
 
 /* Quantise-on-append: token i's K and V rows (in_dtype) are quantised row by
- * row (orc_quantize_row) and the codes and scale stored at the token's slot
- * of the 8-bit pools: codes [num_blocks][H_kv][bs][d], scales
- * [num_blocks][H_kv][bs].  Slots as orc_append_kv (padding, out-of-range
- * count, duplicates refused). */
-int64_t orc_append_kv_quant(void *k_codes, void *v_codes, float *k_scales, float *v_scales, const void *k,
-                            const void *v, const int64_t *slot_mapping, int64_t num_tokens, int num_kv_heads,
-                            int head_dim, int block_size, int num_blocks, int in_dtype, int fmt)
+ * row (orc_quantize_row); the codes go to row `offset` of the slot's page and
+ * the scale to the page's scale rows (8-bit page layout above).  Slots as
+ * orc_append_kv (padding, out-of-range count, duplicates refused). */
+int64_t orc_append_kv_quant(void *k_pages, void *v_pages, const void *k, const void *v,
+                            const int64_t *slot_mapping, int64_t num_tokens, int num_kv_heads, int head_dim,
+                            int block_size, int num_blocks, int in_dtype, int fmt)
 {
     if ((fmt != ORC_I8 && fmt != ORC_E4M3) ||
         (in_dtype != ORC_F32 && in_dtype != ORC_F16 && in_dtype != ORC_BF16))
@@ -500,6 +513,7 @@ int64_t orc_append_kv_quant(void *k_codes, void *v_codes, float *k_scales, float
         for (int64_t j = 0; j < i; ++j)
             if (slot_mapping[i] >= 0 && slot_mapping[i] == slot_mapping[j])
                 return -2;
+    const int64_t page_bytes = (int64_t)(block_size + orc_scale_rows(block_size, head_dim)) * head_dim;
     int64_t bad = 0;
     for (int64_t i = 0; i < num_tokens; ++i) {
         const int64_t slot = slot_mapping[i];
@@ -512,12 +526,15 @@ int64_t orc_append_kv_quant(void *k_codes, void *v_codes, float *k_scales, float
         const int64_t phys = slot / block_size;
         const int64_t off = slot % block_size;
         for (int h = 0; h < num_kv_heads; ++h) {
-            const int64_t dst_row = (phys * num_kv_heads + h) * block_size + off;
+            const int64_t page = phys * num_kv_heads + h;
             const int64_t src_row = i * num_kv_heads + h;
-            orc_quantize_row(k, in_dtype, src_row, head_dim, fmt, (uint8_t *)k_codes + dst_row * head_dim,
-                             &k_scales[dst_row]);
-            orc_quantize_row(v, in_dtype, src_row, head_dim, fmt, (uint8_t *)v_codes + dst_row * head_dim,
-                             &v_scales[dst_row]);
+            uint8_t *kp = (uint8_t *)k_pages + page * page_bytes;
+            uint8_t *vp = (uint8_t *)v_pages + page * page_bytes;
+            float ks, vs;
+            orc_quantize_row(k, in_dtype, src_row, head_dim, fmt, kp + off * head_dim, &ks);
+            orc_quantize_row(v, in_dtype, src_row, head_dim, fmt, vp + off * head_dim, &vs);
+            memcpy(kp + (int64_t)block_size * head_dim + 4 * off, &ks, 4);
+            memcpy(vp + (int64_t)block_size * head_dim + 4 * off, &vs, 4);
         }
     }
     return bad;

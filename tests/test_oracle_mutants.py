@@ -79,12 +79,14 @@ QUANT_MUTANTS = {
                                  "const double r = floor(a / quantum + 0.5);"),
     "e4m3_no_subnormal_floor": ("    if (b < -6)\n        b = -6;\n    const double quantum",
                                 "    const double quantum"),
-    "v_read_with_k_scale": ("orc_cache_value(a->v_cache, a->v_scale, a->cache_dtype, row[i] + j, d)",
-                            "orc_cache_value(a->v_cache, a->k_scale, a->cache_dtype, row[i] + j, d)"),
-    "scale_indexed_by_block": ("* (double)scales[elem / d];", "* (double)scales[elem / d / 16];"),
+    "scale_read_one_row_late": ("memcpy(&sc, pg + (int64_t)bs * d + 4 * r, 4);",
+                                "memcpy(&sc, pg + (int64_t)bs * d + 4 * (r + 1), 4);"),
+    "page_stride_without_scale_rows": (
+        "const int64_t page_bytes = (int64_t)(bs + orc_scale_rows(bs, d)) * d;",
+        "const int64_t page_bytes = (int64_t)bs * d;"),
     "append_k_codes_from_v": (
-        "orc_quantize_row(k, in_dtype, src_row, head_dim, fmt, (uint8_t *)k_codes",
-        "orc_quantize_row(v, in_dtype, src_row, head_dim, fmt, (uint8_t *)k_codes"),
+        "orc_quantize_row(k, in_dtype, src_row, head_dim, fmt, kp + off * head_dim, &ks);",
+        "orc_quantize_row(v, in_dtype, src_row, head_dim, fmt, kp + off * head_dim, &ks);"),
 }
 
 
@@ -118,8 +120,9 @@ def _quant_pins_pass(lib) -> bool:
         return False
     # attention over a quantised cache against torch SDPA on torch-decoded values
     for fmt in ("int8", "e4m3"):
-        q, kc, vc, ks, vs, t, cl, M = _quant_identity_case(2, 4, 2, 64, 16, torch.float16, fmt, [40, 21], seed=5)
-        got = oracle.paged_attention(q, kc, vc, t, cl, num_kv_heads=2, scale=0.125, k_scale=ks, v_scale=vs, lib=lib)
+        q, kp, vp, kc, vc, ks, vs, t, cl, M = _quant_identity_case(2, 4, 2, 64, 16, torch.float16, fmt, [40, 21],
+                                                                   seed=5)
+        got = oracle.paged_attention(q, kp, vp, t, cl, num_kv_heads=2, scale=0.125, lib=lib)
         kd = _torch_dequant(kc, ks).reshape(2, M, 2, 16, 64).permute(0, 2, 1, 3, 4).reshape(2, 2, M * 16, 64)
         vd = _torch_dequant(vc, vs).reshape(2, M, 2, 16, 64).permute(0, 2, 1, 3, 4).reshape(2, 2, M * 16, 64)
         for si in range(2):
@@ -129,12 +132,13 @@ def _quant_pins_pass(lib) -> bool:
             if not np.allclose(got[si], ref.numpy(), rtol=1e-12, atol=1e-13):
                 return False
     # quantise-on-append stores each row's quantisation at its slot
-    kc = torch.zeros((4, 2, 16, 64), dtype=torch.int8)
-    vc = torch.zeros_like(kc)
-    ks, vs = torch.zeros(4, 2, 16), torch.zeros(4, 2, 16)
+    kp = torch.zeros((4, 2, 17, 64), dtype=torch.int8)
+    vp = torch.zeros_like(kp)
     k = wl.normal_tensor(30, 1, (3, 2, 64), dtype=torch.float16)
     v = wl.normal_tensor(30, 2, (3, 2, 64), dtype=torch.float16)
-    oracle.append_kv_quant(kc, vc, ks, vs, k, v, torch.tensor([5, 17, 40]), lib=lib)
+    oracle.append_kv_quant(kp, vp, k, v, torch.tensor([5, 17, 40]), lib=lib)
+    kc, ks = oracle.unpack_pages(kp)
+    vc, vs = oracle.unpack_pages(vp)
     kq, kqs = oracle.quantize_rows(k, "int8")
     vq, vqs = oracle.quantize_rows(v, "int8")
     for i, sl in enumerate([5, 17, 40]):

@@ -122,6 +122,7 @@ def test_e4m3_rows_meet_the_rounding_bound(dtype):
 
 
 def _quant_identity_case(n_seqs, n_heads, n_kv, d, bs, qdtype, fmt, lens, seed):
+    """Identity-table case with 8-bit pages; also returns the codes and scales."""
     M = max(1, max((int(L) + bs - 1) // bs for L in lens))
     nb = n_seqs * M
     k = wl.normal_tensor(seed, 11, (nb, n_kv, bs, d), dtype=torch.float16)
@@ -130,7 +131,8 @@ def _quant_identity_case(n_seqs, n_heads, n_kv, d, bs, qdtype, fmt, lens, seed):
     kc, ks = oracle.quantize_rows(k, fmt)
     vc, vs = oracle.quantize_rows(v, fmt)
     tables = torch.arange(nb, dtype=torch.int32).reshape(n_seqs, M)
-    return q, kc, vc, ks, vs, tables, torch.tensor(lens, dtype=torch.int32), M
+    return (q, oracle.pack_pages(kc, ks), oracle.pack_pages(vc, vs), kc, vc, ks, vs, tables,
+            torch.tensor(lens, dtype=torch.int32), M)
 
 
 def _torch_dequant(codes, scales):
@@ -139,12 +141,11 @@ def _torch_dequant(codes, scales):
 
 @pytest.mark.parametrize("fmt", ["int8", "e4m3"])
 @pytest.mark.parametrize("case", [(3, 8, 2, 128, 16, [40, 1, 77], 0), (2, 4, 4, 64, 8, [30, 12], 10),
-                                  (2, 8, 1, 128, 32, [65, 64], 0)])
+                                  (2, 8, 1, 128, 32, [65, 64], 0), (2, 4, 2, 64, 32, [70, 33], 0)])
 def test_quantised_cache_attention_equals_library_sdpa(fmt, case):
     n, H, hkv, d, bs, lens, window = case
-    q, kc, vc, ks, vs, t, cl, M = _quant_identity_case(n, H, hkv, d, bs, torch.bfloat16, fmt, lens, seed=5)
-    got = oracle.paged_attention(q, kc, vc, t, cl, num_kv_heads=hkv, scale=1 / math.sqrt(d), window=window,
-                                 k_scale=ks, v_scale=vs)
+    q, kp, vp, kc, vc, ks, vs, t, cl, M = _quant_identity_case(n, H, hkv, d, bs, torch.bfloat16, fmt, lens, seed=5)
+    got = oracle.paged_attention(q, kp, vp, t, cl, num_kv_heads=hkv, scale=1 / math.sqrt(d), window=window)
     # torch decodes the codes and applies the row scales; fp64 SDPA on the contiguous view
     kd, vd = _torch_dequant(kc, ks), _torch_dequant(vc, vs)
     N, G = n, H // hkv
@@ -159,14 +160,41 @@ def test_quantised_cache_attention_equals_library_sdpa(fmt, case):
         np.testing.assert_allclose(got[s], ref.numpy(), rtol=1e-12, atol=1e-13)
 
 
+def test_page_layout_by_hand():
+    """The page of (block 1, head 0) at block 16, head_dim 128: rows 0-15 the
+    codes, row 16 the 16 scales then zeros; the oracle reads element (token
+    3, dim 5) of that page as code * scale."""
+    codes = torch.zeros((2, 1, 16, 128), dtype=torch.int8)
+    scales = torch.zeros((2, 1, 16))
+    codes[1, 0, 3, 5] = -7
+    scales[1, 0, 3] = 0.25
+    pages = oracle.pack_pages(codes, scales)
+    assert tuple(pages.shape) == (2, 1, 17, 128)
+    raw = pages.view(torch.uint8)[1, 0]
+    assert int(raw[3, 5]) == 256 - 7
+    assert torch.equal(raw[16, 12:16], torch.tensor([0, 0, 128, 62], dtype=torch.uint8))  # 0.25f, little-endian
+    assert int(raw[16, 64:].sum()) == 0
+    # one token (3) attended through table [1]: the output is V's row 3 = code * scale
+    q = torch.ones((1, 1, 128), dtype=torch.float16)
+    t = torch.tensor([[1]], dtype=torch.int32)
+    cl = torch.tensor([4], dtype=torch.int32)
+    vcodes = torch.zeros_like(codes)
+    vcodes[1, 0, 3] = 9
+    vsc = torch.zeros_like(scales)
+    vsc[1, 0, 3] = 0.5
+    kp = oracle.pack_pages(torch.zeros_like(codes), torch.zeros_like(scales))
+    out = oracle.paged_attention(q, kp, oracle.pack_pages(vcodes, vsc), t, cl, num_kv_heads=1, scale=1.0)
+    np.testing.assert_allclose(out[0, 0], np.full(128, 4.5 / 4), rtol=0, atol=0)   # mean over 4 tokens
+
+
 def test_quantised_cache_k_and_v_scales_are_not_interchangeable():
     # a V-only rescale must change the output by exactly that factor; K's scale
     # moves the softmax instead
-    q, kc, vc, ks, vs, t, cl, M = _quant_identity_case(1, 2, 1, 64, 16, torch.float16, "int8", [20], seed=6)
-    base = oracle.paged_attention(q, kc, vc, t, cl, num_kv_heads=1, scale=0.125, k_scale=ks, v_scale=vs)
-    twice_v = oracle.paged_attention(q, kc, vc, t, cl, num_kv_heads=1, scale=0.125, k_scale=ks, v_scale=vs * 2)
+    q, kp, vp, kc, vc, ks, vs, t, cl, M = _quant_identity_case(1, 2, 1, 64, 16, torch.float16, "int8", [20], seed=6)
+    base = oracle.paged_attention(q, kp, vp, t, cl, num_kv_heads=1, scale=0.125)
+    twice_v = oracle.paged_attention(q, kp, oracle.pack_pages(vc, vs * 2), t, cl, num_kv_heads=1, scale=0.125)
     np.testing.assert_allclose(twice_v, 2 * base, rtol=1e-14, atol=0)
-    k_zero = oracle.paged_attention(q, kc, vc, t, cl, num_kv_heads=1, scale=0.125, k_scale=ks * 0, v_scale=vs)
+    k_zero = oracle.paged_attention(q, oracle.pack_pages(kc, ks * 0), vp, t, cl, num_kv_heads=1, scale=0.125)
     vd = _torch_dequant(vc, vs)                                       # [M, 1, 16, 64], blocks in order
     mean_v = vd.permute(1, 0, 2, 3).reshape(1, -1, 64)[0, :20].mean(dim=0).numpy()  # zero scores -> mean of V
     np.testing.assert_allclose(k_zero[0, 0], mean_v, rtol=1e-12, atol=1e-14)
@@ -175,78 +203,83 @@ def test_quantised_cache_k_and_v_scales_are_not_interchangeable():
 
 @pytest.mark.parametrize("fmt", ["int8", "e4m3"])
 def test_quantised_cache_block_permutation_is_bit_identical(fmt):
-    q, kc, vc, ks, vs, t, cl, M = _quant_identity_case(2, 4, 2, 64, 16, torch.float16, fmt, [50, 33], seed=8)
-    base = oracle.paged_attention(q, kc, vc, t, cl, num_kv_heads=2, scale=0.125, k_scale=ks, v_scale=vs)
-    perm = wl.permutation(9, 1, kc.shape[0])
+    q, kp, vp, *_, t, cl, M = _quant_identity_case(2, 4, 2, 64, 16, torch.float16, fmt, [50, 33], seed=8)
+    base = oracle.paged_attention(q, kp, vp, t, cl, num_kv_heads=2, scale=0.125)
+    perm = wl.permutation(9, 1, kp.shape[0])
     inv = torch.empty_like(perm)
     inv[perm] = torch.arange(perm.numel())
     # physical block p moves to slot inv[p]; tables follow
-    moved = [x[perm] for x in (kc, vc, ks, vs)]
-    got = oracle.paged_attention(q, moved[0], moved[1], inv[t.long()].to(torch.int32), cl, num_kv_heads=2,
-                                 scale=0.125, k_scale=moved[2], v_scale=moved[3])
+    got = oracle.paged_attention(q, kp[perm], vp[perm], inv[t.long()].to(torch.int32), cl, num_kv_heads=2,
+                                 scale=0.125)
     assert np.array_equal(base, got)
 
 
 @pytest.mark.parametrize("fmt", ["int8", "e4m3"])
 @pytest.mark.parametrize("in_dtype", [torch.float16, torch.bfloat16])
-def test_append_quant_stores_the_row_quantisation_at_the_slot(fmt, in_dtype):
-    nb, hkv, bs, d, T = 12, 2, 16, 64, 9
+@pytest.mark.parametrize("bs,d", [(16, 64), (32, 64), (8, 128)])
+def test_append_quant_stores_the_row_quantisation_at_the_slot(fmt, in_dtype, bs, d):
+    nb, hkv, T = 12, 2, 9
     code_dtype = torch.int8 if fmt == "int8" else torch.float8_e4m3fn
-    kc = torch.zeros((nb, hkv, bs, d), dtype=torch.uint8).view(code_dtype)
-    vc = torch.zeros_like(kc)
-    ks = torch.full((nb, hkv, bs), -1.0)
-    vs = torch.full((nb, hkv, bs), -1.0)
+    rows = bs + oracle.scale_rows(bs, d)
+    kp = torch.full((nb, hkv, rows, d), 0x55, dtype=torch.uint8).view(code_dtype)
+    vp = torch.full_like(kp.view(torch.uint8), 0x66).view(code_dtype)
+    k0, v0 = kp.clone(), vp.clone()
     k = wl.normal_tensor(30, 1, (T, hkv, d), dtype=in_dtype)
     v = wl.normal_tensor(30, 2, (T, hkv, d), dtype=in_dtype)
     slots = wl.permutation(31, 1, nb * bs)[:T].clone()
     slots[4] = -1
-    bad = oracle.append_kv_quant(kc, vc, ks, vs, k, v, slots)
-    assert bad == 0
+    assert oracle.append_kv_quant(kp, vp, k, v, slots) == 0
     kq, kqs = oracle.quantize_rows(k, fmt)
     vq, vqs = oracle.quantize_rows(v, fmt)
+    kc, ks = oracle.unpack_pages(kp)
+    vc, vs = oracle.unpack_pages(vp)
+    kc0, ks0 = oracle.unpack_pages(k0)
     touched = torch.zeros((nb, bs), dtype=torch.bool)
     for i in range(T):
         sl = int(slots[i])
         if sl < 0:
             continue
-        p, o = sl // bs, sl % bs
-        touched[p, o] = True
-        assert torch.equal(kc[p, :, o].view(torch.uint8), kq[i].view(torch.uint8))
-        assert torch.equal(vc[p, :, o].view(torch.uint8), vq[i].view(torch.uint8))
-        assert torch.equal(ks[p, :, o], kqs[i]) and torch.equal(vs[p, :, o], vqs[i])
-    # untouched slots keep their bytes
-    assert bool((ks.permute(0, 2, 1)[~touched] == -1.0).all())
-    assert int(kc.view(torch.uint8).permute(0, 2, 1, 3)[~touched].max()) == 0
+        pb, o = sl // bs, sl % bs
+        touched[pb, o] = True
+        assert torch.equal(kc[pb, :, o].view(torch.uint8), kq[i].view(torch.uint8))
+        assert torch.equal(vc[pb, :, o].view(torch.uint8), vq[i].view(torch.uint8))
+        assert torch.equal(ks[pb, :, o], kqs[i]) and torch.equal(vs[pb, :, o], vqs[i])
+    # untouched rows and scales keep their bytes; the padding after the scales too
+    untouched = ~touched
+    assert torch.equal(kc.view(torch.uint8).permute(0, 2, 1, 3)[untouched],
+                       kc0.view(torch.uint8).permute(0, 2, 1, 3)[untouched])
+    assert torch.equal(ks.permute(0, 2, 1)[untouched].view(torch.int32),
+                       ks0.permute(0, 2, 1)[untouched].view(torch.int32))
+    pad = kp.view(torch.uint8)[:, :, bs:].reshape(nb, hkv, -1)[:, :, 4 * bs:]
+    assert bool((pad == 0x55).all())
     # duplicates refused, out-of-range counted
     with pytest.raises(ValueError):
-        oracle.append_kv_quant(kc, vc, ks, vs, k[:2], v[:2], torch.tensor([3, 3]))
-    assert oracle.append_kv_quant(kc, vc, ks, vs, k[:1], v[:1], torch.tensor([nb * bs])) == 1
+        oracle.append_kv_quant(kp, vp, k[:2], v[:2], torch.tensor([3, 3]))
+    assert oracle.append_kv_quant(kp, vp, k[:1], v[:1], torch.tensor([nb * bs])) == 1
 
 
 def test_append_quant_worked_example_slot():
     """Token 34 through the page's table [7, 1, 3] (block size 16): its codes
-    and scale land at physical block 3, offset 2."""
+    and scale land in the page of physical block 3, row 2."""
     g = json.loads((GOLDEN / "locate_worked_example.json").read_text())
     bs = g["block_size"]
-    kc = torch.zeros((8, 1, bs, 64), dtype=torch.int8)
-    vc = torch.zeros_like(kc)
-    ks, vs = torch.zeros(8, 1, bs), torch.zeros(8, 1, bs)
+    kp = torch.zeros((8, 1, bs + 1, 64), dtype=torch.int8)
+    vp = torch.zeros_like(kp)
     row = torch.full((1, 1, 64), 3.0, dtype=torch.float16)
     slot = g["physical"] * bs + g["offset"]
-    oracle.append_kv_quant(kc, vc, ks, vs, row, row, torch.tensor([slot]))
+    oracle.append_kv_quant(kp, vp, row, row, torch.tensor([slot]))
+    kc, ks = oracle.unpack_pages(kp)
     assert float(ks[3, 0, 2]) == float(torch.tensor(3.0) / 127.0) and bool((kc[3, 0, 2] == 127).all())
     assert int((kc != 0).sum()) == 64 and int((ks != 0).sum()) == 1
 
 
-def test_quantised_pool_copy_moves_codes_and_scales():
+def test_quantised_page_copy_moves_codes_and_scales():
     nb, hkv, bs, d = 6, 2, 8, 64
-    kc = (wl.bits64(40, 1, nb * hkv * bs * d) & 0xFF).to(torch.uint8).reshape(nb, hkv, bs, d).view(torch.int8)
-    vc = (wl.bits64(40, 2, nb * hkv * bs * d) & 0xFF).to(torch.uint8).reshape(nb, hkv, bs, d).view(torch.int8)
-    ks, vs = torch.rand(nb, hkv, bs), torch.rand(nb, hkv, bs)
-    k0, v0, ks0, vs0 = kc.clone(), vc.clone(), ks.clone(), vs.clone()
-    oracle.copy_blocks(kc, vc, [[1, 4]])
-    oracle.copy_blocks(ks, vs, [[1, 4]])
-    assert torch.equal(kc[4], k0[1]) and torch.equal(vc[4], v0[1])
-    assert torch.equal(ks[4], ks0[1]) and torch.equal(vs[4], vs0[1])
+    codes = (wl.bits64(40, 1, nb * hkv * bs * d) & 0xFF).to(torch.uint8).reshape(nb, hkv, bs, d).view(torch.int8)
+    kp = oracle.pack_pages(codes, torch.rand(nb, hkv, bs))
+    vp = oracle.pack_pages(codes.flip(0), torch.rand(nb, hkv, bs))
+    k0, v0 = kp.clone(), vp.clone()
+    oracle.copy_blocks(kp, vp, [[1, 4]])
+    assert torch.equal(kp[4], k0[1]) and torch.equal(vp[4], v0[1])
     keep = [0, 1, 2, 3, 5]
-    assert torch.equal(kc[keep], k0[keep]) and torch.equal(ks[keep], ks0[keep])
+    assert torch.equal(kp[keep], k0[keep]) and torch.equal(vp[keep], v0[keep])
