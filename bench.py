@@ -291,9 +291,10 @@ class DecodeAppendStep(Step):
             # 8-bit pools: random codes and row scales from the seeded generator
             # (the 16-bit pools are dropped); the new tokens are quantised on append
             self.k_cache = self.v_cache = inp.k_cache = inp.v_cache = None
-            self.kq, self.vq, self.ks, self.vs = wl.quant_pools(inp, self.kv_format, device=device)
+            self.kq, self.vq = wl.quant_pools(inp, self.kv_format, device=device)
             self.description += (f"; 8-bit cache: {self.kv_format.upper()} codes + one fp32 scale per "
-                                 f"(token, kv head) row, step = pa_decode_quant + pa_append_kv_quant")
+                                 f"(token, kv head) row in (block, kv head) pages, "
+                                 f"step = pa_decode_quant + pa_append_kv_quant")
             self.dec_bytes = acc.decode_bytes(inp.context_lens, s.num_heads, s.num_kv_heads, s.head_dim,
                                               s.block_size, 1, out_elt_bytes=4, q_elt_bytes=elt, row_scale_bytes=4)
         else:
@@ -306,7 +307,7 @@ class DecodeAppendStep(Step):
     def decode(self, stream, q=None, bt=None, cl=None):
         s = self.shape
         if self.kv_format:
-            self.pa.pa_decode_quant(self.out, self.q if q is None else q, self.kq, self.vq, self.ks, self.vs,
+            self.pa.pa_decode_quant(self.out, self.q if q is None else q, self.kq, self.vq,
                                     self.bt if bt is None else bt, self.cl if cl is None else cl,
                                     num_kv_heads=s.num_kv_heads, window=self.window, partition_size=self.partition,
                                     workspace=self.ws, err_word=self.err, stream=stream)
@@ -321,15 +322,14 @@ class DecodeAppendStep(Step):
         vn = self.v_new if v_new is None else v_new
         sl = self.slots if slots is None else slots
         if self.kv_format:
-            self.pa.pa_append_kv_quant(kn, vn, sl, self.kq, self.vq, self.ks, self.vs, err_word=self.err,
-                                       stream=stream)
+            self.pa.pa_append_kv_quant(kn, vn, sl, self.kq, self.vq, err_word=self.err, stream=stream)
             return
         self.pa.pa_append_kv(kn, vn, sl, self.k_cache, self.v_cache, err_word=self.err, stream=stream)
 
     def cache_args(self):
         """(k, v, extra oracle kwargs) of the cache for the oracle."""
         if self.kv_format:
-            return self.kq, self.vq, {"k_scale": self.ks, "v_scale": self.vs}
+            return self.kq, self.vq, {}
         return self.k_cache, self.v_cache, {}
 
     def e2e(self, stream, dev):
@@ -349,12 +349,11 @@ class DecodeAppendStep(Step):
         n = s.num_seqs if rows is None else rows
         if self.kv_format:
             if not hasattr(self, "_h"):
-                self._h = [t.cpu() for t in (self.q, self.kq, self.vq, self.ks, self.vs, self.k_new, self.v_new)]
-            q, kq, vq, ks, vs, kn, vn = self._h
+                self._h = [t.cpu() for t in (self.q, self.kq, self.vq, self.k_new, self.v_new)]
+            q, kq, vq, kn, vn = self._h
             oracle.paged_attention(q[:n], kq, vq, self.inp.block_tables[:n], self.inp.context_lens[:n],
-                                   num_kv_heads=s.num_kv_heads, scale=1.0 / math.sqrt(s.head_dim), threads=threads,
-                                   k_scale=ks, v_scale=vs)
-            oracle.append_kv_quant(kq, vq, ks, vs, kn, vn, self.host["slots"])
+                                   num_kv_heads=s.num_kv_heads, scale=1.0 / math.sqrt(s.head_dim), threads=threads)
+            oracle.append_kv_quant(kq, vq, kn, vn, self.host["slots"])
             return int(self.inp.context_lens[:n].to(torch.int64).sum()) * 2 * s.num_kv_heads * (s.head_dim + 4)
         if not hasattr(self, "_h"):
             self._h = [t.cpu() for t in (self.q, self.k_cache, self.v_cache, self.k_new, self.v_new)]

@@ -271,21 +271,27 @@ PA_API pa_status pa_swap_blocks(const int64_t *src_dst_pairs, int num_pairs, con
  *                     ties to even, saturating at +-448,
  * a row of zeros storing scale 0 and zero codes.  The cached value of an
  * element is code * scale.
- * Pools: k_cache / v_cache hold the codes, one byte per element, in the
- * layout of the 16-bit caches; k_scale / v_scale are fp32
- * [num_blocks][num_kv_heads][block_size] (16-byte aligned).
+ * Pools are pages: k_cache / v_cache are [num_blocks][num_kv_heads][page]
+ * with page = pa_quant_page_bytes(head_dim, block_size) bytes: the block's
+ * block_size code rows of head_dim bytes (one byte per element), then
+ * ceil(4 * block_size / head_dim) rows whose first 4 * block_size bytes are
+ * the rows' fp32 scales (little-endian, in row order; the rest is padding).
+ * A page moves with one contiguous copy, its scales included.
  */
+
+/* Bytes of one (block, kv head) page of an 8-bit pool (0 for bad arguments). */
+PA_API size_t pa_quant_page_bytes(int head_dim, int block_size);
 
 /*
  * Quantise-on-append: token i's K and V rows (dtype PA_F32 / PA_F16 /
  * PA_BF16, [num_tokens][num_kv_heads][head_dim]) are quantised row by row as
- * above and their codes and scales written at slot_mapping[i] (padding and
- * out-of-range slots as pa_append_kv).  cache_dtype is PA_I8 or PA_E4M3.
+ * above; the codes go to row slot % block_size of the slot's page, the scale
+ * to the page's scale rows (padding and out-of-range slots as pa_append_kv).
+ * cache_dtype is PA_I8 or PA_E4M3.
  */
 PA_API pa_status pa_append_kv_quant(const void *k, const void *v, const int64_t *slot_mapping, void *k_cache,
-                                    void *v_cache, float *k_scale, float *v_scale, int num_tokens,
-                                    int num_kv_heads, int head_dim, int block_size, int num_blocks,
-                                    pa_dtype dtype, pa_dtype cache_dtype, uint32_t *err_word,
+                                    void *v_cache, int num_tokens, int num_kv_heads, int head_dim, int block_size,
+                                    int num_blocks, pa_dtype dtype, pa_dtype cache_dtype, uint32_t *err_word,
                                     pa_stream_t stream);
 
 /*
@@ -295,25 +301,23 @@ PA_API pa_status pa_append_kv_quant(const void *k, const void *v, const int64_t 
  * is pa_decode_workspace_size() bytes, as for pa_decode.
  */
 PA_API pa_status pa_decode_quant(void *out, const void *q, const void *k_cache, const void *v_cache,
-                                 const float *k_scale, const float *v_scale, const int32_t *block_tables,
-                                 const int32_t *context_lens, int num_seqs, int num_heads, int num_kv_heads,
-                                 int head_dim, int block_size, float scale, int window, pa_dtype dtype,
-                                 pa_dtype cache_dtype, pa_dtype out_dtype, int max_blocks_per_seq,
-                                 int num_blocks, int partition_size, void *workspace, size_t workspace_bytes,
-                                 uint32_t *err_word, pa_stream_t stream);
+                                 const int32_t *block_tables, const int32_t *context_lens, int num_seqs,
+                                 int num_heads, int num_kv_heads, int head_dim, int block_size, float scale,
+                                 int window, pa_dtype dtype, pa_dtype cache_dtype, pa_dtype out_dtype,
+                                 int max_blocks_per_seq, int num_blocks, int partition_size, void *workspace,
+                                 size_t workspace_bytes, uint32_t *err_word, pa_stream_t stream);
 
-/* pa_copy_blocks for an 8-bit cache: codes and scales of each pair's block. */
+/* pa_copy_blocks for 8-bit pools: whole pages (codes and scales). */
 PA_API pa_status pa_copy_blocks_quant(const int64_t *src_dst_pairs, int num_pairs, void *k_cache, void *v_cache,
-                                      float *k_scale, float *v_scale, int num_kv_heads, int head_dim,
-                                      int block_size, int num_blocks, uint32_t *err_word, pa_stream_t stream);
+                                      int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                                      uint32_t *err_word, pa_stream_t stream);
 
-/* pa_swap_blocks for 8-bit pools: codes and scales (either side may be
+/* pa_swap_blocks for 8-bit pools: whole pages (either side may be
  * GPU-addressable host memory, as pa_swap_blocks). */
 PA_API pa_status pa_swap_blocks_quant(const int64_t *src_dst_pairs, int num_pairs, const void *src_k,
-                                      const void *src_v, const float *src_k_scale, const float *src_v_scale,
-                                      void *dst_k, void *dst_v, float *dst_k_scale, float *dst_v_scale,
-                                      int src_num_blocks, int dst_num_blocks, int num_kv_heads, int head_dim,
-                                      int block_size, uint32_t *err_word, pa_stream_t stream);
+                                      const void *src_v, void *dst_k, void *dst_v, int src_num_blocks,
+                                      int dst_num_blocks, int num_kv_heads, int head_dim, int block_size,
+                                      uint32_t *err_word, pa_stream_t stream);
 
 /* Static text for a status code. */
 PA_API const char *pa_status_string(pa_status status);

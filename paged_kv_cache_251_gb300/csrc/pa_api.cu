@@ -189,26 +189,6 @@ pa_status q_tensor_map(CUtensorMap *map, const void *base, int dtype, int head_d
     return PA_OK;
 }
 
-// 3-D view of an 8-bit code pool with head_dim 128 as [tile][row][128 bytes];
-// one box is a whole (block, head) tile (128-byte swizzle).
-pa_status code_tensor_map(CUtensorMap *map, const void *base, int block_size, long long tiles) {
-    PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
-    cudaError_t e = tensor_map_encoder(&enc);
-    if (e != cudaSuccess || !enc)
-        return cuda_fail(e == cudaSuccess ? cudaErrorSymbolNotFound : e, "cuTensorMapEncodeTiled lookup");
-    cuuint64_t dims[3] = {128, static_cast<cuuint64_t>(block_size), static_cast<cuuint64_t>(tiles)};
-    cuuint64_t strides[2] = {128, 128ull * block_size};
-    cuuint32_t box[3] = {128, static_cast<cuuint32_t>(block_size), 1};
-    cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(base), dims, strides, box, estr,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS)
-        return fail(PA_ERR_INVALID_ARGUMENT, "cuTensorMapEncodeTiled rejected the code pool layout (code " +
-                                                 std::to_string(static_cast<int>(r)) + ")");
-    return PA_OK;
-}
-
 constexpr int kDefaultPartition = 512;
 constexpr int kQ8fStageBudget = 48 * 1024;
 constexpr int kMhaStageBudget = 64 * 1024;
@@ -347,18 +327,12 @@ pa_status launch_decode_q8_kernel(DecodeParams &p, int cache_dtype, int head_dim
             return fail(PA_ERR_UNSUPPORTED, "no 8-bit-cache decode kernel for this group / block size");
         // stages are owned round-robin by the consumer warps: a multiple of
         // their count keeps each stage with one warp (no phase aliasing)
-        const int stage = 2 * p.block_size * (kQ8fD + 4);
+        const int stage = 2 * q8_page_bytes(p.block_size, kQ8fD);
         int S = kQ8fStageBudget / stage;
         S -= S % kQ8fWarps;
         S = S < kQ8fWarps ? kQ8fWarps : (S > 16 ? 16 : S);
         p.stages = S;
         const size_t smem = q8f_smem_layout(S, p.block_size, G).total;
-        CUtensorMap tmk, tmv;
-        pa_status ts = code_tensor_map(&tmk, p.k_cache, p.block_size, tiles);
-        if (ts == PA_OK)
-            ts = code_tensor_map(&tmv, p.v_cache, p.block_size, tiles);
-        if (ts != PA_OK)
-            return ts;
         int dev = 0, sms = 0, per_sm = 0;
         cudaError_t e = device_sms(&dev, &sms);
         if (e != cudaSuccess)
@@ -374,7 +348,7 @@ pa_status launch_decode_q8_kernel(DecodeParams &p, int cache_dtype, int head_dim
             grid = items_max;
         if (grid < 1)
             grid = 1;
-        void *args[] = {&p, &tmk, &tmv};
+        void *args[] = {&p};
         e = cudaLaunchKernel(ffn, dim3(static_cast<unsigned>(grid)), dim3(kQ8fThreads), args, smem, cs);
         if (e != cudaSuccess)
             return cuda_fail(e, "decode launch");
@@ -486,8 +460,6 @@ pa_status pa_decode(void *out, const void *q, const void *k_cache, const void *v
     p.scale_log2 = scale * 1.4426950408889634f;
     p.start_tok = nullptr;
     p.force_partial = 0;
-    p.k_scale = nullptr;
-    p.v_scale = nullptr;
     p.q_dtype = dtype;
 
     const pa_status ls = launch_decode_kernel(p, dtype, head_dim, G, reinterpret_cast<cudaStream_t>(stream));
@@ -603,8 +575,14 @@ pa_status pa_swap_blocks(const int64_t *src_dst_pairs, int num_pairs, const void
     return PA_OK;
 }
 
-pa_status pa_decode_quant(void *out, const void *q, const void *k_cache, const void *v_cache, const float *k_scale,
-                          const float *v_scale, const int32_t *block_tables, const int32_t *context_lens,
+size_t pa_quant_page_bytes(int head_dim, int block_size) {
+    if (!head_dim_ok(head_dim) || !block_size_ok(block_size))
+        return 0;
+    return static_cast<size_t>(q8_page_bytes(block_size, head_dim));
+}
+
+pa_status pa_decode_quant(void *out, const void *q, const void *k_cache, const void *v_cache,
+                          const int32_t *block_tables, const int32_t *context_lens,
                           int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size, float scale,
                           int window, pa_dtype dtype, pa_dtype cache_dtype, pa_dtype out_dtype,
                           int max_blocks_per_seq, int num_blocks, int partition_size, void *workspace,
@@ -617,7 +595,7 @@ pa_status pa_decode_quant(void *out, const void *q, const void *k_cache, const v
         return st;
     if (num_seqs == 0)
         return PA_OK;
-    if (!out || !q || !k_cache || !v_cache || !k_scale || !v_scale || !block_tables || !context_lens)
+    if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens)
         return fail(PA_ERR_INVALID_ARGUMENT, "null pointer");
     if (num_kv_heads <= 0 || num_heads % num_kv_heads != 0)
         return fail(PA_ERR_INVALID_ARGUMENT, "num_heads must be a multiple of num_kv_heads");
@@ -630,8 +608,8 @@ pa_status pa_decode_quant(void *out, const void *q, const void *k_cache, const v
         return fail(PA_ERR_INVALID_ARGUMENT, "num_blocks must be positive");
     if (!std::isfinite(scale))
         return fail(PA_ERR_INVALID_ARGUMENT, "scale must be finite");
-    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(k_scale) || !aligned16(v_scale))
-        return fail(PA_ERR_INVALID_ARGUMENT, "q, the code pools and the scale pools must be 16-byte aligned");
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
+        return fail(PA_ERR_INVALID_ARGUMENT, "q and the page pools must be 16-byte aligned");
     if ((reinterpret_cast<uintptr_t>(out) & (elt_bytes(out_dtype) - 1)) != 0)
         return fail(PA_ERR_INVALID_ARGUMENT, "out is not aligned to its element size");
     if (plan.workspace > 0 && (workspace == nullptr || workspace_bytes < plan.workspace))
@@ -665,8 +643,6 @@ pa_status pa_decode_quant(void *out, const void *q, const void *k_cache, const v
     p.scale_log2 = scale * 1.4426950408889634f;
     p.start_tok = nullptr;
     p.force_partial = 0;
-    p.k_scale = k_scale;
-    p.v_scale = v_scale;
     p.q_dtype = dtype;
 
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
@@ -685,9 +661,8 @@ pa_status pa_decode_quant(void *out, const void *q, const void *k_cache, const v
 }
 
 pa_status pa_append_kv_quant(const void *k, const void *v, const int64_t *slot_mapping, void *k_cache, void *v_cache,
-                             float *k_scale, float *v_scale, int num_tokens, int num_kv_heads, int head_dim,
-                             int block_size, int num_blocks, pa_dtype dtype, pa_dtype cache_dtype,
-                             uint32_t *err_word, pa_stream_t stream) {
+                             int num_tokens, int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                             pa_dtype dtype, pa_dtype cache_dtype, uint32_t *err_word, pa_stream_t stream) {
     g_detail.clear();
     if (num_tokens < 0 || num_kv_heads <= 0 || num_blocks <= 0)
         return fail(PA_ERR_INVALID_ARGUMENT, "num_tokens, num_kv_heads or num_blocks out of range");
@@ -699,28 +674,26 @@ pa_status pa_append_kv_quant(const void *k, const void *v, const int64_t *slot_m
         return fail(PA_ERR_INVALID_ARGUMENT, "unknown dtype (rows: PA_F32/F16/BF16; cache: PA_I8/PA_E4M3)");
     if (num_tokens == 0)
         return PA_OK;
-    if (!k || !v || !slot_mapping || !k_cache || !v_cache || !k_scale || !v_scale)
+    if (!k || !v || !slot_mapping || !k_cache || !v_cache)
         return fail(PA_ERR_INVALID_ARGUMENT, "null pointer");
-    if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(k_scale) ||
-        !aligned16(v_scale))
-        return fail(PA_ERR_INVALID_ARGUMENT, "k, v, the code pools and the scale pools must be 16-byte aligned");
+    if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache))
+        return fail(PA_ERR_INVALID_ARGUMENT, "k, v and the page pools must be 16-byte aligned");
     if ((reinterpret_cast<uintptr_t>(slot_mapping) & 7u) != 0)
         return fail(PA_ERR_INVALID_ARGUMENT, "slot_mapping must be 8-byte aligned");
     int dev = 0, sms = 0;
     cudaError_t e = device_sms(&dev, &sms);
     if (e != cudaSuccess)
         return cuda_fail(e, "device query");
-    e = launch_append_quant(k, v, slot_mapping, k_cache, v_cache, k_scale, v_scale, num_tokens, num_kv_heads,
-                            head_dim, dtype, cache_dtype, block_size, num_blocks, err_word, sms,
-                            reinterpret_cast<cudaStream_t>(stream));
+    e = launch_append_quant(k, v, slot_mapping, k_cache, v_cache, num_tokens, num_kv_heads, head_dim, dtype,
+                            cache_dtype, block_size, num_blocks, err_word, sms, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess)
         return cuda_fail(e, "append launch");
     return PA_OK;
 }
 
 pa_status pa_copy_blocks_quant(const int64_t *src_dst_pairs, int num_pairs, void *k_cache, void *v_cache,
-                               float *k_scale, float *v_scale, int num_kv_heads, int head_dim, int block_size,
-                               int num_blocks, uint32_t *err_word, pa_stream_t stream) {
+                               int num_kv_heads, int head_dim, int block_size, int num_blocks, uint32_t *err_word,
+                               pa_stream_t stream) {
     g_detail.clear();
     if (num_pairs < 0 || num_kv_heads <= 0 || num_blocks <= 0)
         return fail(PA_ERR_INVALID_ARGUMENT, "num_pairs, num_kv_heads or num_blocks out of range");
@@ -730,33 +703,27 @@ pa_status pa_copy_blocks_quant(const int64_t *src_dst_pairs, int num_pairs, void
         return fail(PA_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
     if (num_pairs == 0)
         return PA_OK;
-    if (!src_dst_pairs || !k_cache || !v_cache || !k_scale || !v_scale)
+    if (!src_dst_pairs || !k_cache || !v_cache)
         return fail(PA_ERR_INVALID_ARGUMENT, "null pointer");
-    if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(k_scale) || !aligned16(v_scale))
-        return fail(PA_ERR_INVALID_ARGUMENT, "the code and scale pools must be 16-byte aligned");
+    if (!aligned16(k_cache) || !aligned16(v_cache))
+        return fail(PA_ERR_INVALID_ARGUMENT, "the page pools must be 16-byte aligned");
     if ((reinterpret_cast<uintptr_t>(src_dst_pairs) & 7u) != 0)
         return fail(PA_ERR_INVALID_ARGUMENT, "src_dst_pairs must be 8-byte aligned");
     int dev = 0, sms = 0;
     cudaError_t e = device_sms(&dev, &sms);
     if (e != cudaSuccess)
         return cuda_fail(e, "device query");
-    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-    const long long code_bytes = static_cast<long long>(num_kv_heads) * block_size * head_dim;
-    const long long scale_bytes = static_cast<long long>(num_kv_heads) * block_size * 4;
-    e = launch_copy_blocks(src_dst_pairs, num_pairs, k_cache, v_cache, code_bytes, num_blocks, err_word, sms, cs);
-    if (e == cudaSuccess)
-        e = launch_copy_blocks(src_dst_pairs, num_pairs, k_scale, v_scale, scale_bytes, num_blocks, err_word, sms,
-                               cs);
+    const long long block_bytes = static_cast<long long>(num_kv_heads) * q8_page_bytes(block_size, head_dim);
+    e = launch_copy_blocks(src_dst_pairs, num_pairs, k_cache, v_cache, block_bytes, num_blocks, err_word, sms,
+                           reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess)
         return cuda_fail(e, "copy_blocks launch");
     return PA_OK;
 }
 
 pa_status pa_swap_blocks_quant(const int64_t *src_dst_pairs, int num_pairs, const void *src_k, const void *src_v,
-                               const float *src_k_scale, const float *src_v_scale, void *dst_k, void *dst_v,
-                               float *dst_k_scale, float *dst_v_scale, int src_num_blocks, int dst_num_blocks,
-                               int num_kv_heads, int head_dim, int block_size, uint32_t *err_word,
-                               pa_stream_t stream) {
+                               void *dst_k, void *dst_v, int src_num_blocks, int dst_num_blocks, int num_kv_heads,
+                               int head_dim, int block_size, uint32_t *err_word, pa_stream_t stream) {
     g_detail.clear();
     if (num_pairs < 0 || num_kv_heads <= 0 || src_num_blocks <= 0 || dst_num_blocks <= 0)
         return fail(PA_ERR_INVALID_ARGUMENT, "num_pairs, num_kv_heads or a pool size out of range");
@@ -766,11 +733,9 @@ pa_status pa_swap_blocks_quant(const int64_t *src_dst_pairs, int num_pairs, cons
         return fail(PA_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
     if (num_pairs == 0)
         return PA_OK;
-    if (!src_dst_pairs || !src_k || !src_v || !dst_k || !dst_v || !src_k_scale || !src_v_scale || !dst_k_scale ||
-        !dst_v_scale)
+    if (!src_dst_pairs || !src_k || !src_v || !dst_k || !dst_v)
         return fail(PA_ERR_INVALID_ARGUMENT, "null pointer");
-    if (!aligned16(src_k) || !aligned16(src_v) || !aligned16(dst_k) || !aligned16(dst_v) ||
-        !aligned16(src_k_scale) || !aligned16(src_v_scale) || !aligned16(dst_k_scale) || !aligned16(dst_v_scale))
+    if (!aligned16(src_k) || !aligned16(src_v) || !aligned16(dst_k) || !aligned16(dst_v))
         return fail(PA_ERR_INVALID_ARGUMENT, "the pools must be 16-byte aligned");
     if ((reinterpret_cast<uintptr_t>(src_dst_pairs) & 7u) != 0)
         return fail(PA_ERR_INVALID_ARGUMENT, "src_dst_pairs must be 8-byte aligned");
@@ -778,14 +743,9 @@ pa_status pa_swap_blocks_quant(const int64_t *src_dst_pairs, int num_pairs, cons
     cudaError_t e = device_sms(&dev, &sms);
     if (e != cudaSuccess)
         return cuda_fail(e, "device query");
-    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-    const long long code_bytes = static_cast<long long>(num_kv_heads) * block_size * head_dim;
-    const long long scale_bytes = static_cast<long long>(num_kv_heads) * block_size * 4;
-    e = launch_swap_blocks(src_dst_pairs, num_pairs, src_k, src_v, dst_k, dst_v, code_bytes, src_num_blocks,
-                           dst_num_blocks, err_word, sms, cs);
-    if (e == cudaSuccess)
-        e = launch_swap_blocks(src_dst_pairs, num_pairs, src_k_scale, src_v_scale, dst_k_scale, dst_v_scale,
-                               scale_bytes, src_num_blocks, dst_num_blocks, err_word, sms, cs);
+    const long long block_bytes = static_cast<long long>(num_kv_heads) * q8_page_bytes(block_size, head_dim);
+    e = launch_swap_blocks(src_dst_pairs, num_pairs, src_k, src_v, dst_k, dst_v, block_bytes, src_num_blocks,
+                           dst_num_blocks, err_word, sms, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess)
         return cuda_fail(e, "swap_blocks launch");
     return PA_OK;

@@ -65,19 +65,21 @@ __global__ void __launch_bounds__(256) append_kernel(const uint4 *__restrict__ k
 // Quantise-on-append: one warp per (token, kv head) row of K and of V.  Each
 // lane holds D / 32 consecutive elements; the row's absolute maximum is a warp
 // max, the scale amax / Q is one IEEE fp32 division, and every code is decided
-// from the IEEE fp32 quotient x / scale (pa_quant.cuh).  Codes are stored as
-// one (D / 32)-byte word per lane (a coalesced row), the scale by lane 0.
+// from the IEEE fp32 quotient x / scale (pa_quant.cuh).  Codes go to the row's
+// line of the slot's page as one (D / 32)-byte word per lane (a coalesced
+// row), the scale to the page's scale rows (lane 0).
 template <int Fmt, int D>
 __global__ void __launch_bounds__(256) append_quant_kernel(const char *__restrict__ k, const char *__restrict__ v,
-                                                           const int64_t *__restrict__ slots, uint8_t *k_codes,
-                                                           uint8_t *v_codes, float *k_scale, float *v_scale,
-                                                           long long num_tokens, int num_kv_heads, int in_dtype,
-                                                           int block_size, long long pool_slots, uint32_t *err) {
+                                                           const int64_t *__restrict__ slots, uint8_t *k_pages,
+                                                           uint8_t *v_pages, long long num_tokens, int num_kv_heads,
+                                                           int in_dtype, int block_size, long long pool_slots,
+                                                           uint32_t *err) {
     constexpr int E = D / 32;
     const int lane = threadIdx.x & 31;
     const long long rows = num_tokens * num_kv_heads;
     const long long warps = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
     const int elt = in_dtype == PA_F32 ? 4 : 2;
+    const long long page_bytes = q8_page_bytes(block_size, D);
     for (long long w = blockIdx.x * static_cast<long long>(blockDim.x >> 5) + (threadIdx.x >> 5); w < 2 * rows;
          w += warps) {
         const bool is_v = w >= rows;
@@ -112,14 +114,14 @@ __global__ void __launch_bounds__(256) append_quant_kernel(const char *__restric
         }
         const long long phys = slot / block_size;
         const long long off = slot - phys * block_size;
-        const long long dst_row = (phys * num_kv_heads + h) * block_size + off;
-        uint8_t *codes = (is_v ? v_codes : k_codes) + dst_row * D + lane * E;
+        uint8_t *page = (is_v ? v_pages : k_pages) + (phys * num_kv_heads + h) * page_bytes;
+        uint8_t *codes = page + off * D + lane * E;
         if (E == 4)
             *reinterpret_cast<uint32_t *>(codes) = word;
         else
             *reinterpret_cast<uint16_t *>(codes) = static_cast<uint16_t>(word);
         if (lane == 0)
-            (is_v ? v_scale : k_scale)[dst_row] = s;
+            reinterpret_cast<float *>(page + static_cast<long long>(block_size) * D)[off] = s;
     }
 }
 
@@ -239,10 +241,9 @@ cudaError_t launch_append(const void *k, const void *v, const int64_t *slots, vo
     return cudaGetLastError();
 }
 
-cudaError_t launch_append_quant(const void *k, const void *v, const int64_t *slots, void *k_codes, void *v_codes,
-                                float *k_scale, float *v_scale, int num_tokens, int num_kv_heads, int head_dim,
-                                int in_dtype, int cache_dtype, int block_size, int num_blocks, uint32_t *err,
-                                int num_sms, cudaStream_t stream) {
+cudaError_t launch_append_quant(const void *k, const void *v, const int64_t *slots, void *k_pages, void *v_pages,
+                                int num_tokens, int num_kv_heads, int head_dim, int in_dtype, int cache_dtype,
+                                int block_size, int num_blocks, uint32_t *err, int num_sms, cudaStream_t stream) {
     const long long warps = 2LL * num_tokens * num_kv_heads;
     long long blocks = (warps + 7) / 8;
     const long long cap = static_cast<long long>(num_sms) * 8;
@@ -251,11 +252,10 @@ cudaError_t launch_append_quant(const void *k, const void *v, const int64_t *slo
     if (blocks < 1)
         blocks = 1;
     const long long pool_slots = static_cast<long long>(num_blocks) * block_size;
-#define PA_APPEND_Q(F, D)                                                                                       \
-    append_quant_kernel<F, D><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(                               \
-        static_cast<const char *>(k), static_cast<const char *>(v), slots, static_cast<uint8_t *>(k_codes),     \
-        static_cast<uint8_t *>(v_codes), k_scale, v_scale, num_tokens, num_kv_heads, in_dtype, block_size,     \
-        pool_slots, err)
+#define PA_APPEND_Q(F, D)                                                                                      \
+    append_quant_kernel<F, D><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(                              \
+        static_cast<const char *>(k), static_cast<const char *>(v), slots, static_cast<uint8_t *>(k_pages),    \
+        static_cast<uint8_t *>(v_pages), num_tokens, num_kv_heads, in_dtype, block_size, pool_slots, err)
     if (cache_dtype == PA_I8)
         head_dim == 128 ? PA_APPEND_Q(kFmtI8, 128) : PA_APPEND_Q(kFmtI8, 64);
     else

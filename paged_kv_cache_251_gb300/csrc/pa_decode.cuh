@@ -59,10 +59,8 @@ struct DecodeParams {
     float scale_log2;  // scale * log2(e): scores are kept in base-2 units
     const int32_t *start_tok;  // per-sequence first attended token (nullable)
     int force_partial;         // 1: always write partials, even for one partition
-    // 8-bit caches only: row scales [num_blocks][H_kv][block_size] and the
-    // element type of q (the caches hold codes)
-    const float *k_scale;
-    const float *v_scale;
+    // 8-bit caches only: the element type of q (the caches hold pages of
+    // codes and row scales)
     int q_dtype;
 };
 

@@ -290,8 +290,6 @@ extern "C" pa_status pa_decode_shared_prefix(void *out, const void *q, const voi
     base.stages = 0;
     base.scale_log2 = scale * 1.4426950408889634f;
     base.force_partial = 1;
-    base.k_scale = nullptr;
-    base.v_scale = nullptr;
     base.q_dtype = dtype;
 
     // 2) the shared prefix, once per group: one grouped "sequence" per group

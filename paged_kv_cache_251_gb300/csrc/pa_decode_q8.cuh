@@ -5,9 +5,9 @@
 //
 // Same item structure as the 16-bit general kernel (pa_decode.cuh): items are
 // (sequence, kv head, context partition); a producer warp prefetches the
-// item's block-table slice and streams, per block, four 1-D bulk copies into a
-// stage — K codes, V codes (block_size x head_dim bytes each) and the two rows
-// of scales (block_size floats each) — guarded by full/empty mbarriers.
+// item's block-table slice and streams, per block, two 1-D bulk copies into a
+// stage — the K page and the V page (codes and row scales, pa_quant.cuh) —
+// guarded by full/empty mbarriers.
 //
 // The cached value is code * scale ("KV Cache与长上下文管理", KV-cache
 // quantisation; read as per-row scales), so with the codes c_t, c'_t and the
@@ -37,9 +37,9 @@ template <int D, int G> struct Q8Cfg {
     static_assert(kLpr >= 1 && kLpr <= 32 && 32 % kLpr == 0, "a row must map onto whole lanes of a warp");
 };
 
-// Stage = [K codes][V codes][K scales][V scales].
+// Stage = [K page][V page].
 __host__ __device__ inline uint32_t q8_stage_bytes(int block_size, int D) {
-    return static_cast<uint32_t>(block_size) * (2 * D + 8);
+    return 2u * static_cast<uint32_t>(q8_page_bytes(block_size, D));
 }
 
 __host__ __device__ inline SmemLayout q8_smem_layout(int S, int block_size, int G, int D) {
@@ -53,8 +53,7 @@ __device__ inline void q8_producer(const DecodeParams &p, char *smem, const Smem
     const int lane = threadIdx.x & 31;
     const int S = p.stages;
     const int bs = p.block_size;
-    const uint32_t tile = static_cast<uint32_t>(bs) * C::kRow;
-    const uint32_t srow = static_cast<uint32_t>(bs) * 4;
+    const uint32_t page = static_cast<uint32_t>(q8_page_bytes(bs, D));
     const uint32_t stage_bytes = q8_stage_bytes(bs, D);
     const uint32_t qrow = static_cast<uint32_t>(D) * (p.q_dtype == PA_F32 ? 4 : 2);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.full);
@@ -67,8 +66,6 @@ __device__ inline void q8_producer(const DecodeParams &p, char *smem, const Smem
     char *stage_buf = smem + L.stages;
     const char *kc = static_cast<const char *>(p.k_cache);
     const char *vc = static_cast<const char *>(p.v_cache);
-    const char *ksc = reinterpret_cast<const char *>(p.k_scale);
-    const char *vsc = reinterpret_cast<const char *>(p.v_scale);
     const char *qg = static_cast<const char *>(p.q);
     const uint64_t policy = policy_evict_first();
 
@@ -181,12 +178,10 @@ __device__ inline void q8_producer(const DecodeParams &p, char *smem, const Smem
                                  qg + (static_cast<long long>(s) * p.num_heads + kvh * G) * qrow, G * qrow,
                                  &full[stage]);
                     if (pb >= 0) {
-                        const long long tix = static_cast<long long>(pb) * p.num_kv_heads + kvh;
+                        const long long pix = static_cast<long long>(pb) * p.num_kv_heads + kvh;
                         char *dst = stage_buf + static_cast<size_t>(stage) * stage_bytes;
-                        bulk_g2s_hint(dst, kc + tix * tile, tile, &full[stage], policy);
-                        bulk_g2s_hint(dst + tile, vc + tix * tile, tile, &full[stage], policy);
-                        bulk_g2s_hint(dst + 2 * tile, ksc + tix * srow, srow, &full[stage], policy);
-                        bulk_g2s_hint(dst + 2 * tile + srow, vsc + tix * srow, srow, &full[stage], policy);
+                        bulk_g2s_hint(dst, kc + pix * page, page, &full[stage], policy);
+                        bulk_g2s_hint(dst + page, vc + pix * page, page, &full[stage], policy);
                     }
                 } else {
                     mbar_arrive(&full[stage]);
@@ -234,7 +229,7 @@ __device__ inline void q8_consumer(const DecodeParams &p, char *smem, const Smem
     const int li = lane % C::kLpr;  // 8-code chunk of the row
     const int S = p.stages;
     const int bs = p.block_size;
-    const uint32_t tile = static_cast<uint32_t>(bs) * C::kRow;
+    const uint32_t page = static_cast<uint32_t>(q8_page_bytes(bs, D));
     const uint32_t stage_bytes = q8_stage_bytes(bs, D);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.full);
     uint64_t *empty = reinterpret_cast<uint64_t *>(smem + L.empty);
@@ -285,9 +280,9 @@ __device__ inline void q8_consumer(const DecodeParams &p, char *smem, const Smem
         }
         if (mt.flags & kValid) {
             const char *kb = stage_buf + static_cast<size_t>(stage) * stage_bytes;
-            const char *vb = kb + tile;
-            const float *ks = reinterpret_cast<const float *>(kb + 2 * tile);
-            const float *vs = ks + bs;
+            const char *vb = kb + page;
+            const float *ks = reinterpret_cast<const float *>(kb + bs * C::kRow);  // the pages' scale rows
+            const float *vs = reinterpret_cast<const float *>(vb + bs * C::kRow);
             for (int base = warp * C::kTpp; base < mt.hi; base += kConsumerWarps * C::kTpp) {
                 const int r = base + gi;
                 const bool act = r >= mt.lo && r < mt.hi;

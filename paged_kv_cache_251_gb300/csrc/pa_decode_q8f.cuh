@@ -8,11 +8,12 @@
 // c_t, c'_t and row scales sk_t, sv_t,
 //   x_t = scale * sk_t * <q, c_t>,  out = sum_t e^(x_t - m) sv_t c'_t / sum_t e^(x_t - m).
 //
-// Data path: per (block, kv head) tile one 3-D TMA copy of the K codes and
-// one of the V codes (block_size rows x 128 bytes, 128-byte swizzle) and two
-// 1-D bulk copies of the row scales, into a ring of stages owned round-robin
-// by the 4 consumer warps.  Items (sequence, kv head, partition) flow through
-// a 4-slot ring; each item's G query rows ride on its item barrier.
+// Data path: per (block, kv head) one 1-D bulk copy of the K page and one of
+// the V page (block_size code rows of 128 bytes, then a row of fp32 scales:
+// pa_quant.cuh) into a ring of stages owned round-robin by the 4 consumer
+// warps (stage t belongs to warp t % 4; the ring length is a multiple of 4).
+// Items (sequence, kv head, partition) flow through a 4-slot ring; each
+// item's G query rows ride on its item barrier.
 //
 // Consumers: a warp is G head groups of W = 32 / G lanes; each lane serves one
 // query head through the whole item (its own running max, denominator and
@@ -34,13 +35,14 @@
 //      a dimension in one instruction; the int32 sums join the fp32
 //      accumulator once per block.
 //      E4M3: codes widened to fp32, fp32 FMA with the fp32 weight.
-//  Shared-memory offsets (the 128-byte swizzle included) are per-lane
-//  constants, stage indices advance without division.
+//  Pages land unswizzled: in QK the lanes of one token row read its chunks in
+//  an order rotated by the token index (their query pairs are stored rotated
+//  the same way), so each shared load spreads over all 32 banks; in PV all
+//  lanes read one row.  Shared-memory offsets are per-lane constants, stage
+//  indices advance without division.
 // Every wait is bounded (PA_DEVERR_TIMEOUT); table entries outside the pool
 // are never dereferenced (PA_DEVERR_BAD_BLOCK).
 #pragma once
-
-#include <cuda.h>  // CUtensorMap (type only)
 
 #include "pa_decode.cuh"
 #include "pa_quant.cuh"
@@ -72,13 +74,13 @@ template <int G, int BS> struct Q8fCfg {
     static constexpr int kCpl = 8 / kP;                                 // 16-byte code chunks per QK lane
     static constexpr int kQp = 64 / kP;                                 // packed query pairs per lane
     static constexpr int kDG = 4 * G;                                   // PV dims per lane
-    static constexpr int kTile = BS * D;                                // bytes of one code tile
+    static constexpr int kPage = q8_page_bytes(BS, D);                  // bytes of one page
     static constexpr int kQRow = D * 4;                                 // query row slot (fp32 at most)
     static_assert(kTpr % 8 == 0 && kP >= 1 && kCpl >= 1 && BS % kTpr == 0, "lane mapping");
 };
 
 struct Q8fLayout {
-    uint32_t full, empty, ifull, iempty, mfull, mempty, valid, items, table, qbuf, mscr, mml, scales, stages, total;
+    uint32_t full, empty, ifull, iempty, mfull, mempty, valid, items, table, qbuf, mscr, mml, stages, total;
 };
 
 __host__ __device__ inline Q8fLayout q8f_smem_layout(int S, int BS, int G) {
@@ -108,32 +110,16 @@ __host__ __device__ inline Q8fLayout q8f_smem_layout(int S, int BS, int G) {
     off = L.mscr + 2 * kQ8fWarps * G * kQ8fD * 4;
     L.mml = off;
     off += 2 * kQ8fWarps * G * 2 * 4;
-    L.scales = align_up(off, 16);
-    off = L.scales + S * 2 * BS * 4;
-    L.stages = align_up(off, 1024);  // the 128-byte swizzle pattern repeats every 1024 bytes
-    off = L.stages + S * 2 * BS * kQ8fD;
-    L.total = off + 1024;            // slack to align the dynamic shared memory base
+    L.stages = align_up(off, 128);
+    off = L.stages + S * 2 * q8_page_bytes(BS, kQ8fD);
+    L.total = off + 128;  // slack to align the dynamic shared memory base
     return L;
-}
-
-// One (block, head) code tile through the 3-D view [tile][row][128 bytes].
-__device__ inline void tma_load_3d(void *dst, const CUtensorMap *map, int z, uint64_t *bar, uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint "
-        "[%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_addr(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(0), "r"(z), "r"(smem_addr(bar)), "l"(policy)
-        : "memory");
 }
 
 __device__ inline float q8f_exp2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
-}
-
-// Byte offset of (row r, 16-byte chunk c) inside a 128-byte-swizzled tile of 128-byte rows.
-__device__ inline uint32_t q8f_swz(int r, int c) {
-    return static_cast<uint32_t>(r * 128 + ((c ^ (r & 7)) << 4));
 }
 
 __device__ inline float f16_bits_to_float(uint32_t h) { return __half2float(__ushort_as_half(static_cast<uint16_t>(h))); }
@@ -200,8 +186,7 @@ template <int G> __device__ inline void lds_pv(uint32_t a, uint32_t *w) {
 // ---------------------------------------------------------------------------
 
 template <int G, int BS>
-__device__ inline void q8f_producer(const DecodeParams &p, const CUtensorMap *tmk, const CUtensorMap *tmv, char *smem,
-                                    const Q8fLayout &L) {
+__device__ inline void q8f_producer(const DecodeParams &p, char *smem, const Q8fLayout &L) {
     using C = Q8fCfg<G, BS>;
     const int lane = threadIdx.x & 31;
     const int S = p.stages;
@@ -213,15 +198,12 @@ __device__ inline void q8f_producer(const DecodeParams &p, const CUtensorMap *tm
     Q8fItem *items = reinterpret_cast<Q8fItem *>(smem + L.items);
     int32_t *tbl = reinterpret_cast<int32_t *>(smem + L.table);
     char *qbuf = smem + L.qbuf;
-    float *scales = reinterpret_cast<float *>(smem + L.scales);
     char *stage_buf = smem + L.stages;
     const char *qg = static_cast<const char *>(p.q);
+    const char *kc = static_cast<const char *>(p.k_cache);
+    const char *vc = static_cast<const char *>(p.v_cache);
     const uint32_t qrow = kQ8fD * (p.q_dtype == PA_F32 ? 4 : 2);
     const uint64_t policy = policy_evict_first();
-    if (lane == 0) {
-        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmk)) : "memory");
-        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmv)) : "memory");
-    }
 
     int chunk_base = 0;
     long long chunk_prefix = 0;
@@ -338,14 +320,11 @@ __device__ inline void q8f_producer(const DecodeParams &p, const CUtensorMap *tm
                 if (pb >= 0 && Q8F_OK(stage >= 0 && stage < S, 0) &&
                     Q8F_OK(static_cast<long long>(pb) * p.num_kv_heads + kvh <
                                static_cast<long long>(p.num_blocks) * p.num_kv_heads, 1)) {
-                    mbar_arrive_expect_tx(&full[stage], 2 * C::kTile + 2 * BS * 4);
-                    char *dk = stage_buf + static_cast<size_t>(stage) * 2 * C::kTile;
+                    mbar_arrive_expect_tx(&full[stage], 2 * C::kPage);
+                    char *dk = stage_buf + static_cast<size_t>(stage) * 2 * C::kPage;
                     const long long z = static_cast<long long>(pb) * p.num_kv_heads + kvh;
-                    tma_load_3d(dk, tmk, static_cast<int>(z), &full[stage], policy);
-                    tma_load_3d(dk + C::kTile, tmv, static_cast<int>(z), &full[stage], policy);
-                    float *sc = scales + stage * 2 * BS;
-                    bulk_g2s_hint(sc, p.k_scale + z * BS, BS * 4, &full[stage], policy);
-                    bulk_g2s_hint(sc + BS, p.v_scale + z * BS, BS * 4, &full[stage], policy);
+                    bulk_g2s_hint(dk, kc + z * C::kPage, C::kPage, &full[stage], policy);
+                    bulk_g2s_hint(dk + C::kPage, vc + z * C::kPage, C::kPage, &full[stage], policy);
                 } else {
                     mbar_arrive(&full[stage]);
                 }
@@ -392,23 +371,16 @@ __device__ inline void q8f_consumer(const DecodeParams &p, char *smem, const Q8f
     float *mscr = reinterpret_cast<float *>(smem + L.mscr);  // [2][warps][G][D]
     float *mml = reinterpret_cast<float *>(smem + L.mml);    // [2][warps][G][2]
     const uint32_t stages_a = smem_addr(smem + L.stages);
-    const uint32_t scales_a = smem_addr(smem + L.scales);
     const int qelt = p.q_dtype == PA_F32 ? 4 : 2;
 
-    // per-lane offsets inside a tile: QK chunks of row `tok` (every round's
-    // rows share tok & 7, since kTpr is a multiple of 8), PV dims of a row r
-    // by r & 7
+    // per-lane offsets inside a page: QK chunk i of row `tok` is the lane's
+    // chunk (i + tok) mod kCpl (the rotation spreads a warp's loads over all
+    // banks); PV reads this lane's dims of a row
     uint32_t qk_off[kCpl];
 #pragma unroll
     for (int i = 0; i < kCpl; ++i)
-        qk_off[i] = static_cast<uint32_t>(tok * 128 + (((part * kCpl + i) ^ (tok & 7)) << 4));
-    uint32_t pv_off[8];
-    {
-        const int byte = wl * kDG;  // first byte of this lane's dims in a row
-#pragma unroll
-        for (int k7 = 0; k7 < 8; ++k7)
-            pv_off[k7] = static_cast<uint32_t>((((byte >> 4) ^ k7) << 4) + (byte & 15));
-    }
+        qk_off[i] = static_cast<uint32_t>(tok * 128 + (part * kCpl + (i + tok) % kCpl) * 16);
+    const uint32_t pv_off = static_cast<uint32_t>(wl * kDG);
 
     uint32_t qp[kQp];  // query pairs of this lane's QK dims: int16x2 (INT8) or f16x2 (E4M3)
     float cq = 0.f;    // score factor (query scale * scale * log2 e)
@@ -442,7 +414,8 @@ __device__ inline void q8f_consumer(const DecodeParams &p, char *smem, const Q8f
                 cq = amax * (1.f / 32767.f) * p.scale_log2;
 #pragma unroll
                 for (int i = 0; i < kQp; ++i) {
-                    const int j = part * (kQ8fD / kP) + 2 * i;
+                    // pair i: chunk i / 8 of the rotated order, dims 2 (i % 8), +1 of that chunk
+                    const int j = part * (kQ8fD / kP) + ((i / 8 + tok) % kCpl) * 16 + 2 * (i % 8);
                     int a = __float2int_rn(load_elt(qr, p.q_dtype, j) * inv);
                     int b = __float2int_rn(load_elt(qr, p.q_dtype, j + 1) * inv);
                     a = max(-32767, min(32767, a));
@@ -456,7 +429,7 @@ __device__ inline void q8f_consumer(const DecodeParams &p, char *smem, const Q8f
                 cq = ldexpf(p.scale_log2, -e2);
 #pragma unroll
                 for (int i = 0; i < kQp; ++i) {
-                    const int j = part * (kQ8fD / kP) + 2 * i;
+                    const int j = part * (kQ8fD / kP) + ((i / 8 + tok) % kCpl) * 16 + 2 * (i % 8);
                     const __half2 h = __floats2half2_rn(load_elt(qr, p.q_dtype, j) * up,
                                                         load_elt(qr, p.q_dtype, j + 1) * up);
                     qp[i] = *reinterpret_cast<const uint32_t *>(&h);
@@ -483,10 +456,10 @@ __device__ inline void q8f_consumer(const DecodeParams &p, char *smem, const Q8f
                 break;
             }
             if (valid[stage] && Q8F_OK(stage >= 0 && stage < S, 3)) {
-                const uint32_t kt = stages_a + static_cast<uint32_t>(stage) * 2 * C::kTile;
-                const uint32_t vt = kt + C::kTile;
-                const uint32_t sk = scales_a + static_cast<uint32_t>(stage) * 2 * BS * 4;
-                const uint32_t sv = sk + BS * 4;
+                const uint32_t kt = stages_a + static_cast<uint32_t>(stage) * 2 * C::kPage;
+                const uint32_t vt = kt + C::kPage;
+                const uint32_t sk = kt + BS * 128;  // the pages' scale rows
+                const uint32_t sv = vt + BS * 128;
                 const int blk = it.blk_lo + j;
                 const int lo = max(it.tok_lo - blk * BS, 0);
                 const int hi = min(it.tok_hi - blk * BS, BS);
@@ -503,7 +476,7 @@ __device__ inline void q8f_consumer(const DecodeParams &p, char *smem, const Q8f
 #pragma unroll
                         for (int i = 0; i < kCpl; ++i) {
                             const uint32_t qa = rowa + qk_off[i];
-                            const uint4 w = Q8F_OK(qa >= kt && qa + 16 <= kt + C::kTile && (qa & 15) == 0, 4)
+                            const uint4 w = Q8F_OK(qa >= kt && qa + 16 <= kt + BS * 128 && (qa & 15) == 0, 4)
                                                 ? lds128(qa) : make_uint4(0, 0, 0, 0);
                             const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
@@ -593,9 +566,9 @@ __device__ inline void q8f_consumer(const DecodeParams &p, char *smem, const Q8f
                             const int ta = rd * kTpr + tp;  // the pair (ta, ta + 1)
                             const int pp = static_cast<int>(__shfl_sync(0xffffffffu, pk[rd], gbase + tp));
                             uint32_t w0[G], w1[G];
-                            const uint32_t a0 = vt + ta * 128 + pv_off[ta & 7];
-                            const uint32_t a1 = vt + (ta + 1) * 128 + pv_off[(ta + 1) & 7];
-                            if (Q8F_OK(a0 >= vt && a1 + 4 * G <= vt + C::kTile && (a0 & (4 * G - 1)) == 0 &&
+                            const uint32_t a0 = vt + ta * 128 + pv_off;
+                            const uint32_t a1 = vt + (ta + 1) * 128 + pv_off;
+                            if (Q8F_OK(a0 >= vt && a1 + 4 * G <= vt + BS * 128 && (a0 & (4 * G - 1)) == 0 &&
                                            (a1 & (4 * G - 1)) == 0, 5)) {
                                 lds_pv<G>(a0, w0);
                                 lds_pv<G>(a1, w1);
@@ -629,7 +602,7 @@ __device__ inline void q8f_consumer(const DecodeParams &p, char *smem, const Q8f
                             if (ta < lo || ta >= hi)
                                 continue;
                             uint32_t w[G];
-                            lds_pv<G>(vt + ta * 128 + pv_off[ta & 7], w);
+                            lds_pv<G>(vt + ta * 128 + pv_off, w);
 #pragma unroll
                             for (int q4 = 0; q4 < G; ++q4) {
                                 const uint32_t h01 = e4m3x2_to_f16x2(w[q4] & 0xffffu);
@@ -721,11 +694,9 @@ __device__ inline void q8f_consumer(const DecodeParams &p, char *smem, const Q8f
 }
 
 template <int Fmt, int G, int BS>
-__global__ void __launch_bounds__(kQ8fThreads) pa_decode_q8f_kernel(const DecodeParams p,
-                                                                   const __grid_constant__ CUtensorMap tmk,
-                                                                   const __grid_constant__ CUtensorMap tmv) {
-    extern __shared__ __align__(1024) char smem_raw[];
-    char *smem = reinterpret_cast<char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+__global__ void __launch_bounds__(kQ8fThreads) pa_decode_q8f_kernel(const DecodeParams p) {
+    extern __shared__ __align__(128) char smem_raw[];
+    char *smem = reinterpret_cast<char *>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
     const Q8fLayout L = q8f_smem_layout(p.stages, BS, G);
     // Stage t belongs to consumer warp t % 4.  With a stage count that is not a
     // multiple of 4, one stage would pass between warps, and a warp running a
@@ -759,7 +730,7 @@ __global__ void __launch_bounds__(kQ8fThreads) pa_decode_q8f_kernel(const Decode
     }
     __syncthreads();
     if ((threadIdx.x >> 5) == kQ8fWarps)
-        q8f_producer<G, BS>(p, &tmk, &tmv, smem, L);
+        q8f_producer<G, BS>(p, smem, L);
     else
         q8f_consumer<Fmt, G, BS>(p, smem, L);
 }

@@ -42,10 +42,9 @@ cudaError_t launch_append(const void *k, const void *v, const int64_t *slots, vo
                           int num_tokens, int num_kv_heads, int row_bytes, int block_size, int num_blocks,
                           uint32_t *err, int num_sms, cudaStream_t stream);
 
-cudaError_t launch_append_quant(const void *k, const void *v, const int64_t *slots, void *k_codes, void *v_codes,
-                                float *k_scale, float *v_scale, int num_tokens, int num_kv_heads, int head_dim,
-                                int in_dtype, int cache_dtype, int block_size, int num_blocks, uint32_t *err,
-                                int num_sms, cudaStream_t stream);
+cudaError_t launch_append_quant(const void *k, const void *v, const int64_t *slots, void *k_pages, void *v_pages,
+                                int num_tokens, int num_kv_heads, int head_dim, int in_dtype, int cache_dtype,
+                                int block_size, int num_blocks, uint32_t *err, int num_sms, cudaStream_t stream);
 
 cudaError_t launch_copy_blocks(const int64_t *pairs, int num_pairs, void *k_cache, void *v_cache,
                                long long block_bytes, int num_blocks, uint32_t *err, int num_sms,
@@ -60,8 +59,8 @@ cudaError_t launch_swap_blocks(const int64_t *pairs, int num_pairs, const void *
 // stage count is set there).  The partition reduce is the caller's.
 pa_status launch_decode_kernel(DecodeParams &p, int dtype, int head_dim, int G, cudaStream_t cs);
 
-// Same for an 8-bit cache of cache_dtype (PA_I8 / PA_E4M3); p.k_scale,
-// p.v_scale and p.q_dtype must be set.
+// Same for an 8-bit cache of cache_dtype (PA_I8 / PA_E4M3) in pages
+// (pa_quant.cuh); p.q_dtype must be set.
 pa_status launch_decode_q8_kernel(DecodeParams &p, int cache_dtype, int head_dim, int G, cudaStream_t cs);
 
 // Text returned by pa_last_error_detail() on the calling thread.

@@ -13,6 +13,11 @@
 // and a row of zeros stores scale 0 and zero codes.  The cached value is
 // code_j * scale; decode widens codes to fp32 exactly and applies the K scale
 // to each dot product and the V scale to each softmax weight.
+//
+// Pages: the (block, kv head) page of an 8-bit pool holds the block's
+// block_size code rows of head_dim bytes, then ceil(4 * block_size / head_dim)
+// rows that start with the rows' fp32 scales (the rest zero), so one
+// contiguous copy moves a page with its scales.
 #pragma once
 
 #include <cuda_fp16.h>
@@ -24,6 +29,13 @@
 namespace pa {
 
 enum { kFmtI8 = PA_I8, kFmtE4M3 = PA_E4M3 };
+
+__host__ __device__ constexpr int q8_scale_rows(int block_size, int head_dim) {
+    return (4 * block_size + head_dim - 1) / head_dim;
+}
+__host__ __device__ constexpr int q8_page_bytes(int block_size, int head_dim) {
+    return (block_size + q8_scale_rows(block_size, head_dim)) * head_dim;
+}
 
 template <int Fmt> struct Q8;
 

@@ -53,13 +53,15 @@ def _load():
     lib.pa_decode_shared_prefix_workspace_size.restype = SZ
     lib.pa_swap_blocks.argtypes = [P, I, P, P, P, P, I, I, I, I, I, I, P, P]
     lib.pa_swap_blocks.restype = I
-    lib.pa_append_kv_quant.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, P]
+    lib.pa_quant_page_bytes.argtypes = [I, I]
+    lib.pa_quant_page_bytes.restype = SZ
+    lib.pa_append_kv_quant.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, P, P]
     lib.pa_append_kv_quant.restype = I
-    lib.pa_decode_quant.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, F, I, I, I, I, I, I, I, P, SZ, P, P]
+    lib.pa_decode_quant.argtypes = [P, P, P, P, P, P, I, I, I, I, I, F, I, I, I, I, I, I, I, P, SZ, P, P]
     lib.pa_decode_quant.restype = I
-    lib.pa_copy_blocks_quant.argtypes = [P, I, P, P, P, P, I, I, I, I, P, P]
+    lib.pa_copy_blocks_quant.argtypes = [P, I, P, P, I, I, I, I, P, P]
     lib.pa_copy_blocks_quant.restype = I
-    lib.pa_swap_blocks_quant.argtypes = [P, I, P, P, P, P, P, P, P, P, I, I, I, I, I, P, P]
+    lib.pa_swap_blocks_quant.argtypes = [P, I, P, P, P, P, I, I, I, I, I, P, P]
     lib.pa_swap_blocks_quant.restype = I
     lib.pa_status_string.argtypes = [I]
     lib.pa_status_string.restype = ctypes.c_char_p
@@ -257,100 +259,103 @@ def pa_swap_blocks(src_dst_pairs: torch.Tensor, src_k: torch.Tensor, src_v: torc
                                _ptr(err_word), _stream(stream)))
 
 
-def _check_quant_pool(codes: torch.Tensor, scales: torch.Tensor) -> None:
-    if codes.dtype not in CODE_DTYPE:
-        raise TypeError("8-bit code pools must be int8 or float8_e4m3fn tensors")
-    if scales.dtype != torch.float32 or tuple(scales.shape) != tuple(codes.shape[:3]):
-        raise TypeError("scale pools must be float32 [num_blocks, num_kv_heads, block_size]")
+def pa_quant_page_bytes(head_dim: int, block_size: int) -> int:
+    """Bytes of one (block, kv head) page of an 8-bit pool: block_size code rows
+    of head_dim bytes, then the rows holding their fp32 scales."""
+    return int(_lib.pa_quant_page_bytes(head_dim, block_size))
+
+
+def quant_pool_shape(num_blocks: int, num_kv_heads: int, block_size: int, head_dim: int) -> tuple:
+    """Shape of an 8-bit pool tensor: [num_blocks, H_kv, page rows, head_dim]."""
+    return (num_blocks, num_kv_heads, pa_quant_page_bytes(head_dim, block_size) // head_dim, head_dim)
+
+
+def _pool_block_size(pool: torch.Tensor) -> int:
+    if pool.dtype not in CODE_DTYPE or pool.dim() != 4:
+        raise TypeError("8-bit pools are int8 / float8_e4m3fn tensors [num_blocks, H_kv, page rows, head_dim]")
+    rows, d = pool.shape[2], pool.shape[3]
+    for bs in (8, 16, 32):
+        if pa_quant_page_bytes(d, bs) == rows * d:
+            return bs
+    raise ValueError(f"a {rows}-row page at head_dim {d} matches no block size")
 
 
 def pa_append_kv_quant(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor, k_cache: torch.Tensor,
-                       v_cache: torch.Tensor, k_scale: torch.Tensor, v_scale: torch.Tensor,
-                       err_word: torch.Tensor | None = None, stream=None) -> None:
-    """Quantise token i's K/V rows (fp32/fp16/bf16) into the 8-bit pools at
-    slot_mapping[i]: codes into k_cache / v_cache (int8 or float8_e4m3fn),
-    one fp32 scale per row into k_scale / v_scale (see include/pa.h)."""
-    _cuda(k, v, slot_mapping, k_cache, v_cache, k_scale, v_scale, err_word)
+                       v_cache: torch.Tensor, err_word: torch.Tensor | None = None, stream=None) -> None:
+    """Quantise token i's K/V rows (fp32/fp16/bf16) into the 8-bit pages at
+    slot_mapping[i]: codes into the slot's row, the row scale into the page's
+    scale rows (see include/pa.h)."""
+    _cuda(k, v, slot_mapping, k_cache, v_cache, err_word)
     if slot_mapping.dtype != torch.int64:
         raise TypeError("slot_mapping must be int64")
-    _check_quant_pool(k_cache, k_scale)
-    _check_quant_pool(v_cache, v_scale)
-    if k.dtype != v.dtype or k_cache.dtype != v_cache.dtype:
-        raise TypeError("k and v share one dtype, the code pools another")
-    nb, hkv, bs, d = k_cache.shape
+    bs = _pool_block_size(k_cache)
+    if k.dtype != v.dtype or k_cache.dtype != v_cache.dtype or k_cache.shape != v_cache.shape:
+        raise TypeError("k and v share one dtype, the page pools another and one shape")
+    nb, hkv, _, d = k_cache.shape
     _check(_lib.pa_append_kv_quant(_ptr(k), _ptr(v), _ptr(slot_mapping), _ptr(k_cache), _ptr(v_cache),
-                                   _ptr(k_scale), _ptr(v_scale), slot_mapping.numel(), hkv, d, bs, nb,
-                                   DTYPE_CODE[k.dtype], CODE_DTYPE[k_cache.dtype], _ptr(err_word), _stream(stream)))
+                                   slot_mapping.numel(), hkv, d, bs, nb, DTYPE_CODE[k.dtype],
+                                   CODE_DTYPE[k_cache.dtype], _ptr(err_word), _stream(stream)))
 
 
 def pa_decode_quant(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
-                    k_scale: torch.Tensor, v_scale: torch.Tensor, block_tables: torch.Tensor,
-                    context_lens: torch.Tensor, num_kv_heads: int | None = None, scale: float | None = None,
-                    window: int = 0, partition_size: int = 0, workspace: torch.Tensor | None = None,
-                    err_word: torch.Tensor | None = None, stream=None) -> torch.Tensor:
-    """pa_decode over an 8-bit cache: every cached element is code * scale of
-    its row (see include/pa.h)."""
-    _cuda(out, q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens, workspace, err_word)
+                    block_tables: torch.Tensor, context_lens: torch.Tensor, num_kv_heads: int | None = None,
+                    scale: float | None = None, window: int = 0, partition_size: int = 0,
+                    workspace: torch.Tensor | None = None, err_word: torch.Tensor | None = None,
+                    stream=None) -> torch.Tensor:
+    """pa_decode over 8-bit pages: every cached element is code * scale of its
+    row (see include/pa.h)."""
+    _cuda(out, q, k_cache, v_cache, block_tables, context_lens, workspace, err_word)
     N, H, d = q.shape
-    nb, hkv, bs, d2 = k_cache.shape
+    bs = _pool_block_size(k_cache)
+    nb, hkv, _, d2 = k_cache.shape
     if num_kv_heads is None:
         num_kv_heads = hkv
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
         raise TypeError("block_tables and context_lens must be int32")
-    _check_quant_pool(k_cache, k_scale)
-    _check_quant_pool(v_cache, v_scale)
-    if v_cache.dtype != k_cache.dtype:
-        raise TypeError("k_cache and v_cache must share one code dtype")
+    if v_cache.dtype != k_cache.dtype or v_cache.shape != k_cache.shape:
+        raise TypeError("k_cache and v_cache must share one code dtype and shape")
     if workspace is None:
         workspace = workspace_for(q, bs, block_tables.shape[1], window, partition_size)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    _check(_lib.pa_decode_quant(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
-                                _ptr(block_tables), _ptr(context_lens), N, H, num_kv_heads, d, bs, float(scale),
-                                int(window), DTYPE_CODE[q.dtype], CODE_DTYPE[k_cache.dtype],
-                                DTYPE_CODE[out.dtype], block_tables.shape[1], nb, int(partition_size),
-                                _ptr(workspace), ws_bytes, _ptr(err_word), _stream(stream)))
+    _check(_lib.pa_decode_quant(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                                _ptr(context_lens), N, H, num_kv_heads, d, bs, float(scale), int(window),
+                                DTYPE_CODE[q.dtype], CODE_DTYPE[k_cache.dtype], DTYPE_CODE[out.dtype],
+                                block_tables.shape[1], nb, int(partition_size), _ptr(workspace), ws_bytes,
+                                _ptr(err_word), _stream(stream)))
     return out
 
 
 def pa_copy_blocks_quant(src_dst_pairs: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
-                         k_scale: torch.Tensor, v_scale: torch.Tensor, err_word: torch.Tensor | None = None,
-                         stream=None) -> None:
-    """pa_copy_blocks for 8-bit pools: codes and scales of every pair."""
-    _cuda(src_dst_pairs, k_cache, v_cache, k_scale, v_scale, err_word)
+                         err_word: torch.Tensor | None = None, stream=None) -> None:
+    """pa_copy_blocks for 8-bit pools: whole pages (codes and scales)."""
+    _cuda(src_dst_pairs, k_cache, v_cache, err_word)
     if src_dst_pairs.dtype != torch.int64:
         raise TypeError("src_dst_pairs must be int64")
-    _check_quant_pool(k_cache, k_scale)
-    _check_quant_pool(v_cache, v_scale)
-    nb, hkv, bs, d = k_cache.shape
+    bs = _pool_block_size(k_cache)
+    nb, hkv, _, d = k_cache.shape
     _check(_lib.pa_copy_blocks_quant(_ptr(src_dst_pairs), src_dst_pairs.numel() // 2, _ptr(k_cache),
-                                     _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), hkv, d, bs, nb,
-                                     _ptr(err_word), _stream(stream)))
+                                     _ptr(v_cache), hkv, d, bs, nb, _ptr(err_word), _stream(stream)))
 
 
-def pa_swap_blocks_quant(src_dst_pairs: torch.Tensor, src_k: torch.Tensor, src_v: torch.Tensor,
-                         src_k_scale: torch.Tensor, src_v_scale: torch.Tensor, dst_k: torch.Tensor,
-                         dst_v: torch.Tensor, dst_k_scale: torch.Tensor, dst_v_scale: torch.Tensor,
-                         err_word: torch.Tensor | None = None, stream=None) -> None:
-    """pa_swap_blocks for 8-bit pools (codes and scales; CUDA or pinned host tensors)."""
-    ts = (src_dst_pairs, src_k, src_v, src_k_scale, src_v_scale, dst_k, dst_v, dst_k_scale, dst_v_scale)
-    for t in ts:
+def pa_swap_blocks_quant(src_dst_pairs: torch.Tensor, src_k: torch.Tensor, src_v: torch.Tensor, dst_k: torch.Tensor,
+                         dst_v: torch.Tensor, err_word: torch.Tensor | None = None, stream=None) -> None:
+    """pa_swap_blocks for 8-bit pools: whole pages (CUDA or pinned host tensors)."""
+    for t in (src_dst_pairs, src_k, src_v, dst_k, dst_v):
         if not t.is_contiguous() or not (t.is_cuda or t.is_pinned()):
             raise ValueError("pools and pairs must be contiguous CUDA tensors or pinned host tensors")
     if err_word is not None:
         _cuda(err_word)
     if src_dst_pairs.dtype != torch.int64:
         raise TypeError("src_dst_pairs must be int64")
-    for c, sc in ((src_k, src_k_scale), (src_v, src_v_scale), (dst_k, dst_k_scale), (dst_v, dst_v_scale)):
-        _check_quant_pool(c, sc)
-    snb, hkv, bs, d = src_k.shape
-    dnb, hkv2, bs2, d2 = dst_k.shape
-    if (hkv, bs, d) != (hkv2, bs2, d2) or src_k.dtype != dst_k.dtype:
-        raise ValueError("both pools must share the block layout and code dtype")
+    bs = _pool_block_size(src_k)
+    snb, hkv, rows, d = src_k.shape
+    dnb, hkv2, rows2, d2 = dst_k.shape
+    if (hkv, rows, d) != (hkv2, rows2, d2) or src_k.dtype != dst_k.dtype:
+        raise ValueError("both pools must share the page layout and code dtype")
     _check(_lib.pa_swap_blocks_quant(_ptr(src_dst_pairs), src_dst_pairs.numel() // 2, _ptr(src_k), _ptr(src_v),
-                                     _ptr(src_k_scale), _ptr(src_v_scale), _ptr(dst_k), _ptr(dst_v),
-                                     _ptr(dst_k_scale), _ptr(dst_v_scale), snb, dnb, hkv, d, bs, _ptr(err_word),
+                                     _ptr(dst_k), _ptr(dst_v), snb, dnb, hkv, d, bs, _ptr(err_word),
                                      _stream(stream)))
 
 

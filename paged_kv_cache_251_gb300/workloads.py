@@ -280,13 +280,28 @@ def scale_pool(seed: int, stream: int, shape, fmt: str, device="cpu") -> torch.T
     return ((0.5 + u) * base).reshape(tuple(shape))
 
 
+def page_pool(codes: torch.Tensor, scales: torch.Tensor) -> torch.Tensor:
+    """An 8-bit page pool [nb, H_kv, bs + scale_rows, d] holding `codes`
+    [nb, H_kv, bs, d] and the bytes of `scales` float32 [nb, H_kv, bs] in
+    each page's trailing rows (zero padding after them)."""
+    nb, hkv, bs, d = codes.shape
+    sr = (4 * bs + d - 1) // d
+    pool = torch.zeros((nb, hkv, bs + sr, d), dtype=torch.uint8, device=codes.device)
+    pool[:, :, :bs] = codes.view(torch.uint8)
+    tail = pool[:, :, bs:].reshape(nb, hkv, sr * d)
+    tail[:, :, :4 * bs] = scales.contiguous().view(torch.uint8).reshape(nb, hkv, 4 * bs)
+    pool[:, :, bs:] = tail.reshape(nb, hkv, sr, d)
+    return pool.view(codes.dtype)
+
+
 def quant_pools(inp: DecodeInputs, fmt: str, device="cpu"):
-    """Random code and scale pools with the block layout of ``inp``'s caches:
-    (k_codes, v_codes, k_scale, v_scale)."""
+    """Random 8-bit page pools (codes and row scales from code_pool /
+    scale_pool) with the block layout of ``inp``'s caches: (k_pages, v_pages)."""
     s = inp.shape
     shp = (inp.num_blocks, s.num_kv_heads, s.block_size, s.head_dim)
-    return (code_pool(s.seed, _S_KCODE, shp, fmt, device), code_pool(s.seed, _S_VCODE, shp, fmt, device),
-            scale_pool(s.seed, _S_KSCALE, shp[:3], fmt, device), scale_pool(s.seed, _S_VSCALE, shp[:3], fmt, device))
+    kp = page_pool(code_pool(s.seed, _S_KCODE, shp, fmt, device), scale_pool(s.seed, _S_KSCALE, shp[:3], fmt, device))
+    vp = page_pool(code_pool(s.seed, _S_VCODE, shp, fmt, device), scale_pool(s.seed, _S_VSCALE, shp[:3], fmt, device))
+    return kp, vp
 
 
 def window_ring_blocks(shape: Shape, ring_len: int) -> torch.Tensor:

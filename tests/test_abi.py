@@ -107,16 +107,15 @@ def test_cache_ops_host_validation(lib):
 
 
 def _call_decode_quant(lib, **over):
-    a = dict(out=0x1000, q=0x2000, k=0x3000, v=0x4000, ks=0x7000, vs=0x8000, bt=0x5000, cl=0x6000, N=4, H=8,
+    a = dict(out=0x1000, q=0x2000, k=0x3000, v=0x4000, bt=0x5000, cl=0x6000, N=4, H=8,
              Hkv=2, d=128, bs=16, scale=0.088, window=0, dtype=1, cdt=3, out_dtype=0, M=8, nb=64, part=0, ws=0,
              wsb=0, err=0, stream=0)
     a.update(over)
     P, I = ctypes.c_void_p, ctypes.c_int
     f = lib.pa_decode_quant
     f.restype = I
-    f.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, ctypes.c_float, I, I, I, I, I, I, I, P, ctypes.c_size_t,
-                  P, P]
-    return f(a["out"], a["q"], a["k"], a["v"], a["ks"], a["vs"], a["bt"], a["cl"], a["N"], a["H"], a["Hkv"],
+    f.argtypes = [P, P, P, P, P, P, I, I, I, I, I, ctypes.c_float, I, I, I, I, I, I, I, P, ctypes.c_size_t, P, P]
+    return f(a["out"], a["q"], a["k"], a["v"], a["bt"], a["cl"], a["N"], a["H"], a["Hkv"],
              a["d"], a["bs"], a["scale"], a["window"], a["dtype"], a["cdt"], a["out_dtype"], a["M"], a["nb"],
              a["part"], a["ws"], a["wsb"], a["err"], a["stream"])
 
@@ -127,30 +126,42 @@ def test_decode_quant_host_validation(lib):
     assert _call_decode_quant(lib, cdt=1) == INV           # a 16-bit dtype is not a code dtype
     assert _call_decode_quant(lib, cdt=5) == INV
     assert _call_decode_quant(lib, dtype=3) == INV         # q cannot be 8-bit
-    assert _call_decode_quant(lib, ks=0) == INV            # scales required
-    assert _call_decode_quant(lib, vs=0x8004) == INV       # misaligned scale pool
+    assert _call_decode_quant(lib, k=0) == INV
+    assert _call_decode_quant(lib, v=0x4008) == INV        # misaligned page pool
     assert _call_decode_quant(lib, d=96) == UNS
     assert _call_decode_quant(lib, H=12, Hkv=4) == UNS
     assert _call_decode_quant(lib, M=100) == WS
+
+
+def test_quant_page_bytes(lib):
+    f = lib.pa_quant_page_bytes
+    f.restype = ctypes.c_size_t
+    f.argtypes = [ctypes.c_int, ctypes.c_int]
+    # block_size code rows of head_dim bytes + ceil(4 * block_size / head_dim) scale rows
+    assert f(128, 16) == 17 * 128
+    assert f(128, 8) == 9 * 128
+    assert f(128, 32) == 33 * 128
+    assert f(64, 16) == 17 * 64
+    assert f(64, 32) == 34 * 64
+    assert f(96, 16) == 0 and f(128, 12) == 0
 
 
 def test_append_quant_host_validation(lib):
     P, I = ctypes.c_void_p, ctypes.c_int
     f = lib.pa_append_kv_quant
     f.restype = I
-    f.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, P]
-    ok = dict(k=0x1000, v=0x2000, sl=0x3000, kc=0x4000, vc=0x5000, ks=0x6000, vs=0x7000, T=4, Hkv=2, d=128, bs=16,
-              nb=8, dt=1, cdt=4)
+    f.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, P, P]
+    ok = dict(k=0x1000, v=0x2000, sl=0x3000, kc=0x4000, vc=0x5000, T=4, Hkv=2, d=128, bs=16, nb=8, dt=1, cdt=4)
 
     def call(**o):
         a = dict(ok, **o)
-        return f(a["k"], a["v"], a["sl"], a["kc"], a["vc"], a["ks"], a["vs"], a["T"], a["Hkv"], a["d"], a["bs"],
-                 a["nb"], a["dt"], a["cdt"], None, None)
+        return f(a["k"], a["v"], a["sl"], a["kc"], a["vc"], a["T"], a["Hkv"], a["d"], a["bs"], a["nb"], a["dt"],
+                 a["cdt"], None, None)
 
     assert call(T=0) == 0
     assert call(cdt=2) == 1
     assert call(dt=4) == 1
-    assert call(vs=0) == 1
+    assert call(vc=0) == 1
     assert call(sl=0x3004) == 1
     assert call(d=32) == 2
     assert call(bs=4) == 2

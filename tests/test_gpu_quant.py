@@ -1,10 +1,10 @@
 """GPU parity of the 8-bit KV cache (INT8 / E4M3 codes with one fp32 scale per
-cached row) against the oracle, through the C ABI:
-  - quantise-on-append: codes and scales bit-exact, whole pools compared;
-  - decode over 8-bit pools: the attention tolerances of the 16-bit path,
+cached row, held in self-contained pages) against the oracle, through the C ABI:
+  - quantise-on-append: whole page pools compared byte for byte;
+  - decode over 8-bit pages: the attention tolerances of the 16-bit path,
     against the oracle reading every element as code * scale;
-  - block copy and swap of 8-bit pools: bit-exact.
-Decode inputs are random code and scale pools from the seeded generator (no
+  - block copy and swap of page pools: bit-exact.
+Decode inputs are random codes and scales from the seeded generator (no
 quantiser on either side); the append-then-decode test runs the two steps in
 sequence on each side."""
 import math
@@ -27,11 +27,11 @@ def _u8(t):
     return t.view(torch.uint8)
 
 
-def _filled_pools(nb, hkv, bs, d, fmt, seed):
-    """Pools pre-filled with random codes and scales (so untouched slots are checked)."""
+def _filled_pages(nb, hkv, bs, d, fmt, seed):
+    """Page pools pre-filled with random codes and scales (so untouched rows are checked)."""
     shp = (nb, hkv, bs, d)
-    return (wl.code_pool(seed, 1, shp, fmt), wl.code_pool(seed, 2, shp, fmt),
-            wl.scale_pool(seed, 3, shp[:3], fmt), wl.scale_pool(seed, 4, shp[:3], fmt))
+    return (wl.page_pool(wl.code_pool(seed, 1, shp, fmt), wl.scale_pool(seed, 3, shp[:3], fmt)),
+            wl.page_pool(wl.code_pool(seed, 2, shp, fmt), wl.scale_pool(seed, 4, shp[:3], fmt)))
 
 
 def _gpu_append(k, v, slots, pools, err=None):
@@ -43,20 +43,16 @@ def _gpu_append(k, v, slots, pools, err=None):
 
 
 def _assert_pools_equal(got, want):
-    kc, vc, ks, vs = got
-    okc, ovc, oks, ovs = want
-    assert torch.equal(_u8(kc), _u8(okc)), "K codes differ"
-    assert torch.equal(_u8(vc), _u8(ovc)), "V codes differ"
-    assert torch.equal(ks.view(torch.int32), oks.view(torch.int32)), "K scales differ"
-    assert torch.equal(vs.view(torch.int32), ovs.view(torch.int32)), "V scales differ"
+    for g, w, name in zip(got, want, ("K", "V")):
+        assert torch.equal(_u8(g), _u8(w)), f"{name} pages differ"
 
 
 @pytest.mark.parametrize("fmt", FMTS)
 @pytest.mark.parametrize("in_dt", ["f16", "bf16", "f32"])
-@pytest.mark.parametrize("bs,d,hkv", [(16, 128, 8), (8, 64, 4), (32, 128, 40)])
+@pytest.mark.parametrize("bs,d,hkv", [(16, 128, 8), (8, 64, 4), (32, 128, 40), (32, 64, 2)])
 def test_append_quant_bit_exact(fmt, in_dt, bs, d, hkv):
     nb, T = 24, 37
-    pools = _filled_pools(nb, hkv, bs, d, fmt, seed=bs + d + hkv)
+    pools = _filled_pages(nb, hkv, bs, d, fmt, seed=bs + d + hkv)
     k = wl.normal_tensor(5, 1, (T, hkv, d), dtype=DT[in_dt])
     v = wl.normal_tensor(5, 2, (T, hkv, d), dtype=DT[in_dt]) * 3
     slots = wl.permutation(6, 1, nb * bs)[:T].clone()
@@ -87,7 +83,7 @@ def test_append_quant_special_rows(fmt, in_dt):
     rows[7] = (torch.arange(d, dtype=torch.float32) % 7 - 3) * 0.5
     k = rows.to(DT[in_dt])
     v = (-rows).to(DT[in_dt])
-    pools = _filled_pools(nb, hkv, bs, d, fmt, seed=77)
+    pools = _filled_pages(nb, hkv, bs, d, fmt, seed=77)
     slots = torch.tensor([0, 5, 16, 17, 33, 48, 63, 2], dtype=torch.int64)
     got = _gpu_append(k, v, slots, pools)
     want = [t.clone() for t in pools]
@@ -98,7 +94,7 @@ def test_append_quant_special_rows(fmt, in_dt):
 @pytest.mark.parametrize("fmt", FMTS)
 def test_append_quant_out_of_range_slot_flagged_and_skipped(fmt):
     hkv, d, bs, nb = 2, 128, 16, 4
-    pools = _filled_pools(nb, hkv, bs, d, fmt, seed=9)
+    pools = _filled_pages(nb, hkv, bs, d, fmt, seed=9)
     k = wl.normal_tensor(7, 1, (2, hkv, d), dtype=torch.float16)
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     got = _gpu_append(k, k, torch.tensor([nb * bs, 1 << 40]), pools, err)
@@ -122,8 +118,8 @@ def _gpu_decode_quant(inp, pools, out_dtype=torch.float32, window=None, partitio
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     bt = (inp.block_tables if block_tables is None else block_tables).cuda().contiguous()
     cl = (inp.context_lens if context_lens is None else context_lens).cuda().contiguous()
-    kc, vc, ks, vs = [t.cuda() for t in pools]
-    pa.pa_decode_quant(out, q, kc, vc, ks, vs, bt, cl, num_kv_heads=s.num_kv_heads,
+    kp, vp = [t.cuda() for t in pools]
+    pa.pa_decode_quant(out, q, kp, vp, bt, cl, num_kv_heads=s.num_kv_heads,
                        scale=1.0 / math.sqrt(s.head_dim), window=s.window if window is None else window,
                        partition_size=partition_size, err_word=err)
     torch.cuda.synchronize()
@@ -132,12 +128,11 @@ def _gpu_decode_quant(inp, pools, out_dtype=torch.float32, window=None, partitio
 
 def _oracle_decode_quant(inp, pools, block_tables=None, context_lens=None, invalid_policy=0, pairs=None):
     s = inp.shape
-    kc, vc, ks, vs = pools
-    return oracle.paged_attention(inp.q, kc, vc, inp.block_tables if block_tables is None else block_tables,
+    kp, vp = pools
+    return oracle.paged_attention(inp.q, kp, vp, inp.block_tables if block_tables is None else block_tables,
                                   inp.context_lens if context_lens is None else context_lens,
                                   num_kv_heads=s.num_kv_heads, scale=1.0 / math.sqrt(s.head_dim),
-                                  window=s.window, k_scale=ks, v_scale=vs, invalid_policy=invalid_policy,
-                                  pairs=pairs, threads=8)
+                                  window=s.window, invalid_policy=invalid_policy, pairs=pairs, threads=8)
 
 
 # (name, N, H, H_kv, d, bs, lens, window, partition) — several tiles and a ragged tail each
@@ -184,9 +179,11 @@ def test_decode_quant_low_precision_output(out_dt):
 def test_decode_quant_zero_scale_rows(fmt):
     """Rows stored with scale 0 (all-zero rows) read as zeros."""
     inp, pools = _quant_case("zeros", 2, 4, 2, 128, 16, [40, 70], 0, torch.float16, fmt, seed=4)
-    kc, vc, ks, vs = pools
+    kc, ks = oracle.unpack_pages(pools[0])
+    vc, vs = oracle.unpack_pages(pools[1])
     ks[inp.block_tables[0, 0].item(), :, :5] = 0.0
     vs[inp.block_tables[1, 2].item(), 1, :] = 0.0
+    pools = (wl.page_pool(kc, ks), wl.page_pool(vc, vs))
     got, err = _gpu_decode_quant(inp, pools)
     assert err == 0
     compare(got, _oracle_decode_quant(inp, pools), torch.float16)
@@ -207,16 +204,15 @@ def test_decode_quant_invalid_table_entries_skipped_and_flagged(fmt):
 @pytest.mark.parametrize("hkv", [8, 2])
 def test_decode_quant_append_then_decode(fmt, hkv):
     """Quantise a whole fp16 pool token by token with pa_append_kv_quant (the
-    pools must equal the oracle's bit for bit), then decode both."""
+    pages must equal the oracle's bit for bit), then decode both."""
     from paged_kv_cache_251_gb300 import pa
     sh = shape("e2e", 3, 8, hkv, 128, 16, torch.float16, seed=12)
     inp = wl.decode_inputs(sh, lens=torch.tensor([300, 1, 517], dtype=torch.int32), room_for_append=False,
                            with_append=False)
     nb, bs = inp.num_blocks, 16
     code_dt = wl.CODE_DTYPES[fmt]
-    shp = (nb, hkv, bs, 128)
-    zeros = [torch.zeros(shp, dtype=torch.uint8).view(code_dt), torch.zeros(shp, dtype=torch.uint8).view(code_dt),
-             torch.zeros(shp[:3]), torch.zeros(shp[:3])]
+    shp = pa.quant_pool_shape(nb, hkv, bs, 128)
+    zeros = [torch.zeros(shp, dtype=torch.uint8).view(code_dt), torch.zeros(shp, dtype=torch.uint8).view(code_dt)]
     # every slot of the pool as one appended token: rows [slot][H_kv][d]
     rows_k = inp.k_cache.permute(0, 2, 1, 3).reshape(nb * bs, hkv, 128).contiguous()
     rows_v = inp.v_cache.permute(0, 2, 1, 3).reshape(nb * bs, hkv, 128).contiguous()
@@ -238,7 +234,7 @@ def test_decode_quant_append_then_decode(fmt, hkv):
 def test_copy_blocks_quant_bit_exact(fmt):
     from paged_kv_cache_251_gb300 import pa
     nb, hkv, bs, d = 64, 8, 16, 128
-    pools = _filled_pools(nb, hkv, bs, d, fmt, seed=21)
+    pools = _filled_pages(nb, hkv, bs, d, fmt, seed=21)
     perm = wl.permutation(9, 1, nb)
     pairs = torch.stack([perm[:20], perm[20:40]], dim=1).contiguous()
     pairs[5, 1] = nb + 3                                   # outside the pool: skipped, flagged
@@ -247,7 +243,6 @@ def test_copy_blocks_quant_bit_exact(fmt):
     pa.pa_copy_blocks_quant(pairs.cuda(), *dev, err_word=err)
     want = [t.clone() for t in pools]
     oracle.copy_blocks(want[0], want[1], pairs)
-    oracle.copy_blocks(want[2], want[3], pairs)
     torch.cuda.synchronize()
     assert err.item() & 4
     _assert_pools_equal([t.cpu() for t in dev], want)
@@ -257,19 +252,17 @@ def test_copy_blocks_quant_bit_exact(fmt):
 def test_swap_quant_to_pinned_host_and_back(fmt):
     from paged_kv_cache_251_gb300 import pa
     nb, hb, hkv, bs, d = 40, 24, 8, 16, 128
-    pools = _filled_pools(nb, hkv, bs, d, fmt, seed=22)
+    pools = _filled_pages(nb, hkv, bs, d, fmt, seed=22)
     dev = [t.cuda() for t in pools]
     code_dt = wl.CODE_DTYPES[fmt]
-    host = [torch.zeros((hb, hkv, bs, d), dtype=torch.uint8).view(code_dt).pin_memory(),
-            torch.zeros((hb, hkv, bs, d), dtype=torch.uint8).view(code_dt).pin_memory(),
-            torch.zeros((hb, hkv, bs)).pin_memory(), torch.zeros((hb, hkv, bs)).pin_memory()]
+    hshape = pa.quant_pool_shape(hb, hkv, bs, d)
+    host = [torch.zeros(hshape, dtype=torch.uint8).view(code_dt).pin_memory() for _ in range(2)]
     want_host = [torch.zeros_like(t) for t in host]
     perm = wl.permutation(12, 1, nb)
     out_pairs = torch.stack([perm[:20], wl.permutation(13, 1, hb)[:20]], 1).contiguous()
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     pa.pa_swap_blocks_quant(out_pairs.cuda(), *dev, *host, err_word=err)
     oracle.swap_blocks(pools[0], pools[1], want_host[0], want_host[1], out_pairs)
-    oracle.swap_blocks(pools[2], pools[3], want_host[2], want_host[3], out_pairs)
     torch.cuda.synchronize()
     assert err.item() == 0
     _assert_pools_equal(host, want_host)
@@ -277,7 +270,6 @@ def test_swap_quant_to_pinned_host_and_back(fmt):
     pa.pa_swap_blocks_quant(in_pairs.cuda(), *host, *dev, err_word=err)
     want = [t.clone() for t in pools]
     oracle.swap_blocks(want_host[0], want_host[1], want[0], want[1], in_pairs)
-    oracle.swap_blocks(want_host[2], want_host[3], want[2], want[3], in_pairs)
     torch.cuda.synchronize()
     assert err.item() == 0
     _assert_pools_equal([t.cpu() for t in dev], want)
@@ -314,7 +306,7 @@ def test_full_size_quant_sampled(name, fmt):
     pairs = _sample_pairs(s.num_seqs, s.num_heads, 48, seed=s.seed)
     cpu_pools = [t.cpu() for t in pools]
     ref = oracle.paged_attention(q.cpu(), cpu_pools[0], cpu_pools[1], inp.block_tables, inp.context_lens,
-                                 num_kv_heads=s.num_kv_heads, scale=1 / math.sqrt(s.head_dim),
-                                 k_scale=cpu_pools[2], v_scale=cpu_pools[3], pairs=pairs, threads=16)
+                                 num_kv_heads=s.num_kv_heads, scale=1 / math.sqrt(s.head_dim), pairs=pairs,
+                                 threads=16)
     got = out.cpu()[pairs[:, 0].long(), pairs[:, 1].long()]
     compare(got, ref, torch.float16)
