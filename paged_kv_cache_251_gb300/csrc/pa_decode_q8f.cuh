@@ -356,8 +356,10 @@ __device__ inline void q8f_consumer(const DecodeParams &p, char *smem, const Q8f
     const int g = lane / kW;         // this lane's query head within the kv head's group
     const int wl = lane % kW;        // lane within the head group
     const int gbase = lane & ~(kW - 1);
-    const int tok = wl % kTpr;       // QK: token of the round
-    const int part = wl / kTpr;      // QK: share of the row
+    // QK lanes: part in the low bits, so each 8-lane phase of a 128-bit shared
+    // load covers 8 distinct 16-byte chunk positions of the rows it reads
+    const int tok = wl / kP;         // QK: token of the round
+    const int part = wl % kP;        // QK: share of the row
     const int S = p.stages;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.full);
     uint64_t *empty = reinterpret_cast<uint64_t *>(smem + L.empty);
@@ -487,7 +489,7 @@ __device__ inline void q8f_consumer(const DecodeParams &p, char *smem, const Q8f
                         }
                         int sum = (a[0] + a[1]) + (a[2] + a[3]);
 #pragma unroll
-                        for (int o = kTpr; o < kW; o <<= 1)
+                        for (int o = 1; o < kP; o <<= 1)
                             sum += __shfl_xor_sync(0xffffffffu, sum, o);
                         x = static_cast<float>(sum);
                     } else {
@@ -504,7 +506,7 @@ __device__ inline void q8f_consumer(const DecodeParams &p, char *smem, const Q8f
                         }
                         x = (xa[0] + xa[1]) + (xa[2] + xa[3]);
 #pragma unroll
-                        for (int o = kTpr; o < kW; o <<= 1)
+                        for (int o = 1; o < kP; o <<= 1)
                             x += __shfl_xor_sync(0xffffffffu, x, o);
                     }
                     const float skr = Q8F_OK(r >= 0 && r < BS, 6) ? ldsf(sk + r * 4) : 0.f;
@@ -517,7 +519,7 @@ __device__ inline void q8f_consumer(const DecodeParams &p, char *smem, const Q8f
                 for (int rd = 1; rd < kR; ++rd)
                     mb = fmaxf(mb, sc[rd]);
 #pragma unroll
-                for (int o = 1; o < kTpr; o <<= 1)
+                for (int o = kP; o < kW; o <<= 1)
                     mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, o));
                 if (mb > m) {
                     const float alpha = q8f_exp2(m - mb);
@@ -544,7 +546,7 @@ __device__ inline void q8f_consumer(const DecodeParams &p, char *smem, const Q8f
                     for (int rd = 1; rd < kR; ++rd)
                         pm = fmaxf(pm, pw[rd]);
 #pragma unroll
-                    for (int o = 1; o < kTpr; o <<= 1)
+                    for (int o = kP; o < kW; o <<= 1)
                         pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, o));
                     const float inv = pm > 0.f ? __fdividef(32767.f, pm) : 0.f;
                     const float ps = pm * (1.f / 32767.f);
@@ -552,7 +554,7 @@ __device__ inline void q8f_consumer(const DecodeParams &p, char *smem, const Q8f
 #pragma unroll
                     for (int rd = 0; rd < kR; ++rd) {
                         const int pi = min(32767, __float2int_rn(pw[rd] * inv));
-                        const int nb_pi = __shfl_xor_sync(0xffffffffu, pi, 1);
+                        const int nb_pi = __shfl_xor_sync(0xffffffffu, pi, kP);  // the next token's lane
                         pk[rd] = (static_cast<uint32_t>(pi) & 0xffffu) | (static_cast<uint32_t>(nb_pi) << 16);
                     }
                     int ai[kDG];
@@ -564,7 +566,7 @@ __device__ inline void q8f_consumer(const DecodeParams &p, char *smem, const Q8f
 #pragma unroll
                         for (int tp = 0; tp < kTpr; tp += 2) {
                             const int ta = rd * kTpr + tp;  // the pair (ta, ta + 1)
-                            const int pp = static_cast<int>(__shfl_sync(0xffffffffu, pk[rd], gbase + tp));
+                            const int pp = static_cast<int>(__shfl_sync(0xffffffffu, pk[rd], gbase + tp * kP));
                             uint32_t w0[G], w1[G];
                             const uint32_t a0 = vt + ta * 128 + pv_off;
                             const uint32_t a1 = vt + (ta + 1) * 128 + pv_off;
@@ -598,7 +600,7 @@ __device__ inline void q8f_consumer(const DecodeParams &p, char *smem, const Q8f
 #pragma unroll
                         for (int u = 0; u < kTpr; ++u) {
                             const int ta = rd * kTpr + u;
-                            const float pu = __shfl_sync(0xffffffffu, pw[rd], gbase + u);
+                            const float pu = __shfl_sync(0xffffffffu, pw[rd], gbase + u * kP);
                             if (ta < lo || ta >= hi)
                                 continue;
                             uint32_t w[G];
@@ -631,7 +633,7 @@ __device__ inline void q8f_consumer(const DecodeParams &p, char *smem, const Q8f
         // ---- merge the 4 warps' states of this item (double-buffered by item parity)
         // l holds this lane's tokens (the parts of a token hold copies): sum over tokens
 #pragma unroll
-        for (int o = 1; o < kTpr; o <<= 1)
+        for (int o = kP; o < kW; o <<= 1)
             l += __shfl_xor_sync(0xffffffffu, l, o);
         const int b = k & 1;
         const uint32_t use = static_cast<uint32_t>(k >> 1) & 1u;
@@ -693,8 +695,14 @@ __device__ inline void q8f_consumer(const DecodeParams &p, char *smem, const Q8f
         atomicOr(p.err, PA_DEVERR_TIMEOUT);
 }
 
+// One query head per kv head: 5 CTAs per SM (20 consumer warps) fit in the
+// register file at <= 80 registers a thread; grouped heads keep the default.
+template <int G> struct Q8fOccupancy {
+    static constexpr int kMinBlocks = G == 1 ? 5 : 1;
+};
+
 template <int Fmt, int G, int BS>
-__global__ void __launch_bounds__(kQ8fThreads) pa_decode_q8f_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(kQ8fThreads, Q8fOccupancy<G>::kMinBlocks) pa_decode_q8f_kernel(const DecodeParams p) {
     extern __shared__ __align__(128) char smem_raw[];
     char *smem = reinterpret_cast<char *>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
     const Q8fLayout L = q8f_smem_layout(p.stages, BS, G);
