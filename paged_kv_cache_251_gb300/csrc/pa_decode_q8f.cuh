@@ -68,15 +68,18 @@ struct Q8fItem {
 template <int G, int BS> struct Q8fCfg {
     static constexpr int D = kQ8fD;
     static constexpr int kW = 32 / G;                                   // lanes per head group
-    static constexpr int kTpr = BS < (kW < 16 ? kW : 16) ? BS : (kW < 16 ? kW : 16);  // tokens per QK round
-    static constexpr int kP = kW / kTpr;                                // lanes per token in QK
+    // lanes per token in QK: a token's 128 codes over 2 lanes (G <= 2 with a
+    // 16-token round, G = 4), 4 lanes at block size 8 (G = 1), 1 lane for
+    // G = 2 at 16 tokens a round
+    static constexpr int kP = G == 4 ? 2 : (G == 2 ? (BS < 16 ? 2 : 1) : (BS < 16 ? 4 : 2));
+    static constexpr int kTpr = kW / kP;                                // tokens per QK round
     static constexpr int kRounds = BS / kTpr;
     static constexpr int kCpl = 8 / kP;                                 // 16-byte code chunks per QK lane
     static constexpr int kQp = 64 / kP;                                 // packed query pairs per lane
     static constexpr int kDG = 4 * G;                                   // PV dims per lane
     static constexpr int kPage = q8_page_bytes(BS, D);                  // bytes of one page
     static constexpr int kQRow = D * 4;                                 // query row slot (fp32 at most)
-    static_assert(kTpr % 8 == 0 && kP >= 1 && kCpl >= 1 && BS % kTpr == 0, "lane mapping");
+    static_assert(kTpr % 2 == 0 && kP >= 1 && kCpl >= 1 && BS % kTpr == 0, "lane mapping");
 };
 
 struct Q8fLayout {
@@ -169,6 +172,35 @@ __device__ inline uint32_t lds32(uint32_t a) {
     return r;
 }
 __device__ inline float ldsf(uint32_t a) { return __uint_as_float(lds32(a)); }
+
+// Query elements j .. j + 15 (j a multiple of 16) of a row held in shared
+// memory as fp32, fp16 or bf16, widened to fp32 (16-byte loads).
+__device__ inline void load_q16(const char *qr, int dtype, int j, float *f) {
+    if (dtype == PA_F32) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const uint4 v = ld_shared_v4(qr + (j + 4 * k) * 4);
+            f[4 * k] = __uint_as_float(v.x), f[4 * k + 1] = __uint_as_float(v.y);
+            f[4 * k + 2] = __uint_as_float(v.z), f[4 * k + 3] = __uint_as_float(v.w);
+        }
+        return;
+    }
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        const uint4 v = ld_shared_v4(qr + (j + 8 * k) * 2);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            if (dtype == PA_F16) {
+                const float2 h = __half22float2(*reinterpret_cast<const __half2 *>(&w[u]));
+                f[8 * k + 2 * u] = h.x, f[8 * k + 2 * u + 1] = h.y;
+            } else {
+                f[8 * k + 2 * u] = __uint_as_float(w[u] << 16);
+                f[8 * k + 2 * u + 1] = __uint_as_float(w[u] & 0xffff0000u);
+            }
+        }
+    }
+}
 
 // The G words (4 codes each) of this lane's PV dims in one token row.
 template <int G> __device__ inline void lds_pv(uint32_t a, uint32_t *w) {
@@ -400,41 +432,51 @@ __device__ inline void q8f_consumer(const DecodeParams &p, char *smem, const Q8f
             const char *qr = qbuf + slot * G * C::kQRow + g * kQ8fD * qelt;
             (void)Q8F_OK(slot >= 0 && slot < kQ8fItemSlots && it.s >= 0 && it.s < p.num_seqs &&
                              it.part >= 0 && it.part < p.max_parts, 9);
+            // the row's largest magnitude: this lane's QK dims, then over the
+            // parts of its token (they cover the row once)
             float amax = 0.f;
 #pragma unroll
-            for (int e = 0; e < kDG; ++e)
-                amax = fmaxf(amax, fabsf(load_elt(qr, p.q_dtype, wl * kDG + e)));
+            for (int c = 0; c < kCpl; ++c) {
+                float f[16];
+                load_q16(qr, p.q_dtype, part * (kQ8fD / kP) + c * 16, f);
 #pragma unroll
-            for (int o = 1; o < kW; o <<= 1)
+                for (int e = 0; e < 16; ++e)
+                    amax = fmaxf(amax, fabsf(f[e]));
+            }
+#pragma unroll
+            for (int o = 1; o < kP; o <<= 1)
                 amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
             // a row whose largest element is below 1e-30 is read as zero
             if (!(amax > 1e-30f))
                 amax = 0.f;
+            // query pairs in the rotated chunk order: pair 8 i + u holds dims
+            // 2u, 2u + 1 of the lane's chunk (i + tok) mod kCpl
+            float inv, up = 1.f;
             if (kI8) {
                 // int16 query: q ~ sq * qi, sq = max|q| / 32767
-                const float inv = amax > 0.f ? 32767.f / amax : 0.f;
+                inv = amax > 0.f ? 32767.f / amax : 0.f;
                 cq = amax * (1.f / 32767.f) * p.scale_log2;
-#pragma unroll
-                for (int i = 0; i < kQp; ++i) {
-                    // pair i: chunk i / 8 of the rotated order, dims 2 (i % 8), +1 of that chunk
-                    const int j = part * (kQ8fD / kP) + ((i / 8 + tok) % kCpl) * 16 + 2 * (i % 8);
-                    int a = __float2int_rn(load_elt(qr, p.q_dtype, j) * inv);
-                    int b = __float2int_rn(load_elt(qr, p.q_dtype, j + 1) * inv);
-                    a = max(-32767, min(32767, a));
-                    b = max(-32767, min(32767, b));
-                    qp[i] = (static_cast<uint32_t>(a) & 0xffffu) | (static_cast<uint32_t>(b) << 16);
-                }
             } else {
                 // fp16 query scaled by 2^e so that max |q| * 2^e lies in [2^14, 2^15)
                 const int e2 = amax > 0.f ? min(126, 14 - ilogbf(amax)) : 0;
-                const float up = ldexpf(1.f, e2);
+                up = ldexpf(1.f, e2);
                 cq = ldexpf(p.scale_log2, -e2);
+                inv = 0.f;
+            }
 #pragma unroll
-                for (int i = 0; i < kQp; ++i) {
-                    const int j = part * (kQ8fD / kP) + ((i / 8 + tok) % kCpl) * 16 + 2 * (i % 8);
-                    const __half2 h = __floats2half2_rn(load_elt(qr, p.q_dtype, j) * up,
-                                                        load_elt(qr, p.q_dtype, j + 1) * up);
-                    qp[i] = *reinterpret_cast<const uint32_t *>(&h);
+            for (int i = 0; i < kCpl; ++i) {
+                float f[16];
+                load_q16(qr, p.q_dtype, part * (kQ8fD / kP) + ((i + tok) % kCpl) * 16, f);
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    if (kI8) {
+                        const int a = max(-32767, min(32767, __float2int_rn(f[2 * u] * inv)));
+                        const int b = max(-32767, min(32767, __float2int_rn(f[2 * u + 1] * inv)));
+                        qp[i * 8 + u] = (static_cast<uint32_t>(a) & 0xffffu) | (static_cast<uint32_t>(b) << 16);
+                    } else {
+                        const __half2 h = __floats2half2_rn(f[2 * u] * up, f[2 * u + 1] * up);
+                        qp[i * 8 + u] = *reinterpret_cast<const uint32_t *>(&h);
+                    }
                 }
             }
         }
@@ -695,10 +737,10 @@ __device__ inline void q8f_consumer(const DecodeParams &p, char *smem, const Q8f
         atomicOr(p.err, PA_DEVERR_TIMEOUT);
 }
 
-// One query head per kv head: 5 CTAs per SM (20 consumer warps) fit in the
-// register file at <= 80 registers a thread; grouped heads keep the default.
+// CTAs per SM the register budget is set for: 5 for one query head per kv
+// head (20 consumer warps, <= 72 registers a thread), 3 for grouped heads.
 template <int G> struct Q8fOccupancy {
-    static constexpr int kMinBlocks = G == 1 ? 5 : 1;
+    static constexpr int kMinBlocks = G == 1 ? 5 : 3;
 };
 
 template <int Fmt, int G, int BS>
