@@ -325,14 +325,13 @@ pa_status launch_decode_q8_kernel(DecodeParams &p, int cache_dtype, int head_dim
                                                : decode_q8f_kernel_e4m3(G, p.block_size);
         if (!ffn)
             return fail(PA_ERR_UNSUPPORTED, "no 8-bit-cache decode kernel for this group / block size");
-        // stages are owned round-robin by the consumer warps: a multiple of
-        // their count keeps each stage with one warp (no phase aliasing)
-        const int stage = 2 * q8_page_bytes(p.block_size, kQ8fD);
+        // a stage holds the K and V pages of 4 kv heads; every consumer warp
+        // reads every stage
+        const int stage = 2 * kQ8fWarps * q8_page_bytes(p.block_size, kQ8fD);
         int S = kQ8fStageBudget / stage;
-        S -= S % kQ8fWarps;
-        S = S < kQ8fWarps ? kQ8fWarps : (S > 16 ? 16 : S);
+        S = S < 2 ? 2 : (S > 8 ? 8 : S);
         p.stages = S;
-        const size_t smem = q8f_smem_layout(S, p.block_size, G).total;
+        const size_t smem = q8f_smem_layout(S, p.block_size, G, kQ8fD * (p.q_dtype == PA_F32 ? 4 : 2)).total;
         int dev = 0, sms = 0, per_sm = 0;
         cudaError_t e = device_sms(&dev, &sms);
         if (e != cudaSuccess)
@@ -342,7 +341,8 @@ pa_status launch_decode_q8_kernel(DecodeParams &p, int cache_dtype, int head_dim
             return cuda_fail(e, "decode kernel set-up");
         if (per_sm < 1)
             return fail(PA_ERR_UNSUPPORTED, "decode kernel does not fit on an SM");
-        const long long items_max = static_cast<long long>(p.num_seqs) * p.num_kv_heads * p.max_parts;
+        const long long items_max = static_cast<long long>(p.num_seqs) *
+                                    ((p.num_kv_heads + kQ8fWarps - 1) / kQ8fWarps) * p.max_parts;
         long long grid = static_cast<long long>(sms) * per_sm;
         if (grid > items_max)
             grid = items_max;

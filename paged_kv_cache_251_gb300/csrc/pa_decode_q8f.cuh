@@ -1,26 +1,30 @@
 // Paged decode attention over an 8-bit KV cache, head_dim 128, query groups
-// G in {1, 2, 4}: the persistent, warp-specialised kernel fed by TMA tensor
-// copies (the 16-bit MHA kernel's data path, pa_decode_mha.cuh), with
-// arithmetic chosen for 1-byte elements.
+// G in {1, 2, 4}: the persistent, warp-specialised kernel for 8-bit pages.
 //
 // What it computes is pa_decode's attention with every cached element read as
 // code * scale of its row (pa_quant.cuh): for token t of a sequence with codes
 // c_t, c'_t and row scales sk_t, sv_t,
 //   x_t = scale * sk_t * <q, c_t>,  out = sum_t e^(x_t - m) sv_t c'_t / sum_t e^(x_t - m).
 //
-// Data path: per (block, kv head) one 1-D bulk copy of the K page and one of
-// the V page (block_size code rows of 128 bytes, then a row of fp32 scales:
-// pa_quant.cuh) into a ring of stages owned round-robin by the 4 consumer
-// warps (stage t belongs to warp t % 4; the ring length is a multiple of 4).
-// Items (sequence, kv head, partition) flow through a 4-slot ring; each
-// item's G query rows ride on its item barrier.
+// Work: items (sequence, group of 4 consecutive kv heads, context partition).
+// A block's pages of consecutive kv heads are adjacent in the pool, so the
+// producer warp moves, per block, the 4 heads' K pages with one 1-D bulk copy
+// and their V pages with another (about 8.7 KB each at block size 16: copies
+// of a few KB keep HBM near its copy bandwidth, where single 2 KB pages do
+// not).  Consumer warp w serves kv head 4 * group + w over every block of the
+// item, with its own running max, denominator and accumulator, and writes its
+// rows (or partition partials) itself: no merge between warps.  Every warp
+// consumes every stage (empty barriers count 4 arrivals), so the stage ring
+// has no ownership constraint.
 //
 // Consumers: a warp is G head groups of W = 32 / G lanes; each lane serves one
-// query head through the whole item (its own running max, denominator and
-// accumulator), so every reduction stays inside a head group.  Per block of
-// block_size tokens:
-//  - QK: a head group's lanes are (token, part) pairs, kTpr tokens per round
-//    and kP = W / kTpr lanes per token (a 128-code row split kP ways).
+// query head.  Per block of block_size tokens:
+//  - QK: a head group's lanes are (token, part) pairs, part in the low lane
+//    bits: kTpr tokens per round, kP lanes per token (a 128-code row split kP
+//    ways).  Pages land unswizzled; the lanes of a token read its chunks in an
+//    order rotated by the token index (their query pairs are stored rotated
+//    the same way), so every 8-lane phase of a 16-byte shared load covers 8
+//    distinct bank groups.
 //      INT8: the query row is quantised once per item to int16 (scale
 //      max|q| / 32767) and dp2a multiplies 16-bit query pairs by code bytes
 //      exactly into int32 sums.
@@ -35,11 +39,6 @@
 //      a dimension in one instruction; the int32 sums join the fp32
 //      accumulator once per block.
 //      E4M3: codes widened to fp32, fp32 FMA with the fp32 weight.
-//  Pages land unswizzled: in QK the lanes of one token row read its chunks in
-//  an order rotated by the token index (their query pairs are stored rotated
-//  the same way), so each shared load spreads over all 32 banks; in PV all
-//  lanes read one row.  Shared-memory offsets are per-lane constants, stage
-//  indices advance without division.
 // Every wait is bounded (PA_DEVERR_TIMEOUT); table entries outside the pool
 // are never dereferenced (PA_DEVERR_BAD_BLOCK).
 #pragma once
@@ -49,20 +48,21 @@
 
 namespace pa {
 
-constexpr int kQ8fWarps = 4;
+constexpr int kQ8fWarps = 4;  // consumer warps = kv heads per item
 constexpr int kQ8fThreads = (kQ8fWarps + 1) * 32;
 constexpr int kQ8fItemSlots = 4;
 constexpr int kQ8fD = 128;
 
 struct Q8fItem {
-    int s, kvh, part, nparts;
+    int s, kvh0, nh, part;  // sequence, first kv head, kv heads in the item (<= 4), partition
+    int nparts;
     int nb;       // blocks of the item (0: empty sequence)
     int tok_lo;   // attended tokens of the item: [tok_lo, tok_hi)
     int tok_hi;
     int blk_lo;   // first logical block
-    int t_first;  // pipeline stage of the first block
+    int t_first;  // pipeline stage counter of the first block
     int end;      // 1: no more items
-    int pad[2];
+    int pad;
 };
 
 template <int G, int BS> struct Q8fCfg {
@@ -78,15 +78,15 @@ template <int G, int BS> struct Q8fCfg {
     static constexpr int kQp = 64 / kP;                                 // packed query pairs per lane
     static constexpr int kDG = 4 * G;                                   // PV dims per lane
     static constexpr int kPage = q8_page_bytes(BS, D);                  // bytes of one page
-    static constexpr int kQRow = D * 4;                                 // query row slot (fp32 at most)
     static_assert(kTpr % 2 == 0 && kP >= 1 && kCpl >= 1 && BS % kTpr == 0, "lane mapping");
 };
 
 struct Q8fLayout {
-    uint32_t full, empty, ifull, iempty, mfull, mempty, valid, items, table, qbuf, mscr, mml, stages, total;
+    uint32_t full, empty, ifull, iempty, valid, items, table, qbuf, stages, total;
 };
 
-__host__ __device__ inline Q8fLayout q8f_smem_layout(int S, int BS, int G) {
+// Stage = [K pages of the 4 heads][V pages of the 4 heads]; qrow = bytes of one query row.
+__host__ __device__ inline Q8fLayout q8f_smem_layout(int S, int BS, int G, int qrow) {
     Q8fLayout L;
     uint32_t off = 0;
     L.full = off;
@@ -97,10 +97,6 @@ __host__ __device__ inline Q8fLayout q8f_smem_layout(int S, int BS, int G) {
     off += 8 * kQ8fItemSlots;
     L.iempty = off;
     off += 8 * kQ8fItemSlots;
-    L.mfull = off;
-    off += 16;
-    L.mempty = off;
-    off += 16;
     L.valid = off;
     off += 4 * S;
     L.items = align_up(off, 16);
@@ -108,16 +104,25 @@ __host__ __device__ inline Q8fLayout q8f_smem_layout(int S, int BS, int G) {
     L.table = off;
     off += 4 * kMaxBpp;
     L.qbuf = align_up(off, 128);
-    off = L.qbuf + kQ8fItemSlots * G * kQ8fD * 4;
-    L.mscr = align_up(off, 16);
-    off = L.mscr + 2 * kQ8fWarps * G * kQ8fD * 4;
-    L.mml = off;
-    off += 2 * kQ8fWarps * G * 2 * 4;
+    off = L.qbuf + kQ8fItemSlots * kQ8fWarps * G * qrow;
     L.stages = align_up(off, 128);
-    off = L.stages + S * 2 * q8_page_bytes(BS, kQ8fD);
+    off = L.stages + S * 2 * kQ8fWarps * q8_page_bytes(BS, kQ8fD);
     L.total = off + 128;  // slack to align the dynamic shared memory base
     return L;
 }
+
+// Self-checks (compiled in with PA_SELF_CHECK): an index or address outside
+// its buffer sets bit (8 + code) of the error word and the access is skipped.
+#ifdef PA_SELF_CHECK
+__device__ inline bool q8f_ok(const DecodeParams &p, bool cond, int code) {
+    if (!cond && p.err)
+        atomicOr(p.err, 0x100u << code);
+    return cond;
+}
+#define Q8F_OK(cond, code) q8f_ok(p, (cond), (code))
+#else
+#define Q8F_OK(cond, code) true
+#endif
 
 __device__ inline float q8f_exp2(float x) {
     float y;
@@ -141,19 +146,6 @@ __device__ inline uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
     asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(static_cast<unsigned short>(two_codes)));
     return h2;
 }
-
-// Self-checks (compiled in with PA_SELF_CHECK): an index or address outside
-// its buffer sets bit (8 + code) of the error word and the access is skipped.
-#ifdef PA_SELF_CHECK
-__device__ inline bool q8f_ok(const DecodeParams &p, bool cond, int code) {
-    if (!cond && p.err)
-        atomicOr(p.err, 0x100u << code);
-    return cond;
-}
-#define Q8F_OK(cond, code) q8f_ok(p, (cond), (code))
-#else
-#define Q8F_OK(cond, code) true
-#endif
 
 // Shared-memory loads at 32-bit shared-window addresses.
 __device__ inline uint4 lds128(uint32_t a) {
@@ -218,7 +210,7 @@ template <int G> __device__ inline void lds_pv(uint32_t a, uint32_t *w) {
 // ---------------------------------------------------------------------------
 
 template <int G, int BS>
-__device__ inline void q8f_producer(const DecodeParams &p, char *smem, const Q8fLayout &L) {
+__device__ inline void q8f_producer(const DecodeParams &p, char *smem, const Q8fLayout &L, int qrow) {
     using C = Q8fCfg<G, BS>;
     const int lane = threadIdx.x & 31;
     const int S = p.stages;
@@ -234,8 +226,8 @@ __device__ inline void q8f_producer(const DecodeParams &p, char *smem, const Q8f
     const char *qg = static_cast<const char *>(p.q);
     const char *kc = static_cast<const char *>(p.k_cache);
     const char *vc = static_cast<const char *>(p.v_cache);
-    const uint32_t qrow = kQ8fD * (p.q_dtype == PA_F32 ? 4 : 2);
     const uint64_t policy = policy_evict_first();
+    const uint32_t stage_bytes = 2u * kQ8fWarps * C::kPage;
 
     int chunk_base = 0;
     long long chunk_prefix = 0;
@@ -246,11 +238,11 @@ __device__ inline void q8f_producer(const DecodeParams &p, char *smem, const Q8f
     uint32_t pphase = 0;  // (t / S) & 1
     int k = 0;            // items issued
     bool ok = true;
-    const long long hkv = p.num_kv_heads;
+    const int nquads = (p.num_kv_heads + kQ8fWarps - 1) / kQ8fWarps;
 
     for (long long w = blockIdx.x;; w += gridDim.x) {
-        const long long f = w / hkv;
-        const int kvh = static_cast<int>(w % hkv);
+        const long long f = w / nquads;
+        const int kvh0 = static_cast<int>(w % nquads) * kQ8fWarps;
         int s = -1, part = 0, len = 0, start = 0, nparts = 1;
         for (;;) {
             if (!chunk_ready) {
@@ -304,10 +296,12 @@ __device__ inline void q8f_producer(const DecodeParams &p, char *smem, const Q8f
         const SeqSpan sp = seq_span(len, p.max_len, p.window, BS, p.bpp, start);
         const int blk_lo = sp.b0 + part * p.bpp;
         const int nb = max(0, min(p.bpp, sp.nblk - part * p.bpp));
+        const int nh = min(kQ8fWarps, p.num_kv_heads - kvh0);
         if (lane == 0) {
             Q8fItem it;
             it.s = s;
-            it.kvh = kvh;
+            it.kvh0 = kvh0;
+            it.nh = nh;
             it.part = part;
             it.nparts = sp.nparts;
             it.nb = nb;
@@ -316,11 +310,14 @@ __device__ inline void q8f_producer(const DecodeParams &p, char *smem, const Q8f
             it.blk_lo = blk_lo;
             it.t_first = static_cast<int>(t);
             it.end = 0;
+            it.pad = 0;
             items[slot] = it;
             if (nb > 0) {
-                mbar_arrive_expect_tx(&ifull[slot], G * qrow);
-                bulk_g2s(qbuf + slot * G * C::kQRow, qg + (static_cast<long long>(s) * p.num_heads + kvh * G) * qrow,
-                         G * qrow, &ifull[slot]);
+                // the query rows of the item's heads are consecutive in q
+                const uint32_t qbytes = static_cast<uint32_t>(nh * G * qrow);
+                mbar_arrive_expect_tx(&ifull[slot], qbytes);
+                bulk_g2s(qbuf + slot * kQ8fWarps * G * qrow,
+                         qg + (static_cast<long long>(s) * p.num_heads + kvh0 * G) * qrow, qbytes, &ifull[slot]);
             } else {
                 mbar_arrive(&ifull[slot]);
             }
@@ -349,14 +346,13 @@ __device__ inline void q8f_producer(const DecodeParams &p, char *smem, const Q8f
             if (lane == 0) {
                 const int pb = tbl[j];
                 valid[stage] = pb >= 0;
-                if (pb >= 0 && Q8F_OK(stage >= 0 && stage < S, 0) &&
-                    Q8F_OK(static_cast<long long>(pb) * p.num_kv_heads + kvh <
-                               static_cast<long long>(p.num_blocks) * p.num_kv_heads, 1)) {
-                    mbar_arrive_expect_tx(&full[stage], 2 * C::kPage);
-                    char *dk = stage_buf + static_cast<size_t>(stage) * 2 * C::kPage;
-                    const long long z = static_cast<long long>(pb) * p.num_kv_heads + kvh;
-                    bulk_g2s_hint(dk, kc + z * C::kPage, C::kPage, &full[stage], policy);
-                    bulk_g2s_hint(dk + C::kPage, vc + z * C::kPage, C::kPage, &full[stage], policy);
+                if (pb >= 0 && Q8F_OK(stage >= 0 && stage < S, 0)) {
+                    const uint32_t bytes = static_cast<uint32_t>(nh * C::kPage);
+                    mbar_arrive_expect_tx(&full[stage], 2 * bytes);
+                    char *dk = stage_buf + static_cast<size_t>(stage) * stage_bytes;
+                    const long long z = static_cast<long long>(pb) * p.num_kv_heads + kvh0;
+                    bulk_g2s_hint(dk, kc + z * C::kPage, bytes, &full[stage], policy);
+                    bulk_g2s_hint(dk + kQ8fWarps * C::kPage, vc + z * C::kPage, bytes, &full[stage], policy);
                 } else {
                     mbar_arrive(&full[stage]);
                 }
@@ -378,12 +374,12 @@ __device__ inline void q8f_producer(const DecodeParams &p, char *smem, const Q8f
 }
 
 template <int Fmt, int G, int BS>
-__device__ inline void q8f_consumer(const DecodeParams &p, char *smem, const Q8fLayout &L) {
+__device__ inline void q8f_consumer(const DecodeParams &p, char *smem, const Q8fLayout &L, int qrow) {
     using C = Q8fCfg<G, BS>;
     constexpr int kW = C::kW, kTpr = C::kTpr, kP = C::kP, kR = C::kRounds, kCpl = C::kCpl, kQp = C::kQp;
     constexpr int kDG = C::kDG;
     constexpr bool kI8 = (Fmt == kFmtI8);
-    const int warp = threadIdx.x >> 5;
+    const int warp = threadIdx.x >> 5;  // kv head kvh0 + warp of each item
     const int lane = threadIdx.x & 31;
     const int g = lane / kW;         // this lane's query head within the kv head's group
     const int wl = lane % kW;        // lane within the head group
@@ -397,15 +393,11 @@ __device__ inline void q8f_consumer(const DecodeParams &p, char *smem, const Q8f
     uint64_t *empty = reinterpret_cast<uint64_t *>(smem + L.empty);
     uint64_t *ifull = reinterpret_cast<uint64_t *>(smem + L.ifull);
     uint64_t *iempty = reinterpret_cast<uint64_t *>(smem + L.iempty);
-    uint64_t *mfull = reinterpret_cast<uint64_t *>(smem + L.mfull);
-    uint64_t *mempty = reinterpret_cast<uint64_t *>(smem + L.mempty);
     const int *valid = reinterpret_cast<const int *>(smem + L.valid);
     const Q8fItem *items = reinterpret_cast<const Q8fItem *>(smem + L.items);
     const char *qbuf = smem + L.qbuf;
-    float *mscr = reinterpret_cast<float *>(smem + L.mscr);  // [2][warps][G][D]
-    float *mml = reinterpret_cast<float *>(smem + L.mml);    // [2][warps][G][2]
     const uint32_t stages_a = smem_addr(smem + L.stages);
-    const int qelt = p.q_dtype == PA_F32 ? 4 : 2;
+    const uint32_t stage_bytes = 2u * kQ8fWarps * C::kPage;
 
     // per-lane offsets inside a page: QK chunk i of row `tok` is the lane's
     // chunk (i + tok) mod kCpl (the rotation spreads a warp's loads over all
@@ -428,10 +420,9 @@ __device__ inline void q8f_consumer(const DecodeParams &p, char *smem, const Q8f
         const Q8fItem it = items[slot];
         if (it.end)
             break;
-        if (it.nb > 0) {
-            const char *qr = qbuf + slot * G * C::kQRow + g * kQ8fD * qelt;
-            (void)Q8F_OK(slot >= 0 && slot < kQ8fItemSlots && it.s >= 0 && it.s < p.num_seqs &&
-                             it.part >= 0 && it.part < p.max_parts, 9);
+        const bool active = warp < it.nh;  // a head past num_kv_heads in the last group idles
+        if (it.nb > 0 && active) {
+            const char *qr = qbuf + (slot * kQ8fWarps + warp) * G * qrow + g * qrow;
             // the row's largest magnitude: this lane's QK dims, then over the
             // parts of its token (they cover the row once)
             float amax = 0.f;
@@ -490,18 +481,17 @@ __device__ inline void q8f_consumer(const DecodeParams &p, char *smem, const Q8f
         for (int i = 0; i < kDG; ++i)
             acc[i] = 0.f;
 
-        int j = (warp - it.t_first % kQ8fWarps + kQ8fWarps) % kQ8fWarps;
-        const uint32_t t0 = static_cast<uint32_t>(it.t_first + j);
+        const uint32_t t0 = static_cast<uint32_t>(it.t_first);
         int stage = static_cast<int>(t0 % S);
         uint32_t phase = (t0 / S) & 1u;
-        for (; j < it.nb; j += kQ8fWarps) {
+        for (int j = 0; j < it.nb; ++j) {
             if (!mbar_wait_bounded(&full[stage], phase)) {
                 ok = false;
                 break;
             }
-            if (valid[stage] && Q8F_OK(stage >= 0 && stage < S, 3)) {
-                const uint32_t kt = stages_a + static_cast<uint32_t>(stage) * 2 * C::kPage;
-                const uint32_t vt = kt + C::kPage;
+            if (active && valid[stage] && Q8F_OK(stage >= 0 && stage < S, 3)) {
+                const uint32_t kt = stages_a + static_cast<uint32_t>(stage) * stage_bytes + warp * C::kPage;
+                const uint32_t vt = kt + kQ8fWarps * C::kPage;
                 const uint32_t sk = kt + BS * 128;  // the pages' scale rows
                 const uint32_t sv = vt + BS * 128;
                 const int blk = it.blk_lo + j;
@@ -576,7 +566,7 @@ __device__ inline void q8f_consumer(const DecodeParams &p, char *smem, const Q8f
                 for (int rd = 0; rd < kR; ++rd) {
                     const float pr = q8f_exp2(sc[rd] - m);
                     l += pr;
-                    pw[rd] = pr * (Q8F_OK(rd * kTpr + tok < BS, 6) ? ldsf(sv + (rd * kTpr + tok) * 4) : 0.f);
+                    pw[rd] = pr * ldsf(sv + (rd * kTpr + tok) * 4);
                 }
 
                 // ---- P V: this lane's kDG dims of its head
@@ -663,82 +653,47 @@ __device__ inline void q8f_consumer(const DecodeParams &p, char *smem, const Q8f
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(&empty[stage]);
-            stage += kQ8fWarps;
-            if (stage >= S) {
-                stage -= S;
+            if (++stage == S) {
+                stage = 0;
                 phase ^= 1u;
             }
         }
         if (!ok)
             break;
 
-        // ---- merge the 4 warps' states of this item (double-buffered by item parity)
-        // l holds this lane's tokens (the parts of a token hold copies): sum over tokens
+        // ---- this warp's head: the output rows, or the partition's partials
+        if (active) {
+            // l holds this lane's tokens (the parts of a token hold copies): sum over tokens
 #pragma unroll
-        for (int o = kP; o < kW; o <<= 1)
-            l += __shfl_xor_sync(0xffffffffu, l, o);
-        const int b = k & 1;
-        const uint32_t use = static_cast<uint32_t>(k >> 1) & 1u;
-        if (!mbar_wait_bounded(&mempty[b], use ^ 1u)) {
-            ok = false;
-            break;
-        }
-        float *dst = mscr + ((b * kQ8fWarps + warp) * G + g) * kQ8fD + wl * kDG;
+            for (int o = kP; o < kW; o <<= 1)
+                l += __shfl_xor_sync(0xffffffffu, l, o);
+            const long long orow = static_cast<long long>(it.s) * p.num_heads + (it.kvh0 + warp) * G + g;
+            if (Q8F_OK(orow >= 0 && orow < static_cast<long long>(p.num_seqs) * p.num_heads, 7)) {
+                if (it.nparts == 1 && !p.force_partial) {
+                    const float rl = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
-        for (int i = 0; i < kDG; i += 4)
-            *reinterpret_cast<float4 *>(dst + i) = make_float4(acc[i], acc[i + 1], acc[i + 2], acc[i + 3]);
-        if (wl == 0) {
-            mml[((b * kQ8fWarps + warp) * G + g) * 2] = m;
-            mml[((b * kQ8fWarps + warp) * G + g) * 2 + 1] = l;
-        }
-        __syncwarp();
-        if (lane == 0)
-            mbar_arrive(&mfull[b]);
-        if (!mbar_wait_bounded(&mfull[b], use)) {
-            ok = false;
-            break;
-        }
-        for (int idx = warp * 32 + lane; idx < G * kQ8fD; idx += kQ8fWarps * 32) {
-            const int gg = idx / kQ8fD, dd = idx % kQ8fD;
-            float M = -INFINITY;
+                    for (int i = 0; i < kDG; ++i)
+                        store_out(p.out, p.out_dtype, orow * kQ8fD + wl * kDG + i, acc[i] * rl);
+                } else if (Q8F_OK(p.part_acc != nullptr && it.part >= 0 && it.part < p.max_parts, 8)) {
+                    const long long pr = orow * p.max_parts + it.part;
+                    float *dst = p.part_acc + pr * kQ8fD + wl * kDG;
 #pragma unroll
-            for (int w2 = 0; w2 < kQ8fWarps; ++w2)
-                M = fmaxf(M, mml[((b * kQ8fWarps + w2) * G + gg) * 2]);
-            float num = 0.f, den = 0.f;
-            if (M != -INFINITY) {
-#pragma unroll
-                for (int w2 = 0; w2 < kQ8fWarps; ++w2) {
-                    const float sw = q8f_exp2(mml[((b * kQ8fWarps + w2) * G + gg) * 2] - M);
-                    num = fmaf(mscr[((b * kQ8fWarps + w2) * G + gg) * kQ8fD + dd], sw, num);
-                    den = fmaf(mml[((b * kQ8fWarps + w2) * G + gg) * 2 + 1], sw, den);
-                }
-            }
-            const long long orow = static_cast<long long>(it.s) * p.num_heads + it.kvh * G + gg;
-            if (!Q8F_OK(orow >= 0 && orow < static_cast<long long>(p.num_seqs) * p.num_heads, 7))
-                continue;
-            if (it.nparts == 1 && !p.force_partial) {
-                store_out(p.out, p.out_dtype, orow * kQ8fD + dd, den > 0.f ? num / den : 0.f);
-            } else {
-                const long long pr = orow * p.max_parts + it.part;
-                if (!Q8F_OK(p.part_acc != nullptr && it.part >= 0 && it.part < p.max_parts, 8))
-                    continue;
-                p.part_acc[pr * kQ8fD + dd] = num;
-                if (dd == 0) {
-                    p.part_ml[pr * 2] = M;
-                    p.part_ml[pr * 2 + 1] = den;
+                    for (int i = 0; i < kDG; i += 4)
+                        *reinterpret_cast<float4 *>(dst + i) = make_float4(acc[i], acc[i + 1], acc[i + 2], acc[i + 3]);
+                    if (wl == 0) {
+                        p.part_ml[pr * 2] = m;
+                        p.part_ml[pr * 2 + 1] = l;
+                    }
                 }
             }
         }
-        __syncwarp();
-        if (lane == 0)
-            mbar_arrive(&mempty[b]);
     }
     if (!ok && lane == 0 && p.err)
         atomicOr(p.err, PA_DEVERR_TIMEOUT);
 }
 
 // CTAs per SM the register budget is set for: 5 for one query head per kv
-// head (20 consumer warps, <= 72 registers a thread), 3 for grouped heads.
+// head (<= 72 registers a thread), 3 for grouped heads.
 template <int G> struct Q8fOccupancy {
     static constexpr int kMinBlocks = G == 1 ? 5 : 3;
 };
@@ -747,12 +702,9 @@ template <int Fmt, int G, int BS>
 __global__ void __launch_bounds__(kQ8fThreads, Q8fOccupancy<G>::kMinBlocks) pa_decode_q8f_kernel(const DecodeParams p) {
     extern __shared__ __align__(128) char smem_raw[];
     char *smem = reinterpret_cast<char *>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
-    const Q8fLayout L = q8f_smem_layout(p.stages, BS, G);
-    // Stage t belongs to consumer warp t % 4.  With a stage count that is not a
-    // multiple of 4, one stage would pass between warps, and a warp running a
-    // full ring ahead could see its parity wait satisfied by an older phase of
-    // that stage.  The host never launches such a count; refuse it here too.
-    if (p.stages < kQ8fWarps || p.stages % kQ8fWarps != 0) {
+    const int qrow = kQ8fD * (p.q_dtype == PA_F32 ? 4 : 2);
+    const Q8fLayout L = q8f_smem_layout(p.stages, BS, G, qrow);
+    if (p.stages < 2) {
         if (threadIdx.x == 0 && p.err)
             atomicOr(p.err, PA_DEVERR_BAD_LAUNCH);
         return;
@@ -762,7 +714,7 @@ __global__ void __launch_bounds__(kQ8fThreads, Q8fOccupancy<G>::kMinBlocks) pa_d
         uint64_t *empty = reinterpret_cast<uint64_t *>(smem + L.empty);
         for (int i = 0; i < p.stages; ++i) {
             mbar_init(&full[i], 1);
-            mbar_init(&empty[i], 1);
+            mbar_init(&empty[i], kQ8fWarps);
         }
         uint64_t *ifull = reinterpret_cast<uint64_t *>(smem + L.ifull);
         uint64_t *iempty = reinterpret_cast<uint64_t *>(smem + L.iempty);
@@ -770,19 +722,13 @@ __global__ void __launch_bounds__(kQ8fThreads, Q8fOccupancy<G>::kMinBlocks) pa_d
             mbar_init(&ifull[i], 1);
             mbar_init(&iempty[i], kQ8fWarps);
         }
-        uint64_t *mfull = reinterpret_cast<uint64_t *>(smem + L.mfull);
-        uint64_t *mempty = reinterpret_cast<uint64_t *>(smem + L.mempty);
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(&mfull[i], kQ8fWarps);
-            mbar_init(&mempty[i], kQ8fWarps);
-        }
         fence_mbar_init();
     }
     __syncthreads();
     if ((threadIdx.x >> 5) == kQ8fWarps)
-        q8f_producer<G, BS>(p, smem, L);
+        q8f_producer<G, BS>(p, smem, L, qrow);
     else
-        q8f_consumer<Fmt, G, BS>(p, smem, L);
+        q8f_consumer<Fmt, G, BS>(p, smem, L, qrow);
 }
 
 }  // namespace pa
