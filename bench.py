@@ -533,7 +533,7 @@ def kernel_source_hash() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_cache_251_gb300", "csrc")
     for fn in sorted(os.listdir(csrc)):
-        if fn.startswith("pa_decode") or fn in ("pa_device.cuh", "pa_api.cu"):
+        if fn.startswith("pa_decode") or fn in ("pa_device.cuh", "pa_api.cu", "pa_quant.cuh"):
             with open(os.path.join(csrc, fn), "rb") as f:
                 h.update(fn.encode() + f.read())
     return h.hexdigest()[:16]
