@@ -19,6 +19,7 @@
 #include "pa_decode_mha.cuh"
 #include "pa_decode_q8.cuh"
 #include "pa_decode_q8f.cuh"
+#include "pa_decode_q8t.cuh"
 #include "pa_internal.h"
 
 namespace pa {
@@ -189,6 +190,30 @@ pa_status q_tensor_map(CUtensorMap *map, const void *base, int dtype, int head_d
     return PA_OK;
 }
 
+// 3-D view of an 8-bit page pool [pages = block * H_kv + head][block_size +
+// scale rows][128 bytes] for the tensor-core E4M3 kernel.  Codes: a box is the
+// code rows of 4 adjacent pages (128-byte swizzle); scales: a box is the
+// 4 * block_size scale bytes of the same 4 pages (no swizzle).
+pa_status q8_page_tensor_map(CUtensorMap *map, const void *base, int block_size, long long pages, bool scales) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
+    cudaError_t e = tensor_map_encoder(&enc);
+    if (e != cudaSuccess || !enc)
+        return cuda_fail(e == cudaSuccess ? cudaErrorSymbolNotFound : e, "cuTensorMapEncodeTiled lookup");
+    const cuuint64_t rows = static_cast<cuuint64_t>(block_size + q8_scale_rows(block_size, 128));
+    cuuint64_t dims[3] = {128, rows, static_cast<cuuint64_t>(pages)};
+    cuuint64_t strides[2] = {128, rows * 128};
+    cuuint32_t box[3] = {scales ? static_cast<cuuint32_t>(4 * block_size) : 128u,
+                         scales ? 1u : static_cast<cuuint32_t>(block_size), static_cast<cuuint32_t>(kQ8tHeads)};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, scales ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(PA_ERR_INVALID_ARGUMENT, "cuTensorMapEncodeTiled rejected the 8-bit page layout (code " +
+                                                 std::to_string(static_cast<int>(r)) + ")");
+    return PA_OK;
+}
+
 constexpr int kDefaultPartition = 512;
 constexpr int kQ8fStageBudget = 48 * 1024;
 constexpr int kMhaStageBudget = 64 * 1024;
@@ -316,6 +341,53 @@ pa_status launch_decode_kernel(DecodeParams &p, int dtype, int head_dim, int G, 
 
 pa_status launch_decode_q8_kernel(DecodeParams &p, int cache_dtype, int head_dim, int G, cudaStream_t cs) {
     const long long tiles = static_cast<long long>(p.num_blocks) * p.num_kv_heads;
+    // E4M3 pages, grouped heads, head_dim 128, block size 16 / 32, kv heads in
+    // fours, 16-bit queries: the tensor-core kernel (kind::f8f6f4 on the codes).
+    // One query per kv head stays on the TMA-fed CUDA-core kernel, which is
+    // faster there.
+    const bool tc = cache_dtype == PA_E4M3 && head_dim == 128 && G >= 2 && G <= kQ8tMaxG &&
+                    (p.block_size == 16 || p.block_size == 32) && p.num_kv_heads % kQ8tHeads == 0 &&
+                    (p.q_dtype == PA_F16 || p.q_dtype == PA_BF16) && tiles <= INT_MAX &&
+                    static_cast<long long>(p.num_seqs) * p.num_heads <= INT_MAX;
+    if (tc) {
+        const void *tfn = decode_q8t_kernel_e4m3(G, p.block_size);
+        if (!tfn)
+            return fail(PA_ERR_UNSUPPORTED, "no tensor-core E4M3 decode kernel for this group / block size");
+        CUtensorMap tmk, tmv, tsk, tsv;
+        pa_status ts = q8_page_tensor_map(&tmk, p.k_cache, p.block_size, tiles, false);
+        if (ts == PA_OK)
+            ts = q8_page_tensor_map(&tmv, p.v_cache, p.block_size, tiles, false);
+        if (ts == PA_OK)
+            ts = q8_page_tensor_map(&tsk, p.k_cache, p.block_size, tiles, true);
+        if (ts == PA_OK)
+            ts = q8_page_tensor_map(&tsv, p.v_cache, p.block_size, tiles, true);
+        if (ts != PA_OK)
+            return ts;
+        p.stages = kQ8tStages;
+        const size_t smem = q8t_smem_layout(kQ8tStages).total;
+        int dev = 0, sms = 0, per_sm = 0;
+        cudaError_t e = device_sms(&dev, &sms);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "device query");
+        e = prepare_kernel(dev, tfn, smem, kQ8tThreads, &per_sm);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "decode kernel set-up");
+        if (per_sm < 1)
+            return fail(PA_ERR_UNSUPPORTED, "decode kernel does not fit on an SM");
+        const long long items_max =
+            static_cast<long long>(p.num_seqs) * (p.num_kv_heads / kQ8tHeads) * p.max_parts;
+        // one CTA per SM: each holds all of an SM's tensor memory
+        long long grid = sms;
+        if (grid > items_max)
+            grid = items_max;
+        if (grid < 1)
+            grid = 1;
+        void *args[] = {&p, &tmk, &tmv, &tsk, &tsv};
+        e = cudaLaunchKernel(tfn, dim3(static_cast<unsigned>(grid)), dim3(kQ8tThreads), args, smem, cs);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "decode launch");
+        return PA_OK;
+    }
     // head_dim 128, up to 4 query heads per kv head: the TMA-fed kernel (E4M3
     // multiplies fp16 queries, so fp32 queries stay on the general kernel)
     const bool fast = head_dim == 128 && G <= 4 && tiles <= INT_MAX &&

@@ -38,6 +38,11 @@ const void *decode_q8_kernel_e4m3(int head_dim, int group);
 const void *decode_q8f_kernel_i8(int group, int block_size);
 const void *decode_q8f_kernel_e4m3(int group, int block_size);
 
+// Tensor-core decode kernels for E4M3 pages (kind::f8f6f4): head_dim 128, 4 kv
+// heads per item, per query group (2, 4) and block size (16, 32);
+// nullptr if not built.
+const void *decode_q8t_kernel_e4m3(int group, int block_size);
+
 cudaError_t launch_append(const void *k, const void *v, const int64_t *slots, void *k_cache, void *v_cache,
                           int num_tokens, int num_kv_heads, int row_bytes, int block_size, int num_blocks,
                           uint32_t *err, int num_sms, cudaStream_t stream);

@@ -153,6 +153,15 @@ QCASES = [
     ("g4_bs8", 3, 8, 2, 128, 8, [129, 1, 1000], 0, 0),
     ("g4_bs32_window", 3, 16, 4, 128, 32, [33, 2049, 64], 100, 0),
     ("g1_bs32_empty", 3, 2, 2, 128, 32, [0, 65, 0], 0, 0),
+    # kv heads in fours, block size 16 / 32 (E4M3 with 16-bit queries: the
+    # tensor-core kernel): partitions of 4 blocks (2 tiles) and of 3 blocks (a
+    # last tile with one block), windows, empty sequences
+    ("tc_g4_bs16_parts", 3, 16, 4, 128, 16, [700, 129, 2049], 0, 64),
+    ("tc_g4_bs16_odd_parts", 3, 16, 4, 128, 16, [1000, 1, 47], 0, 48),
+    ("tc_g4_window", 2, 16, 4, 128, 16, [3000, 77], 700, 0),
+    ("tc_g2_bs32", 4, 8, 4, 128, 32, [129, 31, 1000, 257], 0, 0),
+    ("tc_g1_bs32_parts", 3, 8, 8, 128, 32, [2000, 33, 700], 0, 64),
+    ("tc_g4_hkv8_empty", 3, 32, 8, 128, 16, [0, 300, 0], 0, 0),
 ]
 
 
@@ -175,10 +184,11 @@ def test_decode_quant_low_precision_output(out_dt):
     compare(got, _oracle_decode_quant(inp, pools), torch.bfloat16)
 
 
+@pytest.mark.parametrize("hkv", [2, 4])
 @pytest.mark.parametrize("fmt", FMTS)
-def test_decode_quant_zero_scale_rows(fmt):
+def test_decode_quant_zero_scale_rows(fmt, hkv):
     """Rows stored with scale 0 (all-zero rows) read as zeros."""
-    inp, pools = _quant_case("zeros", 2, 4, 2, 128, 16, [40, 70], 0, torch.float16, fmt, seed=4)
+    inp, pools = _quant_case("zeros", 2, 2 * hkv, hkv, 128, 16, [40, 70], 0, torch.float16, fmt, seed=4)
     kc, ks = oracle.unpack_pages(pools[0])
     vc, vs = oracle.unpack_pages(pools[1])
     ks[inp.block_tables[0, 0].item(), :, :5] = 0.0
@@ -189,9 +199,10 @@ def test_decode_quant_zero_scale_rows(fmt):
     compare(got, _oracle_decode_quant(inp, pools), torch.float16)
 
 
+@pytest.mark.parametrize("hkv", [2, 4])
 @pytest.mark.parametrize("fmt", FMTS)
-def test_decode_quant_invalid_table_entries_skipped_and_flagged(fmt):
-    inp, pools = _quant_case("bad", 3, 4, 2, 128, 16, [70, 40, 33], 0, torch.float16, fmt, seed=8)
+def test_decode_quant_invalid_table_entries_skipped_and_flagged(fmt, hkv):
+    inp, pools = _quant_case("bad", 3, 2 * hkv, hkv, 128, 16, [70, 40, 33], 0, torch.float16, fmt, seed=8)
     bt = inp.block_tables.clone()
     bt[0, 1] = inp.num_blocks + 5
     bt[2, 0] = -7
