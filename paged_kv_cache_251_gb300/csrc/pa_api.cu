@@ -24,11 +24,13 @@
 
 namespace pa {
 
-const void *reduce_kernel(int head_dim) {
+const void *reduce_kernel(int head_dim, bool wide) {
     if (head_dim == 64)
-        return reinterpret_cast<const void *>(&pa_reduce_kernel<64>);
+        return wide ? reinterpret_cast<const void *>(&pa_reduce_wide_kernel<64>)
+                    : reinterpret_cast<const void *>(&pa_reduce_kernel<64>);
     if (head_dim == 128)
-        return reinterpret_cast<const void *>(&pa_reduce_kernel<128>);
+        return wide ? reinterpret_cast<const void *>(&pa_reduce_wide_kernel<128>)
+                    : reinterpret_cast<const void *>(&pa_reduce_kernel<128>);
     return nullptr;
 }
 
@@ -256,6 +258,20 @@ pa_status plan_decode(int num_seqs, int num_heads, int head_dim, int block_size,
 
 void set_last_error_detail(const char *why) { g_detail = why; }
 
+// The partition reduce: a warp per row when there are rows enough to fill the
+// GPU and few partitions each, else a CTA per row.
+cudaError_t launch_reduce(DecodeParams &p, int head_dim, long long rows, cudaStream_t cs) {
+    int dev = 0, sms = 0;
+    cudaError_t e = device_sms(&dev, &sms);
+    if (e != cudaSuccess)
+        return e;
+    const bool wide = rows < 8LL * sms || p.max_parts > 32;
+    void *args[] = {&p};
+    const long long grid = wide ? rows : (rows + kReduceRows - 1) / kReduceRows;
+    return cudaLaunchKernel(reduce_kernel(head_dim, wide), dim3(static_cast<unsigned>(grid)), dim3(kReduceThreads),
+                            args, 0, cs);
+}
+
 pa_status launch_decode_kernel(DecodeParams &p, int dtype, int head_dim, int G, cudaStream_t cs) {
     const int block_size = p.block_size;
     const int row = head_dim * elt_bytes(dtype);
@@ -382,6 +398,9 @@ pa_status launch_decode_q8_kernel(DecodeParams &p, int cache_dtype, int head_dim
             grid = items_max;
         if (grid < 1)
             grid = 1;
+        // items are claimed from a per-launch counter (balances contexts of
+        // mixed lengths); without one they go round-robin
+        p.work = q8t_work_counter(dev);
         void *args[] = {&p, &tmk, &tmv, &tsk, &tsv};
         e = cudaLaunchKernel(tfn, dim3(static_cast<unsigned>(grid)), dim3(kQ8tThreads), args, smem, cs);
         if (e != cudaSuccess)
@@ -538,12 +557,9 @@ pa_status pa_decode(void *out, const void *q, const void *k_cache, const void *v
     if (ls != PA_OK)
         return ls;
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-    void *args[] = {&p};
-    cudaError_t e;
     if (plan.max_parts > 1) {
         const long long rows = static_cast<long long>(num_seqs) * num_heads;
-        e = cudaLaunchKernel(reduce_kernel(head_dim), dim3(static_cast<unsigned>(rows)), dim3(kReduceThreads), args, 0,
-                             cs);
+        const cudaError_t e = launch_reduce(p, head_dim, rows, cs);
         if (e != cudaSuccess)
             return cuda_fail(e, "reduce launch");
     }
@@ -722,10 +738,8 @@ pa_status pa_decode_quant(void *out, const void *q, const void *k_cache, const v
     if (ls != PA_OK)
         return ls;
     if (plan.max_parts > 1) {
-        void *args[] = {&p};
         const long long rows = static_cast<long long>(num_seqs) * num_heads;
-        cudaError_t e = cudaLaunchKernel(reduce_kernel(head_dim), dim3(static_cast<unsigned>(rows)),
-                                         dim3(kReduceThreads), args, 0, cs);
+        cudaError_t e = launch_reduce(p, head_dim, rows, cs);
         if (e != cudaSuccess)
             return cuda_fail(e, "reduce launch");
     }

@@ -62,6 +62,10 @@ struct DecodeParams {
     // 8-bit caches only: the element type of q (the caches hold pages of
     // codes and row scales)
     int q_dtype;
+    // Dynamic item scheduling (kernels that support it): {next item, CTAs
+    // done}, zero before the launch and returned to zero by its last CTA;
+    // nullptr: items go round-robin over the CTAs.
+    unsigned int *work = nullptr;
 };
 
 struct StageMeta {
@@ -523,15 +527,80 @@ __global__ void __launch_bounds__(kDecodeThreads) pa_decode_kernel(const DecodeP
 
 // Merge the partitions of every multi-partition (sequence, head):
 //   M = max_p m_p,  out = sum_p 2^(m_p - M) acc_p / sum_p 2^(m_p - M) l_p
-// One CTA of kReduceThreads per (sequence, head) row: the (m, l) pairs are
-// read by all threads at once (block max and sum), then the warps take
-// partitions round-robin, each lane a contiguous slice of head_dim, and sum
-// their slices through shared memory.  Single-partition rows were written by
-// the decode kernel and are left alone.
+// Two layouts: pa_reduce_kernel, one warp per (sequence, head) row and
+// kReduceRows rows per CTA with no CTA-wide step (the lanes take the (m, l)
+// pairs for the row max and the denominator, then each lane sums its head_dim
+// slice over the partitions, the loads of several partitions in flight), for
+// many rows of few partitions; pa_reduce_wide_kernel, one CTA per row (the
+// warps take partitions round-robin and sum their slices through shared
+// memory), for few rows of many partitions.  Single-partition rows were
+// written by the decode kernel and are left alone.
 constexpr int kReduceThreads = 128;
+constexpr int kReduceRows = kReduceThreads / 32;
 
 template <int D>
 __global__ void __launch_bounds__(kReduceThreads) pa_reduce_kernel(const DecodeParams p) {
+    constexpr int kPer = D / 32;  // head_dim slice per lane (4 or 2)
+    const int lane = threadIdx.x & 31;
+    const long long rowi = static_cast<long long>(blockIdx.x) * kReduceRows + (threadIdx.x >> 5);
+    if (rowi >= static_cast<long long>(p.num_seqs) * p.num_heads)
+        return;
+    const int s = static_cast<int>(rowi / p.num_heads);
+    const SeqSpan sp = seq_span(ld_nc_i32(p.context_lens + s), p.max_len, p.window, p.block_size, p.bpp,
+                                p.start_tok ? ld_nc_i32(p.start_tok + s) : 0);
+    if (sp.nparts <= 1)
+        return;
+    const int np = sp.nparts;
+    const long long base = rowi * p.max_parts;
+    const float2 *ml = reinterpret_cast<const float2 *>(p.part_ml + base * 2);
+
+    float M = -INFINITY;
+    for (int q = lane; q < np; q += 32)
+        M = fmaxf(M, ml[q].x);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    float den = 0.f;
+    if (M != -INFINITY)
+        for (int q = lane; q < np; q += 32) {
+            const float2 v = ml[q];
+            if (v.x != -INFINITY)
+                den = fmaf(v.y, exp2f(v.x - M), den);
+        }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        den += __shfl_xor_sync(0xffffffffu, den, o);
+
+    float num[kPer];
+#pragma unroll
+    for (int i = 0; i < kPer; ++i)
+        num[i] = 0.f;
+    if (M != -INFINITY) {
+        const float *a = p.part_acc + base * D + lane * kPer;
+#pragma unroll 4
+        for (int q = 0; q < np; ++q) {
+            const float mq = ml[q].x;
+            const float sc = mq == -INFINITY ? 0.f : exp2f(mq - M);
+            if (kPer == 4) {
+                const float4 v = *reinterpret_cast<const float4 *>(a + static_cast<long long>(q) * D);
+                num[0] = fmaf(v.x, sc, num[0]);
+                num[1] = fmaf(v.y, sc, num[1]);
+                num[2] = fmaf(v.z, sc, num[2]);
+                num[3] = fmaf(v.w, sc, num[3]);
+            } else {
+                const float2 v = *reinterpret_cast<const float2 *>(a + static_cast<long long>(q) * D);
+                num[0] = fmaf(v.x, sc, num[0]);
+                num[kPer > 1 ? 1 : 0] = fmaf(v.y, sc, num[kPer > 1 ? 1 : 0]);
+            }
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < kPer; ++i)
+        store_out(p.out, p.out_dtype, rowi * D + lane * kPer + i, den > 0.f ? num[i] / den : 0.f);
+}
+
+template <int D>
+__global__ void __launch_bounds__(kReduceThreads) pa_reduce_wide_kernel(const DecodeParams p) {
     constexpr int kWarps = kReduceThreads / 32;
     constexpr int kPer = D / 32;  // head_dim slice per lane (4 or 2)
     __shared__ float red[kWarps];

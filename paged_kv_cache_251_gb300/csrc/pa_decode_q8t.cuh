@@ -80,8 +80,8 @@ template <int BS, int G> struct Q8tCfg {
 };
 
 struct Q8tLayout {
-    uint32_t full, empty, ifull, iempty, sfull, sfree, pfull, afull, ofull, ofree, done, fin, fin2;
-    uint32_t meta, items, tmem, table, qf, fbuf, abuf, qbuf, pbuf, stages, total;
+    uint32_t full, empty, ifull, iempty, wfull, sfull, sfree, pfull, afull, ofull, ofree, done, fin, fin2;
+    uint32_t meta, items, witem, tmem, table, qf, fbuf, abuf, qbuf, pbuf, stages, total;
 };
 
 __host__ __device__ inline Q8tLayout q8t_smem_layout(int S) {
@@ -94,6 +94,8 @@ __host__ __device__ inline Q8tLayout q8t_smem_layout(int S) {
     L.ifull = off;
     off += 8 * kQ8tItemSlots;
     L.iempty = off;
+    off += 8 * kQ8tItemSlots;
+    L.wfull = off;
     off += 8 * kQ8tItemSlots;
     L.sfull = off;
     off += 16;
@@ -117,6 +119,8 @@ __host__ __device__ inline Q8tLayout q8t_smem_layout(int S) {
     off += 4 * S;
     L.items = align_up(off, 16);
     off = L.items + sizeof(Q8tItem) * kQ8tItemSlots;
+    L.witem = off;  // item index of each slot, from the query converter to the producer
+    off += 8 * kQ8tItemSlots;
     L.tmem = off;
     off += 16;
     L.table = off;
@@ -303,17 +307,21 @@ __device__ inline void q8t_producer(const DecodeParams &p, const CUtensorMap *tm
         prefetch_tensormap(tsk);
         prefetch_tensormap(tsv);
     }
+    uint64_t *wfull = reinterpret_cast<uint64_t *>(smem + L.wfull);
+    const long long *witem = reinterpret_cast<const long long *>(smem + L.witem);
     Q8tScan<BS> scan;
     uint32_t t = 0;
     bool ok = true;
-    for (long long w = blockIdx.x, k = 0;; w += gridDim.x, ++k) {
-        const auto it0 = scan.find(p, w, true);
-        const int s = it0.s, kvh0 = it0.kvh0;
+    for (long long k = 0;; ++k) {
         const int slot = static_cast<int>(k % kQ8tItemSlots);
-        if (!mbar_wait_bounded(&iempty[slot], static_cast<uint32_t>((k / kQ8tItemSlots) & 1) ^ 1u)) {
+        // the item index comes from the query converter, which picks it
+        if (!mbar_wait_bounded(&iempty[slot], static_cast<uint32_t>((k / kQ8tItemSlots) & 1) ^ 1u) ||
+            !mbar_wait_bounded(&wfull[slot], static_cast<uint32_t>(k / kQ8tItemSlots) & 1u)) {
             ok = false;
             break;
         }
+        const auto it0 = scan.find(p, witem[slot], true);
+        const int s = it0.s, kvh0 = it0.kvh0;
         if (s < 0) {
             if (lane == 0) {
                 items[slot].end = 1;
@@ -410,12 +418,29 @@ __device__ inline bool q8t_qconvert(const DecodeParams &p, char *smem, const Q8t
     float *qfs = reinterpret_cast<float *>(smem + L.qf);
     char *qbuf = smem + L.qbuf;
     const char *qg = static_cast<const char *>(p.q);
+    uint64_t *wfull = reinterpret_cast<uint64_t *>(smem + L.wfull);
+    long long *witem = reinterpret_cast<long long *>(smem + L.witem);
     Q8tScan<BS> scan;
-    for (long long w = blockIdx.x, k = 0;; w += gridDim.x, ++k) {
-        const auto it = scan.find(p, w, false);
+    long long w = blockIdx.x;
+    for (long long k = 0;; ++k) {
         const int slot = static_cast<int>(k % kQ8tItemSlots);
         if (!mbar_wait_bounded(&iempty[slot], static_cast<uint32_t>((k / kQ8tItemSlots) & 1) ^ 1u))
             return false;
+        // the next item: from the launch's shared counter (each CTA takes the
+        // next unclaimed one when it has room), else round-robin
+        if (p.work) {
+            unsigned int v = 0;
+            if (lane == 0)
+                v = atomicAdd(p.work, 1u);
+            w = __shfl_sync(0xffffffffu, v, 0);
+        } else if (k > 0) {
+            w += gridDim.x;
+        }
+        if (lane == 0) {
+            witem[slot] = w;
+            mbar_arrive(&wfull[slot]);
+        }
+        const auto it = scan.find(p, w, false);
         SeqSpan sp;
         int blk_lo;
         if (it.s >= 0 && Q8tScan<BS>::blocks(p, it, sp, blk_lo) > 0) {
@@ -923,6 +948,7 @@ __global__ void __launch_bounds__(kQ8tThreads, 1)
         uint64_t *iempty = reinterpret_cast<uint64_t *>(smem + L.iempty);
         for (int i = 0; i < kQ8tItemSlots; ++i) {
             mbar_init(&ifull[i], 2);  // item record (producer) and query operand (converter)
+            mbar_init(reinterpret_cast<uint64_t *>(smem + L.wfull) + i, 1);
             mbar_init(&iempty[i], 2 * 4 + 2);  // softmax and epilogue warps, S commit, P V thread
         }
         for (int i = 0; i < 2; ++i) {
@@ -995,6 +1021,16 @@ __global__ void __launch_bounds__(kQ8tThreads, 1)
         __syncwarp();
         if ((threadIdx.x & 31) == 0)
             mbar_arrive(reinterpret_cast<uint64_t *>(smem + L.done));
+    }
+    // The CTA has taken its last item: the last CTA to get here returns the
+    // launch's counter to zero for the next launch that uses it.
+    __syncthreads();
+    if (threadIdx.x == 0 && p.work) {
+        __threadfence();
+        if (atomicAdd(p.work + 1, 1u) == gridDim.x - 1) {
+            atomicExch(p.work, 0u);
+            atomicExch(p.work + 1, 0u);
+        }
     }
 }
 

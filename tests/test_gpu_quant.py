@@ -176,6 +176,34 @@ def test_decode_quant_edge_cases(case, qdt, fmt):
     compare(got, _oracle_decode_quant(inp, pools), torch.float16)
 
 
+def test_decode_quant_repeated_launches_reuse_item_counters():
+    """The grouped-head E4M3 kernel claims items from a per-launch counter
+    that each launch returns to zero; launches take counters round-robin from
+    a pool of 4096.  5000 launches reuse every counter, and the last one's
+    output still matches the oracle (a counter left non-zero would make a
+    launch skip items)."""
+    from paged_kv_cache_251_gb300 import pa
+    inp, pools = _quant_case("reuse", 5, 16, 4, 128, 16, [700, 1, 2049, 33, 300], 0, torch.bfloat16, "e4m3",
+                             seed=13)
+    s = inp.shape
+    q = inp.q.cuda()
+    kp, vp = [t.cuda() for t in pools]
+    bt, cl = inp.block_tables.cuda(), inp.context_lens.cuda()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = torch.empty(q.shape, dtype=torch.float32, device="cuda")
+    ws = torch.empty(pa.pa_decode_workspace_size(s.num_seqs, s.num_heads, s.head_dim, s.block_size,
+                                                  bt.shape[1], 0, 64) // 4 + 4, dtype=torch.float32,
+                     device="cuda")
+    for i in range(5000):
+        if i == 4999:
+            out.fill_(float("nan"))
+        pa.pa_decode_quant(out, q, kp, vp, bt, cl, num_kv_heads=s.num_kv_heads, scale=1.0 / math.sqrt(s.head_dim),
+                           partition_size=64, workspace=ws, err_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    compare(out.cpu(), _oracle_decode_quant(inp, pools), torch.float16)
+
+
 @pytest.mark.parametrize("out_dt", ["f16", "bf16"])
 def test_decode_quant_low_precision_output(out_dt):
     inp, pools = _quant_case("lowout", 4, 8, 8, 128, 16, [300, 17, 600, 1], 0, torch.bfloat16, "e4m3", seed=3)
