@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <climits>
 #include <cmath>
 #include <cstdio>
@@ -258,9 +259,35 @@ pa_status plan_decode(int num_seqs, int num_heads, int head_dim, int block_size,
 
 void set_last_error_detail(const char *why) { g_detail = why; }
 
+// Item counters for the kernels that claim their items (DecodeParams::work):
+// zero when the module loads, and every launch returns its pair to zero.
+// Launches take pairs round-robin, so launches in flight at the same time (up
+// to kWorkSlots) never share one.
+constexpr int kWorkSlots = 4096;
+constexpr int kMaxDevices = 64;
+__device__ unsigned int g_work[2 * kWorkSlots];
+
+unsigned int *work_counter(int device) {
+    static unsigned int *base[kMaxDevices] = {};
+    static std::mutex mu;
+    static std::atomic<unsigned int> next{0};
+    if (device < 0 || device >= kMaxDevices)
+        return nullptr;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (!base[device]) {
+            void *ptr = nullptr;
+            if (cudaGetSymbolAddress(&ptr, g_work) != cudaSuccess)
+                return nullptr;
+            base[device] = static_cast<unsigned int *>(ptr);
+        }
+    }
+    return base[device] + 2 * (next.fetch_add(1u) % kWorkSlots);
+}
+
 // The partition reduce: a warp per row when there are rows enough to fill the
 // GPU and few partitions each, else a CTA per row.
-cudaError_t launch_reduce(DecodeParams &p, int head_dim, long long rows, cudaStream_t cs) {
+static cudaError_t launch_reduce(DecodeParams &p, int head_dim, long long rows, cudaStream_t cs) {
     int dev = 0, sms = 0;
     cudaError_t e = device_sms(&dev, &sms);
     if (e != cudaSuccess)
@@ -345,6 +372,10 @@ pa_status launch_decode_kernel(DecodeParams &p, int dtype, int head_dim, int G, 
         grid = items_max;
     if (grid < 1)
         grid = 1;
+    // the TMA-fed kernels claim their items from a per-launch counter
+    // (balances contexts of mixed lengths)
+    if (gqa_tc || mha)
+        p.work = work_counter(dev);
     void *args_gqa[] = {&p, &tmk, &tmv, &tmq};
     void *args_mha[] = {&p, &tmk, &tmv};
     void *args[] = {&p};
@@ -400,7 +431,7 @@ pa_status launch_decode_q8_kernel(DecodeParams &p, int cache_dtype, int head_dim
             grid = 1;
         // items are claimed from a per-launch counter (balances contexts of
         // mixed lengths); without one they go round-robin
-        p.work = q8t_work_counter(dev);
+        p.work = work_counter(dev);
         void *args[] = {&p, &tmk, &tmv, &tsk, &tsv};
         e = cudaLaunchKernel(tfn, dim3(static_cast<unsigned>(grid)), dim3(kQ8tThreads), args, smem, cs);
         if (e != cudaSuccess)
@@ -439,6 +470,7 @@ pa_status launch_decode_q8_kernel(DecodeParams &p, int cache_dtype, int head_dim
             grid = items_max;
         if (grid < 1)
             grid = 1;
+        p.work = work_counter(dev);  // items claimed from a per-launch counter
         void *args[] = {&p};
         e = cudaLaunchKernel(ffn, dim3(static_cast<unsigned>(grid)), dim3(kQ8fThreads), args, smem, cs);
         if (e != cudaSuccess)

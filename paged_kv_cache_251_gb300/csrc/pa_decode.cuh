@@ -68,6 +68,57 @@ struct DecodeParams {
     unsigned int *work = nullptr;
 };
 
+// Items of a persistent decode kernel, for its producer warp: from the
+// launch's counter (DecodeParams::work), each claimed one item ahead so the
+// atomic's latency overlaps the current item, or round-robin without one.
+// Claimed indices only grow, so the producer's forward scan over the contexts
+// still applies; every claimed index below the item count is processed.
+struct ItemClaim {
+    long long w = 0;        // the current item
+    unsigned int ahead = 0;  // the next one (lane 0)
+    __device__ void start(const DecodeParams &p) {
+        const int lane = threadIdx.x & 31;
+        if (p.work) {
+            unsigned int v = 0;
+            if (lane == 0)
+                v = atomicAdd(p.work, 1u);
+            w = __shfl_sync(0xffffffffu, v, 0);
+            if (lane == 0)
+                ahead = atomicAdd(p.work, 1u);
+        } else {
+            w = blockIdx.x;
+        }
+    }
+    __device__ void next(const DecodeParams &p) {
+        const int lane = threadIdx.x & 31;
+        if (p.work) {
+            w = __shfl_sync(0xffffffffu, ahead, 0);
+            if (lane == 0)
+                ahead = atomicAdd(p.work, 1u);
+        } else {
+            w += gridDim.x;
+        }
+    }
+    // the claims are complete before the CTA reports itself done
+    __device__ void finish(const DecodeParams &p) const {
+        if (p.work)
+            __threadfence();
+    }
+};
+
+// End of a launch with claimed items, once every thread of the CTA is past its
+// last claim (the caller synchronises the CTA first): the last CTA returns the
+// counter pair to zero for the next launch that uses it.
+__device__ inline void release_claims(const DecodeParams &p) {
+    if (threadIdx.x == 0 && p.work) {
+        __threadfence();
+        if (atomicAdd(p.work + 1, 1u) == gridDim.x - 1) {
+            atomicExch(p.work, 0u);
+            atomicExch(p.work + 1, 0u);
+        }
+    }
+}
+
 struct StageMeta {
     int slot;   // item slot (item counter mod stages)
     int lo;     // first attended row of the block

@@ -266,7 +266,10 @@ __device__ inline void gqa_producer(const DecodeParams &p, const CUtensorMap *tm
     bool ok = true;
     const long long hkv = p.num_kv_heads;
 
-    for (long long w = blockIdx.x, k = 0;; w += gridDim.x, ++k) {
+    ItemClaim claim;
+    claim.start(p);
+    for (long long k = 0;; claim.next(p), ++k) {
+        const long long w = claim.w;
         const long long f = w / hkv;
         const int kvh = static_cast<int>(w % hkv);
         int s = -1, part = 0, len = 0, start = 0, nparts = 1;
@@ -393,6 +396,7 @@ __device__ inline void gqa_producer(const DecodeParams &p, const CUtensorMap *tm
         for (uint32_t u = first; u < t; ++u)
             (void)mbar_wait_bounded(&full[u % S], (u / S) & 1u);
     }
+    claim.finish(p);
     __syncwarp();
 }
 
@@ -820,6 +824,8 @@ __global__ void __launch_bounds__(kGqaThreads, 1)
         if ((threadIdx.x & 31) == 0)
             mbar_arrive(reinterpret_cast<uint64_t *>(smem + L.done));
     }
+    __syncthreads();
+    release_claims(p);
 }
 
 }  // namespace pa

@@ -255,7 +255,10 @@ __device__ inline void mha_producer(const DecodeParams &p, const CUtensorMap *tm
     bool ok = true;
     const long long hkv = p.num_kv_heads;
 
-    for (long long w = blockIdx.x;; w += gridDim.x) {
+    ItemClaim claim;
+    claim.start(p);
+    for (;; claim.next(p)) {
+        const long long w = claim.w;
         const long long f = w / hkv;
         const int kvh = static_cast<int>(w % hkv);
         int s = -1, part = 0, len = 0, start = 0, nparts = 1;
@@ -378,6 +381,7 @@ __device__ inline void mha_producer(const DecodeParams &p, const CUtensorMap *tm
         for (uint32_t u = first; u < t; ++u)
             (void)mbar_wait_bounded(&full[u % S], (u / S) & 1u);
     }
+    claim.finish(p);
     __syncwarp();
 }
 
@@ -605,6 +609,8 @@ __global__ void __launch_bounds__(kMhaThreads) pa_decode_mha_kernel(const Decode
         mha_producer<T, D, BS>(p, &tmk, &tmv, smem, L);
     else
         mha_consumer<T, D, BS>(p, smem, L);
+    __syncthreads();
+    release_claims(p);
 }
 
 }  // namespace pa

@@ -240,7 +240,10 @@ __device__ inline void q8f_producer(const DecodeParams &p, char *smem, const Q8f
     bool ok = true;
     const int nquads = (p.num_kv_heads + kQ8fWarps - 1) / kQ8fWarps;
 
-    for (long long w = blockIdx.x;; w += gridDim.x) {
+    ItemClaim claim;
+    claim.start(p);
+    for (;; claim.next(p)) {
+        const long long w = claim.w;
         const long long f = w / nquads;
         const int kvh0 = static_cast<int>(w % nquads) * kQ8fWarps;
         int s = -1, part = 0, len = 0, start = 0, nparts = 1;
@@ -370,6 +373,7 @@ __device__ inline void q8f_producer(const DecodeParams &p, char *smem, const Q8f
         for (uint32_t u = first; u < t; ++u)
             (void)mbar_wait_bounded(&full[u % S], (u / S) & 1u);
     }
+    claim.finish(p);
     __syncwarp();
 }
 
@@ -729,6 +733,8 @@ __global__ void __launch_bounds__(kQ8fThreads, Q8fOccupancy<G>::kMinBlocks) pa_d
         q8f_producer<G, BS>(p, smem, L, qrow);
     else
         q8f_consumer<Fmt, G, BS>(p, smem, L, qrow);
+    __syncthreads();
+    release_claims(p);
 }
 
 }  // namespace pa

@@ -496,6 +496,8 @@ __device__ inline bool q8t_qconvert(const DecodeParams &p, char *smem, const Q8t
         if (it.s < 0)
             break;
     }
+    if (p.work)
+        __threadfence();  // the claims are complete before the CTA reports itself done
     return true;
 }
 
@@ -1025,13 +1027,7 @@ __global__ void __launch_bounds__(kQ8tThreads, 1)
     // The CTA has taken its last item: the last CTA to get here returns the
     // launch's counter to zero for the next launch that uses it.
     __syncthreads();
-    if (threadIdx.x == 0 && p.work) {
-        __threadfence();
-        if (atomicAdd(p.work + 1, 1u) == gridDim.x - 1) {
-            atomicExch(p.work, 0u);
-            atomicExch(p.work + 1, 0u);
-        }
-    }
+    release_claims(p);
 }
 
 }  // namespace pa
