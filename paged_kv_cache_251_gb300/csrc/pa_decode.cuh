@@ -591,33 +591,33 @@ constexpr int kReduceRows = kReduceThreads / 32;
 
 template <int D>
 __global__ void __launch_bounds__(kReduceThreads) pa_reduce_kernel(const DecodeParams p) {
+    // (the host takes this layout only for max_parts <= 32: lane q holds partition q)
     constexpr int kPer = D / 32;  // head_dim slice per lane (4 or 2)
+    constexpr int kBatch = 8;     // partitions whose slices are loaded before any is used
     const int lane = threadIdx.x & 31;
     const long long rowi = static_cast<long long>(blockIdx.x) * kReduceRows + (threadIdx.x >> 5);
     if (rowi >= static_cast<long long>(p.num_seqs) * p.num_heads)
         return;
     const int s = static_cast<int>(rowi / p.num_heads);
-    const SeqSpan sp = seq_span(ld_nc_i32(p.context_lens + s), p.max_len, p.window, p.block_size, p.bpp,
-                                p.start_tok ? ld_nc_i32(p.start_tok + s) : 0);
-    if (sp.nparts <= 1)
-        return;
-    const int np = sp.nparts;
     const long long base = rowi * p.max_parts;
-    const float2 *ml = reinterpret_cast<const float2 *>(p.part_ml + base * 2);
-
-    float M = -INFINITY;
-    for (int q = lane; q < np; q += 32)
-        M = fmaxf(M, ml[q].x);
+    // the context length and every partition's (m, l) in one round trip
+    const int len = ld_nc_i32(p.context_lens + s);
+    const int start = p.start_tok ? ld_nc_i32(p.start_tok + s) : 0;
+    float2 mine = make_float2(-INFINITY, 0.f);
+    if (lane < p.max_parts)
+        mine = reinterpret_cast<const float2 *>(p.part_ml + base * 2)[lane];
+    const SeqSpan sp = seq_span(len, p.max_len, p.window, p.block_size, p.bpp, start);
+    const int np = sp.nparts;
+    if (np <= 1)
+        return;
+    if (lane >= np)
+        mine = make_float2(-INFINITY, 0.f);  // stale entries of unused partitions
+    float M = mine.x;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1)
         M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    float den = 0.f;
-    if (M != -INFINITY)
-        for (int q = lane; q < np; q += 32) {
-            const float2 v = ml[q];
-            if (v.x != -INFINITY)
-                den = fmaf(v.y, exp2f(v.x - M), den);
-        }
+    const float sc = (M == -INFINITY || mine.x == -INFINITY) ? 0.f : exp2f(mine.x - M);
+    float den = mine.y * sc;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1)
         den += __shfl_xor_sync(0xffffffffu, den, o);
@@ -626,23 +626,31 @@ __global__ void __launch_bounds__(kReduceThreads) pa_reduce_kernel(const DecodeP
 #pragma unroll
     for (int i = 0; i < kPer; ++i)
         num[i] = 0.f;
-    if (M != -INFINITY) {
-        const float *a = p.part_acc + base * D + lane * kPer;
-#pragma unroll 4
-        for (int q = 0; q < np; ++q) {
-            const float mq = ml[q].x;
-            const float sc = mq == -INFINITY ? 0.f : exp2f(mq - M);
-            if (kPer == 4) {
-                const float4 v = *reinterpret_cast<const float4 *>(a + static_cast<long long>(q) * D);
-                num[0] = fmaf(v.x, sc, num[0]);
-                num[1] = fmaf(v.y, sc, num[1]);
-                num[2] = fmaf(v.z, sc, num[2]);
-                num[3] = fmaf(v.w, sc, num[3]);
+    const float *a = p.part_acc + base * D + lane * kPer;
+    for (int q0 = 0; q0 < np; q0 += kBatch) {
+        float v[kBatch][kPer];
+#pragma unroll
+        for (int j = 0; j < kBatch; ++j) {
+            if (q0 + j < np) {
+                if constexpr (kPer == 4) {
+                    const float4 x = *reinterpret_cast<const float4 *>(a + static_cast<long long>(q0 + j) * D);
+                    v[j][0] = x.x, v[j][1] = x.y, v[j][2] = x.z, v[j][3] = x.w;
+                } else {
+                    const float2 x = *reinterpret_cast<const float2 *>(a + static_cast<long long>(q0 + j) * D);
+                    v[j][0] = x.x, v[j][1] = x.y;
+                }
             } else {
-                const float2 v = *reinterpret_cast<const float2 *>(a + static_cast<long long>(q) * D);
-                num[0] = fmaf(v.x, sc, num[0]);
-                num[kPer > 1 ? 1 : 0] = fmaf(v.y, sc, num[kPer > 1 ? 1 : 0]);
+#pragma unroll
+                for (int i = 0; i < kPer; ++i)
+                    v[j][i] = 0.f;
             }
+        }
+#pragma unroll
+        for (int j = 0; j < kBatch; ++j) {
+            const float scj = __shfl_sync(0xffffffffu, sc, (q0 + j) & 31);
+#pragma unroll
+            for (int i = 0; i < kPer; ++i)
+                num[i] = fmaf(v[j][i], scj, num[i]);
         }
     }
 #pragma unroll
