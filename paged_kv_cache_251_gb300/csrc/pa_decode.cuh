@@ -106,6 +106,110 @@ struct ItemClaim {
     }
 };
 
+// The item order of the persistent kernels: (sequence, context partition)
+// pairs in sequence order, each taken with every kv head (or kv-head group).
+// Item f is found by a forward scan over context_lens, 32 sequences at a
+// time; a CTA's item indices only grow, so the scan never moves backwards.
+// (An order with every full partition first and the partial ones last was
+// measured: it shortens the end of a launch but puts the items with the
+// largest fixed cost per byte back to back, and was slower on the GQA batch.)
+struct ItemScan {
+    int chunk_base = 0;
+    long long chunk_prefix = 0;
+    int my_len = 0, my_start = 0, my_np = 0, my_incl = 0, chunk_total = 0;
+    bool chunk_ready = false;
+
+    // The sequence of item f (-1 past the last item), with its partition, its
+    // context length and its first attended token.  Warp-collective.
+    __device__ int find(const DecodeParams &p, int block_size, long long f, int &part, int &len, int &start) {
+        const int lane = threadIdx.x & 31;
+        for (;;) {
+            if (!chunk_ready) {
+                if (chunk_base >= p.num_seqs)
+                    return -1;
+                const int sq = chunk_base + lane;
+                my_len = sq < p.num_seqs ? ld_nc_i32(p.context_lens + sq) : 0;
+                if (sq < p.num_seqs && my_len > p.max_len && p.err)
+                    atomicOr(p.err, PA_DEVERR_BAD_LEN);
+                my_start = (sq < p.num_seqs && p.start_tok) ? ld_nc_i32(p.start_tok + sq) : 0;
+                my_np = sq < p.num_seqs ? seq_span(my_len, p.max_len, p.window, block_size, p.bpp, my_start).nparts : 0;
+                my_incl = my_np;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int v = __shfl_up_sync(0xffffffffu, my_incl, o);
+                    if (lane >= o)
+                        my_incl += v;
+                }
+                chunk_total = __shfl_sync(0xffffffffu, my_incl, 31);
+                chunk_ready = true;
+            }
+            if (f < chunk_prefix + chunk_total) {
+                const unsigned hit = __ballot_sync(0xffffffffu, chunk_prefix + my_incl > f);
+                const int j = __ffs(hit) - 1;
+                const int incl_j = __shfl_sync(0xffffffffu, my_incl, j);
+                const int np_j = __shfl_sync(0xffffffffu, my_np, j);
+                len = __shfl_sync(0xffffffffu, my_len, j);
+                start = __shfl_sync(0xffffffffu, my_start, j);
+                part = static_cast<int>(f - (chunk_prefix + incl_j - np_j));
+                return chunk_base + j;
+            }
+            chunk_prefix += chunk_total;
+            chunk_base += 32;
+            chunk_ready = false;
+        }
+    }
+};
+
+// A producer's next item, found and its block-table slice loaded into
+// registers one item ahead: the scan's and the table's memory latency then
+// overlaps the current item's copies instead of stalling the stage ring.
+struct NextItem {
+    int s, part, len, start, head;  // head: kv head, or kv-head group, of the item
+    SeqSpan sp;
+    int blk_lo, nb;
+    int tb[kMaxBpp / 32];  // table entry lane + 32 i of the slice (checked when stored)
+};
+
+// Item w of the order (w / groups, head w % groups); warp-collective.
+__device__ inline void prepare_item(const DecodeParams &p, int block_size, ItemScan &scan, long long w,
+                                    long long groups, NextItem &n) {
+    const int lane = threadIdx.x & 31;
+    n.head = static_cast<int>(w % groups);
+    n.part = n.len = n.start = 0;
+    n.s = scan.find(p, block_size, w / groups, n.part, n.len, n.start);
+    n.blk_lo = n.nb = 0;
+    if (n.s < 0)
+        return;
+    n.sp = seq_span(n.len, p.max_len, p.window, block_size, p.bpp, n.start);
+    n.blk_lo = n.sp.b0 + n.part * p.bpp;
+    n.nb = max(0, min(p.bpp, n.sp.nblk - n.part * p.bpp));
+    const int32_t *row = p.block_tables + static_cast<long long>(n.s) * p.max_blocks_per_seq + n.blk_lo;
+#pragma unroll
+    for (int i = 0; i < kMaxBpp / 32; ++i) {
+        const int j = lane + 32 * i;
+        n.tb[i] = j < n.nb ? ld_nc_i32(row + j) : -1;
+    }
+}
+
+// The item's table slice into shared memory; entries outside the pool become
+// -1 and are flagged (PA_DEVERR_BAD_BLOCK).
+__device__ inline void store_table(const DecodeParams &p, const NextItem &n, int32_t *tbl) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int i = 0; i < kMaxBpp / 32; ++i) {
+        const int j = lane + 32 * i;
+        if (j < n.nb) {
+            int pb = n.tb[i];
+            if (pb < 0 || pb >= p.num_blocks) {
+                pb = -1;
+                if (p.err)
+                    atomicOr(p.err, PA_DEVERR_BAD_BLOCK);
+            }
+            tbl[j] = pb;
+        }
+    }
+}
+
 // End of a launch with claimed items, once every thread of the CTA is past its
 // last claim (the caller synchronises the CTA first): the last CTA returns the
 // counter pair to zero for the next launch that uses it.

@@ -258,56 +258,17 @@ __device__ inline void gqa_producer(const DecodeParams &p, const CUtensorMap *tm
         prefetch_tensormap(tmv);
         prefetch_tensormap(tmq);
     }
-    int chunk_base = 0;
-    long long chunk_prefix = 0;
-    int my_len = 0, my_start = 0, my_np = 0, my_incl = 0, chunk_total = 0;
-    bool chunk_ready = false;
+    ItemScan scan;
     uint32_t t = 0;
     bool ok = true;
     const long long hkv = p.num_kv_heads;
 
     ItemClaim claim;
     claim.start(p);
-    for (long long k = 0;; claim.next(p), ++k) {
-        const long long w = claim.w;
-        const long long f = w / hkv;
-        const int kvh = static_cast<int>(w % hkv);
-        int s = -1, part = 0, len = 0, start = 0, nparts = 1;
-        for (;;) {
-            if (!chunk_ready) {
-                if (chunk_base >= p.num_seqs)
-                    break;
-                const int sq = chunk_base + lane;
-                my_len = sq < p.num_seqs ? ld_nc_i32(p.context_lens + sq) : 0;
-                if (sq < p.num_seqs && my_len > p.max_len && p.err)
-                    atomicOr(p.err, PA_DEVERR_BAD_LEN);
-                my_start = (sq < p.num_seqs && p.start_tok) ? ld_nc_i32(p.start_tok + sq) : 0;
-                my_np = sq < p.num_seqs ? seq_span(my_len, p.max_len, p.window, BS, p.bpp, my_start).nparts : 0;
-                my_incl = my_np;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const int v = __shfl_up_sync(0xffffffffu, my_incl, o);
-                    if (lane >= o)
-                        my_incl += v;
-                }
-                chunk_total = __shfl_sync(0xffffffffu, my_incl, 31);
-                chunk_ready = true;
-            }
-            if (f < chunk_prefix + chunk_total) {
-                const unsigned hit = __ballot_sync(0xffffffffu, chunk_prefix + my_incl > f);
-                const int j = __ffs(hit) - 1;
-                s = chunk_base + j;
-                const int incl_j = __shfl_sync(0xffffffffu, my_incl, j);
-                nparts = __shfl_sync(0xffffffffu, my_np, j);
-                len = __shfl_sync(0xffffffffu, my_len, j);
-                start = __shfl_sync(0xffffffffu, my_start, j);
-                part = static_cast<int>(f - (chunk_prefix + incl_j - nparts));
-                break;
-            }
-            chunk_prefix += chunk_total;
-            chunk_base += 32;
-            chunk_ready = false;
-        }
+    NextItem cur, nxt;
+    prepare_item(p, BS, scan, claim.w, hkv, cur);
+    for (long long k = 0;; ++k) {
+        const int s = cur.s, kvh = cur.head, part = cur.part;
         const int slot = static_cast<int>(k % kGqaItemSlots);
         if (!mbar_wait_bounded(&iempty[slot], static_cast<uint32_t>((k / kGqaItemSlots) & 1) ^ 1u)) {
             ok = false;
@@ -321,9 +282,9 @@ __device__ inline void gqa_producer(const DecodeParams &p, const CUtensorMap *tm
             __syncwarp();
             break;
         }
-        const SeqSpan sp = seq_span(len, p.max_len, p.window, BS, p.bpp, start);
-        const int blk_lo = sp.b0 + part * p.bpp;
-        const int nb = max(0, min(p.bpp, sp.nblk - part * p.bpp));
+        const SeqSpan sp = cur.sp;
+        const int blk_lo = cur.blk_lo;
+        const int nb = cur.nb;
         const int ntiles = (nb + C::kBpt - 1) / C::kBpt;
         if (lane == 0) {
             MhaItem it;
@@ -348,17 +309,9 @@ __device__ inline void gqa_producer(const DecodeParams &p, const CUtensorMap *tm
                 mbar_arrive(&ifull[slot]);
             }
         }
-        const int32_t *row = p.block_tables + static_cast<long long>(s) * p.max_blocks_per_seq + blk_lo;
-        for (int j = lane; j < nb; j += 32) {
-            int pb = ld_nc_i32(row + j);
-            if (pb < 0 || pb >= p.num_blocks) {
-                pb = -1;
-                if (p.err)
-                    atomicOr(p.err, PA_DEVERR_BAD_BLOCK);
-            }
-            tbl[j] = pb;
-        }
+        store_table(p, cur, tbl);
         __syncwarp();
+        bool have_next = false;
         for (int ti = 0; ti < ntiles; ++ti, ++t) {
             const int stage = static_cast<int>(t % S);
             if (!mbar_wait_bounded(&empty[stage], ((t / S) & 1u) ^ 1u)) {
@@ -384,9 +337,19 @@ __device__ inline void gqa_producer(const DecodeParams &p, const CUtensorMap *tm
                 tma_load_5d(dk + C::kTile, tmv, z, &full[stage], policy);
             }
             __syncwarp();
+            if (ti == 0) {  // the next item, while this one's first copies are in flight
+                claim.next(p);
+                prepare_item(p, BS, scan, claim.w, hkv, nxt);
+                have_next = true;
+            }
         }
         if (!ok)
             break;
+        if (!have_next) {
+            claim.next(p);
+            prepare_item(p, BS, scan, claim.w, hkv, nxt);
+        }
+        cur = nxt;
     }
     if (!ok && lane == 0) {
         // a wait gave up: flag it, then wait (bounded) for our copies in flight

@@ -246,10 +246,7 @@ __device__ inline void mha_producer(const DecodeParams &p, const CUtensorMap *tm
         prefetch_tensormap(tmv);
     }
 
-    int chunk_base = 0;
-    long long chunk_prefix = 0;
-    int my_len = 0, my_start = 0, my_np = 0, my_incl = 0, chunk_total = 0;
-    bool chunk_ready = false;
+    ItemScan scan;
     uint32_t t = 0;  // stages issued
     int k = 0;       // items issued
     bool ok = true;
@@ -261,42 +258,8 @@ __device__ inline void mha_producer(const DecodeParams &p, const CUtensorMap *tm
         const long long w = claim.w;
         const long long f = w / hkv;
         const int kvh = static_cast<int>(w % hkv);
-        int s = -1, part = 0, len = 0, start = 0, nparts = 1;
-        for (;;) {
-            if (!chunk_ready) {
-                if (chunk_base >= p.num_seqs)
-                    break;
-                const int sq = chunk_base + lane;
-                my_len = sq < p.num_seqs ? ld_nc_i32(p.context_lens + sq) : 0;
-                if (sq < p.num_seqs && my_len > p.max_len && p.err)
-                    atomicOr(p.err, PA_DEVERR_BAD_LEN);
-                my_start = (sq < p.num_seqs && p.start_tok) ? ld_nc_i32(p.start_tok + sq) : 0;
-                my_np = sq < p.num_seqs ? seq_span(my_len, p.max_len, p.window, BS, p.bpp, my_start).nparts : 0;
-                my_incl = my_np;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const int v = __shfl_up_sync(0xffffffffu, my_incl, o);
-                    if (lane >= o)
-                        my_incl += v;
-                }
-                chunk_total = __shfl_sync(0xffffffffu, my_incl, 31);
-                chunk_ready = true;
-            }
-            if (f < chunk_prefix + chunk_total) {
-                const unsigned hit = __ballot_sync(0xffffffffu, chunk_prefix + my_incl > f);
-                const int j = __ffs(hit) - 1;
-                s = chunk_base + j;
-                const int incl_j = __shfl_sync(0xffffffffu, my_incl, j);
-                nparts = __shfl_sync(0xffffffffu, my_np, j);
-                len = __shfl_sync(0xffffffffu, my_len, j);
-                start = __shfl_sync(0xffffffffu, my_start, j);
-                part = static_cast<int>(f - (chunk_prefix + incl_j - nparts));
-                break;
-            }
-            chunk_prefix += chunk_total;
-            chunk_base += 32;
-            chunk_ready = false;
-        }
+        int part = 0, len = 0, start = 0;
+        const int s = scan.find(p, BS, f, part, len, start);
 
         const int slot = k % kItemSlots;
         if (!mbar_wait_bounded(&iempty[slot], ((k / kItemSlots) & 1) ^ 1)) {

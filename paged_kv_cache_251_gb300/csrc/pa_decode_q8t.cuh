@@ -223,58 +223,19 @@ __device__ inline void q8t_pow2(float a, float &up, float &down) {
 
 // ---------------------------------------------------------------------------
 
-// The walk over a CTA's items: item w of the flattened (sequence, partition,
-// kv-head group) order, found by a scan over context_lens that only moves
-// forward (w increasing).  The producer and the query converter each run one.
+// The walk over a CTA's items: item w is (item w / groups of the common order
+// (ItemScan), kv-head group w % groups).  The producer and the query converter
+// each run one.
 template <int BS> struct Q8tScan {
-    int chunk_base = 0;
-    long long chunk_prefix = 0;
-    int my_len = 0, my_start = 0, my_np = 0, my_incl = 0, chunk_total = 0;
-    bool chunk_ready = false;
+    ItemScan scan;
 
     struct Found {
         int s, part, len, start, kvh0;
     };
-    __device__ Found find(const DecodeParams &p, long long w, bool flag_errors) {
-        const int lane = threadIdx.x & 31;
+    __device__ Found find(const DecodeParams &p, long long w, bool) {
         const long long nquads = p.num_kv_heads / kQ8tHeads;
         Found r{-1, 0, 0, 0, static_cast<int>(w % nquads) * kQ8tHeads};
-        const long long f = w / nquads;
-        for (;;) {
-            if (!chunk_ready) {
-                if (chunk_base >= p.num_seqs)
-                    break;
-                const int sq = chunk_base + lane;
-                my_len = sq < p.num_seqs ? ld_nc_i32(p.context_lens + sq) : 0;
-                if (flag_errors && sq < p.num_seqs && my_len > p.max_len && p.err)
-                    atomicOr(p.err, PA_DEVERR_BAD_LEN);
-                my_start = (sq < p.num_seqs && p.start_tok) ? ld_nc_i32(p.start_tok + sq) : 0;
-                my_np = sq < p.num_seqs ? seq_span(my_len, p.max_len, p.window, BS, p.bpp, my_start).nparts : 0;
-                my_incl = my_np;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const int v = __shfl_up_sync(0xffffffffu, my_incl, o);
-                    if (lane >= o)
-                        my_incl += v;
-                }
-                chunk_total = __shfl_sync(0xffffffffu, my_incl, 31);
-                chunk_ready = true;
-            }
-            if (f < chunk_prefix + chunk_total) {
-                const unsigned hit = __ballot_sync(0xffffffffu, chunk_prefix + my_incl > f);
-                const int j = __ffs(hit) - 1;
-                r.s = chunk_base + j;
-                const int incl_j = __shfl_sync(0xffffffffu, my_incl, j);
-                const int nparts = __shfl_sync(0xffffffffu, my_np, j);
-                r.len = __shfl_sync(0xffffffffu, my_len, j);
-                r.start = __shfl_sync(0xffffffffu, my_start, j);
-                r.part = static_cast<int>(f - (chunk_prefix + incl_j - nparts));
-                break;
-            }
-            chunk_prefix += chunk_total;
-            chunk_base += 32;
-            chunk_ready = false;
-        }
+        r.s = scan.find(p, BS, w / nquads, r.part, r.len, r.start);
         return r;
     }
     // the item's span and blocks
