@@ -295,8 +295,8 @@ static cudaError_t launch_reduce(DecodeParams &p, int head_dim, long long rows, 
     const bool wide = rows < 8LL * sms || p.max_parts > 32;
     void *args[] = {&p};
     const long long grid = wide ? rows : (rows + kReduceRows - 1) / kReduceRows;
-    return cudaLaunchKernel(reduce_kernel(head_dim, wide), dim3(static_cast<unsigned>(grid)), dim3(kReduceThreads),
-                            args, 0, cs);
+    return cudaLaunchKernel(reduce_kernel(head_dim, wide), dim3(static_cast<unsigned>(grid)),
+                            dim3(wide ? kReduceWideThreads : kReduceThreads), args, 0, cs);
 }
 
 pa_status launch_decode_kernel(DecodeParams &p, int dtype, int head_dim, int G, cudaStream_t cs) {

@@ -687,10 +687,12 @@ __global__ void __launch_bounds__(kDecodeThreads) pa_decode_kernel(const DecodeP
 // pairs for the row max and the denominator, then each lane sums its head_dim
 // slice over the partitions, the loads of several partitions in flight), for
 // many rows of few partitions; pa_reduce_wide_kernel, one CTA per row (the
-// warps take partitions round-robin and sum their slices through shared
-// memory), for few rows of many partitions.  Single-partition rows were
-// written by the decode kernel and are left alone.
+// warps take partitions round-robin, each merges its own with a running max,
+// and the warps' results are merged through shared memory), for few rows of
+// many partitions.  Single-partition rows were written by the decode kernel
+// and are left alone.
 constexpr int kReduceThreads = 128;
+constexpr int kReduceWideThreads = 256;
 constexpr int kReduceRows = kReduceThreads / 32;
 
 template <int D>
@@ -763,90 +765,111 @@ __global__ void __launch_bounds__(kReduceThreads) pa_reduce_kernel(const DecodeP
 }
 
 template <int D>
-__global__ void __launch_bounds__(kReduceThreads) pa_reduce_wide_kernel(const DecodeParams p) {
-    constexpr int kWarps = kReduceThreads / 32;
+__global__ void __launch_bounds__(kReduceWideThreads) pa_reduce_wide_kernel(const DecodeParams p) {
+    constexpr int kWarps = kReduceWideThreads / 32;
     constexpr int kPer = D / 32;  // head_dim slice per lane (4 or 2)
-    __shared__ float red[kWarps];
+    constexpr int kBatch = 8;     // partitions of one warp whose slices are loaded before any is used
+    constexpr int kStep = kWarps * kBatch;
+    __shared__ float wmax[kWarps], wden[kWarps];
     __shared__ float accs[kWarps][D];
     const long long rowi = blockIdx.x;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int s = static_cast<int>(rowi / p.num_heads);
-    const SeqSpan sp = seq_span(p.context_lens[s], p.max_len, p.window, p.block_size, p.bpp,
-                                p.start_tok ? p.start_tok[s] : 0);
-    if (sp.nparts <= 1)
-        return;
-    const int np = sp.nparts;
     const long long base = rowi * p.max_parts;
     const float2 *ml = reinterpret_cast<const float2 *>(p.part_ml + base * 2);
+    const float *acc = p.part_acc + base * D + lane * kPer;
 
-    // row max over the partitions' running maxima
-    float M = -INFINITY;
-    for (int q = tid; q < np; q += kReduceThreads)
-        M = fmaxf(M, ml[q].x);
+    // warp w takes partitions w, w + kWarps, ...; a batch is kBatch of them
+    float2 m[kBatch];
+    float v[kBatch][kPer];
+    auto load = [&](int q0, int lim) {
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1)
-        M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    if (lane == 0)
-        red[warp] = M;
-    __syncthreads();
-    M = red[0];
+        for (int j = 0; j < kBatch; ++j) {
+            const int q = q0 + warp + kWarps * j;
+            m[j] = make_float2(-INFINITY, 0.f);
 #pragma unroll
-    for (int w = 1; w < kWarps; ++w)
-        M = fmaxf(M, red[w]);
-    __syncthreads();
-
-    // denominator
-    float den = 0.f;
-    if (M != -INFINITY)
-        for (int q = tid; q < np; q += kReduceThreads) {
-            const float2 v = ml[q];
-            if (v.x != -INFINITY)
-                den = fmaf(v.y, exp2f(v.x - M), den);
-        }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1)
-        den += __shfl_xor_sync(0xffffffffu, den, o);
-    if (lane == 0)
-        red[warp] = den;
-
-    // numerator: warp w takes partitions w, w + kWarps, ...
-    float num[kPer];
-#pragma unroll
-    for (int i = 0; i < kPer; ++i)
-        num[i] = 0.f;
-    if (M != -INFINITY) {
-#pragma unroll 4
-        for (int q = warp; q < np; q += kWarps) {
-            const float mq = ml[q].x;
-            const float sc = mq == -INFINITY ? 0.f : exp2f(mq - M);
-            const float *a = p.part_acc + (base + q) * D + lane * kPer;
-            if (kPer == 4) {
-                const float4 v = *reinterpret_cast<const float4 *>(a);
-                num[0] = fmaf(v.x, sc, num[0]);
-                num[1] = fmaf(v.y, sc, num[1]);
-                num[2] = fmaf(v.z, sc, num[2]);
-                num[3] = fmaf(v.w, sc, num[3]);
-            } else {
-#pragma unroll
-                for (int i = 0; i < kPer; ++i)
-                    num[i] = fmaf(a[i], sc, num[i]);
+            for (int i = 0; i < kPer; ++i)
+                v[j][i] = 0.f;
+            if (q < lim) {
+                m[j] = ml[q];
+                if constexpr (kPer == 4) {
+                    const float4 x = *reinterpret_cast<const float4 *>(acc + static_cast<long long>(q) * D);
+                    v[j][0] = x.x, v[j][1] = x.y, v[j][2] = x.z, v[j][3] = x.w;
+                } else {
+                    const float2 x = *reinterpret_cast<const float2 *>(acc + static_cast<long long>(q) * D);
+                    v[j][0] = x.x, v[j][1] = x.y;
+                }
             }
         }
+    };
+    // the context length and the first batch in one round trip: the batch is
+    // bounded by the workspace's partitions per row, entries past the row's
+    // own partitions are dropped below
+    const int len = ld_nc_i32(p.context_lens + s);
+    const int start = p.start_tok ? ld_nc_i32(p.start_tok + s) : 0;
+    load(0, p.max_parts);
+    const SeqSpan sp = seq_span(len, p.max_len, p.window, p.block_size, p.bpp, start);
+    const int np = sp.nparts;
+    if (np <= 1)
+        return;
+
+    // this warp's running max, denominator and numerator slice
+    float mw = -INFINITY, dw = 0.f, nw[kPer];
+#pragma unroll
+    for (int i = 0; i < kPer; ++i)
+        nw[i] = 0.f;
+    for (int q0 = 0;; q0 += kStep) {
+        float bm = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < kBatch; ++j)
+            if (q0 + warp + kWarps * j < np)
+                bm = fmaxf(bm, m[j].x);
+        const float mn = fmaxf(mw, bm);
+        if (mn != -INFINITY) {
+            const float a = mw == -INFINITY ? 0.f : exp2f(mw - mn);
+            dw *= a;
+#pragma unroll
+            for (int i = 0; i < kPer; ++i)
+                nw[i] *= a;
+#pragma unroll
+            for (int j = 0; j < kBatch; ++j) {
+                if (q0 + warp + kWarps * j < np && m[j].x != -INFINITY) {
+                    const float sc = exp2f(m[j].x - mn);
+                    dw = fmaf(m[j].y, sc, dw);
+#pragma unroll
+                    for (int i = 0; i < kPer; ++i)
+                        nw[i] = fmaf(v[j][i], sc, nw[i]);
+                }
+            }
+            mw = mn;
+        }
+        if (q0 + kStep >= np)
+            break;
+        load(q0 + kStep, np);
+    }
+    if (lane == 0) {
+        wmax[warp] = mw;
+        wden[warp] = dw;
     }
 #pragma unroll
     for (int i = 0; i < kPer; ++i)
-        accs[warp][lane * kPer + i] = num[i];
+        accs[warp][lane * kPer + i] = nw[i];
     __syncthreads();
-    float dsum = 0.f;
+    float M = -INFINITY;
 #pragma unroll
     for (int w = 0; w < kWarps; ++w)
-        dsum += red[w];
-    for (int d = tid; d < D; d += kReduceThreads) {
-        float v = 0.f;
+        M = fmaxf(M, wmax[w]);
+    for (int d = tid; d < D; d += kReduceWideThreads) {
+        float num = 0.f, den = 0.f;
+        if (M != -INFINITY) {
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w)
-            v += accs[w][d];
-        store_out(p.out, p.out_dtype, rowi * D + d, dsum > 0.f ? v / dsum : 0.f);
+            for (int w = 0; w < kWarps; ++w) {
+                const float sc = wmax[w] == -INFINITY ? 0.f : exp2f(wmax[w] - M);
+                num = fmaf(accs[w][d], sc, num);
+                den = fmaf(wden[w], sc, den);
+            }
+        }
+        store_out(p.out, p.out_dtype, rowi * D + d, den > 0.f ? num / den : 0.f);
     }
 }
 

@@ -15,13 +15,21 @@
 // (hi = round(p), lo = round(p - hi)) that occupy the N columns the heads
 // leave free, so the PV product keeps about 16 mantissa bits of p.
 //
-// Warp roles (192 threads, one CTA per SM, persistent over items
+// Warp roles (224 threads, one CTA per SM, persistent over items
 // (sequence, kv head, partition)):
-//   warp 0      producer: item ring (+ the item's G query rows by TMA),
-//               block-table slice into shared memory (range-checked), K and V
-//               of each 128-token tile by 5-D TMA tensor copies (one per block
-//               and operand, issued by one lane per block; 128-byte swizzle)
-//               into a ring of stages;
+//   warp 0      K producer: item ring (+ the item's G query rows by TMA),
+//               block-table slice into shared memory (range-checked), K of
+//               each 128-token tile by 5-D TMA tensor copies (one per block,
+//               issued by one lane per block; 128-byte swizzle) into the K
+//               half of a ring of stages, and a record per stage of the
+//               tile's blocks for the V producer;
+//   warp 6      V producer: V of each tile into the V half of its stage, from
+//               the record.  The two halves are released separately: K once
+//               S of its tile finished (and the softmax warps read the
+//               tile's block mask), V once P V finished.  A stage's K half
+//               is thus refilled while its V is still in use, which keeps
+//               more of the ring in flight: the kernel is bound by the bytes
+//               each SM keeps in flight to HBM;
 //   warp 1      tensor-memory allocation and the single thread that issues
 //               the MMAs and their commits; tile g's S = K . Q^T is issued
 //               before tile g-1's P V, so scoring overlaps the P V product;
@@ -41,7 +49,7 @@
 
 namespace pa {
 
-constexpr int kGqaThreads = 6 * 32;
+constexpr int kGqaThreads = 7 * 32;
 constexpr int kGqaSmWarps = 4;    // softmax / epilogue warps
 constexpr int kGqaItemSlots = 4;
 constexpr int kTileTokens = 128;  // MMA M
@@ -64,16 +72,30 @@ template <typename T, int BS, int G> struct GqaCfg {
 };
 
 struct GqaLayout {
-    uint32_t full, empty, ifull, iempty, sfull, sfree, pfull, ofull, ofree, xfull, done, fin;
-    uint32_t meta, items, tmem, table, xbuf, abuf, qbuf, pbuf, stages, total;
+    uint32_t kfull, vfull, kempty, vempty, zfull, zfree, ifull, iempty, sfull, sfree, pfull, ofull, ofree, xfull, done,
+        fin;
+    uint32_t meta, zmask, zid, items, tmem, table, xbuf, abuf, qbuf, pbuf, stages, total;
 };
+
+// The V producer's record of a stage: the valid-block mask of its tile (or
+// this value: no more tiles) and the blocks' tensor-map tile indices.
+constexpr uint32_t kGqaEndRecord = 0xFFFFFFFFu;
+constexpr int kGqaMaxBpt = 16;  // blocks per 128-token tile at block size 8
 
 __host__ __device__ inline GqaLayout gqa_smem_layout(int S) {
     GqaLayout L;
     uint32_t off = 0;
-    L.full = off;
+    L.kfull = off;
     off += 8 * S;
-    L.empty = off;
+    L.vfull = off;
+    off += 8 * S;
+    L.kempty = off;
+    off += 8 * S;
+    L.vempty = off;
+    off += 8 * S;
+    L.zfull = off;
+    off += 8 * S;
+    L.zfree = off;
     off += 8 * S;
     L.ifull = off;
     off += 8 * kGqaItemSlots;
@@ -97,6 +119,10 @@ __host__ __device__ inline GqaLayout gqa_smem_layout(int S) {
     off += 8;
     L.meta = off;
     off += 4 * S;
+    L.zmask = off;
+    off += 4 * S;
+    L.zid = off;
+    off += 4 * S * kGqaMaxBpt;
     L.items = align_up(off, 16);
     off = L.items + sizeof(MhaItem) * kGqaItemSlots;
     L.tmem = off;
@@ -243,11 +269,15 @@ __device__ inline void gqa_producer(const DecodeParams &p, const CUtensorMap *tm
     using C = GqaCfg<T, BS, G>;
     const int lane = threadIdx.x & 31;
     const int S = p.stages;
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.full);
-    uint64_t *empty = reinterpret_cast<uint64_t *>(smem + L.empty);
+    uint64_t *kfull = reinterpret_cast<uint64_t *>(smem + L.kfull);
+    uint64_t *kempty = reinterpret_cast<uint64_t *>(smem + L.kempty);
+    uint64_t *zfull = reinterpret_cast<uint64_t *>(smem + L.zfull);
+    uint64_t *zfree = reinterpret_cast<uint64_t *>(smem + L.zfree);
     uint64_t *ifull = reinterpret_cast<uint64_t *>(smem + L.ifull);
     uint64_t *iempty = reinterpret_cast<uint64_t *>(smem + L.iempty);
     uint32_t *meta = reinterpret_cast<uint32_t *>(smem + L.meta);
+    uint32_t *zmask = reinterpret_cast<uint32_t *>(smem + L.zmask);
+    int32_t *zid = reinterpret_cast<int32_t *>(smem + L.zid);
     MhaItem *items = reinterpret_cast<MhaItem *>(smem + L.items);
     int32_t *tbl = reinterpret_cast<int32_t *>(smem + L.table);
     char *qbuf = smem + L.qbuf;
@@ -255,7 +285,6 @@ __device__ inline void gqa_producer(const DecodeParams &p, const CUtensorMap *tm
     const uint64_t policy = policy_evict_first();
     if (lane == 0) {
         prefetch_tensormap(tmk);
-        prefetch_tensormap(tmv);
         prefetch_tensormap(tmq);
     }
     ItemScan scan;
@@ -314,28 +343,35 @@ __device__ inline void gqa_producer(const DecodeParams &p, const CUtensorMap *tm
         bool have_next = false;
         for (int ti = 0; ti < ntiles; ++ti, ++t) {
             const int stage = static_cast<int>(t % S);
-            if (!mbar_wait_bounded(&empty[stage], ((t / S) & 1u) ^ 1u)) {
+            // the K half is free (S of tile t - S finished, the softmax warps
+            // read its block mask) and the V producer took tile t - S's record
+            if (!mbar_wait_bounded(&kempty[stage], ((t / S) & 1u) ^ 1u) ||
+                !mbar_wait_bounded(&zfree[stage], ((t / S) & 1u) ^ 1u)) {
                 ok = false;
                 break;
             }
-            // lane j issues block j of the tile: one copy for K, one for V
+            // lane j issues the K copy of block j of the tile and leaves its
+            // tile index for the V producer
             const int bj = ti * C::kBpt + lane;
             const bool mine = lane < C::kBpt && bj < nb && tbl[bj] >= 0;
             const uint32_t mask = __ballot_sync(0xffffffffu, mine);
+            const int z = mine ? tbl[bj] * p.num_kv_heads + kvh : 0;
+            if (lane < C::kBpt)
+                zid[stage * kGqaMaxBpt + lane] = z;
             if (lane == 0) {
                 meta[stage] = mask;
+                zmask[stage] = mask;
                 if (mask)
-                    mbar_arrive_expect_tx(&full[stage], __popc(mask) * 2 * C::kBlockBytes);
+                    mbar_arrive_expect_tx(&kfull[stage], __popc(mask) * C::kBlockBytes);
                 else
-                    mbar_arrive(&full[stage]);
+                    mbar_arrive(&kfull[stage]);
             }
             __syncwarp();
-            if (mine) {
-                char *dk = stage_buf + static_cast<size_t>(stage) * 2 * C::kTile + lane * C::kBlockBytes;
-                const int z = tbl[bj] * p.num_kv_heads + kvh;
-                tma_load_5d(dk, tmk, z, &full[stage], policy);
-                tma_load_5d(dk + C::kTile, tmv, z, &full[stage], policy);
-            }
+            if (mine)
+                tma_load_5d(stage_buf + static_cast<size_t>(stage) * 2 * C::kTile + lane * C::kBlockBytes, tmk, z,
+                            &kfull[stage], policy);
+            if (lane == 0)
+                mbar_arrive(&zfull[stage]);
             __syncwarp();
             if (ti == 0) {  // the next item, while this one's first copies are in flight
                 claim.next(p);
@@ -351,15 +387,84 @@ __device__ inline void gqa_producer(const DecodeParams &p, const CUtensorMap *tm
         }
         cur = nxt;
     }
+    // no more tiles for the V producer (after a failed wait too, so that it
+    // stops without waiting out its own limit)
+    if (lane == 0) {
+        const int stage = static_cast<int>(t % S);
+        if (!mbar_wait_bounded(&zfree[stage], ((t / S) & 1u) ^ 1u))
+            ok = false;
+        zmask[stage] = kGqaEndRecord;
+        mbar_arrive(&zfull[stage]);
+    }
     if (!ok && lane == 0) {
         // a wait gave up: flag it, then wait (bounded) for our copies in flight
         if (p.err)
             atomicOr(p.err, PA_DEVERR_TIMEOUT);
         const uint32_t first = t > static_cast<uint32_t>(S) ? t - S : 0;
         for (uint32_t u = first; u < t; ++u)
-            (void)mbar_wait_bounded(&full[u % S], (u / S) & 1u);
+            (void)mbar_wait_bounded(&kfull[u % S], (u / S) & 1u);
     }
     claim.finish(p);
+    __syncwarp();
+}
+
+// The V producer (warp 6): for each tile, in order, the K producer's record
+// (valid-block mask and tile indices), handed back as soon as it is read,
+// then the V copies into the V half of the tile's stage once P V of tile
+// t - S finished.
+template <typename T, int BS, int G>
+__device__ inline void gqa_vproducer(const DecodeParams &p, const CUtensorMap *tmv, char *smem, const GqaLayout &L) {
+    using C = GqaCfg<T, BS, G>;
+    const int lane = threadIdx.x & 31;
+    const int S = p.stages;
+    uint64_t *vfull = reinterpret_cast<uint64_t *>(smem + L.vfull);
+    uint64_t *vempty = reinterpret_cast<uint64_t *>(smem + L.vempty);
+    uint64_t *zfull = reinterpret_cast<uint64_t *>(smem + L.zfull);
+    uint64_t *zfree = reinterpret_cast<uint64_t *>(smem + L.zfree);
+    const uint32_t *zmask = reinterpret_cast<const uint32_t *>(smem + L.zmask);
+    const int32_t *zid = reinterpret_cast<const int32_t *>(smem + L.zid);
+    char *stage_buf = smem + L.stages;
+    const uint64_t policy = policy_evict_first();
+    if (lane == 0)
+        prefetch_tensormap(tmv);
+    bool ok = true;
+    uint32_t t = 0;
+    for (;; ++t) {
+        const int stage = static_cast<int>(t % S);
+        if (!mbar_wait_bounded(&zfull[stage], (t / S) & 1u)) {
+            ok = false;
+            break;
+        }
+        const uint32_t mask = zmask[stage];
+        if (mask == kGqaEndRecord)
+            break;
+        const int z = lane < C::kBpt ? zid[stage * kGqaMaxBpt + lane] : 0;
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(&zfree[stage]);  // the record is in registers
+        if (!mbar_wait_bounded(&vempty[stage], ((t / S) & 1u) ^ 1u)) {
+            ok = false;
+            break;
+        }
+        if (lane == 0) {
+            if (mask)
+                mbar_arrive_expect_tx(&vfull[stage], __popc(mask) * C::kBlockBytes);
+            else
+                mbar_arrive(&vfull[stage]);
+        }
+        __syncwarp();
+        if ((mask >> lane) & 1u)
+            tma_load_5d(stage_buf + static_cast<size_t>(stage) * 2 * C::kTile + C::kTile + lane * C::kBlockBytes, tmv,
+                        z, &vfull[stage], policy);
+        __syncwarp();
+    }
+    if (!ok && lane == 0) {
+        if (p.err)
+            atomicOr(p.err, PA_DEVERR_TIMEOUT);
+        const uint32_t first = t > static_cast<uint32_t>(S) ? t - S : 0;
+        for (uint32_t u = first; u < t; ++u)
+            (void)mbar_wait_bounded(&vfull[u % S], (u / S) & 1u);
+    }
     __syncwarp();
 }
 
@@ -370,8 +475,10 @@ template <typename T, int BS, int G>
 __device__ inline bool gqa_mma(const DecodeParams &p, char *smem, const GqaLayout &L, uint32_t tmem) {
     using C = GqaCfg<T, BS, G>;
     const int S = p.stages;
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.full);
-    uint64_t *empty = reinterpret_cast<uint64_t *>(smem + L.empty);
+    uint64_t *kfull = reinterpret_cast<uint64_t *>(smem + L.kfull);
+    uint64_t *vfull = reinterpret_cast<uint64_t *>(smem + L.vfull);
+    uint64_t *kempty = reinterpret_cast<uint64_t *>(smem + L.kempty);
+    uint64_t *vempty = reinterpret_cast<uint64_t *>(smem + L.vempty);
     uint64_t *ifull = reinterpret_cast<uint64_t *>(smem + L.ifull);
     uint64_t *iempty = reinterpret_cast<uint64_t *>(smem + L.iempty);
     uint64_t *sfull = reinterpret_cast<uint64_t *>(smem + L.sfull);
@@ -388,10 +495,12 @@ __device__ inline bool gqa_mma(const DecodeParams &p, char *smem, const GqaLayou
 
     // P V of a tile whose S was issued earlier: one accumulator per quarter of
     // the tile's tokens (the softmax warp that owns those tokens scales them).
-    auto pv = [&](uint32_t gp, int stage_p) -> bool {
+    auto pv = [&](uint32_t gp, uint32_t tp) -> bool {
         const int b = static_cast<int>(gp & 1u);
         const uint32_t use = (gp >> 1) & 1u;
-        if (!mbar_wait_bounded(&pfull[b], use) || !mbar_wait_bounded(&ofree[b], use ^ 1u))
+        const int stage_p = static_cast<int>(tp % S);
+        if (!mbar_wait_bounded(&pfull[b], use) || !mbar_wait_bounded(&ofree[b], use ^ 1u) ||
+            !mbar_wait_bounded(&vfull[stage_p], (tp / S) & 1u))
             return false;
         tc_fence_after();
         const char *vt = stage_buf + static_cast<size_t>(stage_p) * 2 * C::kTile + C::kTile;
@@ -410,13 +519,13 @@ __device__ inline bool gqa_mma(const DecodeParams &p, char *smem, const GqaLayou
             }
         }
         tc_commit(&ofull[b]);
-        tc_commit(&empty[stage_p]);  // K/V stage free once both products finish
+        tc_commit(&vempty[stage_p]);  // the V half is free once P V finishes
         return true;
     };
 
     uint32_t g = 0;  // tiles whose S has been issued (S / P / O buffer = g & 1)
     bool have_prev = false;
-    int prev_stage = 0;
+    uint32_t prev_t = 0;
     for (int k = 0;; ++k) {
         const int slot = k % kGqaItemSlots;
         if (!mbar_wait_bounded(&ifull[slot], static_cast<uint32_t>(k / kGqaItemSlots) & 1u))
@@ -435,7 +544,7 @@ __device__ inline bool gqa_mma(const DecodeParams &p, char *smem, const GqaLayou
             const int stage = static_cast<int>(t % S);
             const int b = static_cast<int>(g & 1u);
             const uint32_t use = (g >> 1) & 1u;
-            if (!mbar_wait_bounded(&full[stage], (t / S) & 1u) || !mbar_wait_bounded(&sfree[b], use ^ 1u))
+            if (!mbar_wait_bounded(&kfull[stage], (t / S) & 1u) || !mbar_wait_bounded(&sfree[b], use ^ 1u))
                 return false;
             tc_fence_after();
             const char *kt = stage_buf + static_cast<size_t>(stage) * 2 * C::kTile;
@@ -447,15 +556,16 @@ __device__ inline bool gqa_mma(const DecodeParams &p, char *smem, const GqaLayou
                 tc_mma(tmem + b * 16, ad, bd, kIdQK, kk > 0);
             }
             tc_commit(&sfull[b]);
+            tc_commit(&kempty[stage]);  // the K half: once these MMAs finish (and the softmax warps read the mask)
             if (ti == ntiles - 1)
                 tc_commit(&iempty[slot]);  // the query rows are free once these MMAs finish
-            if (have_prev && !pv(g - 1, prev_stage))
+            if (have_prev && !pv(g - 1, prev_t))
                 return false;
             have_prev = true;
-            prev_stage = stage;
+            prev_t = t;
         }
     }
-    if (have_prev && !pv(g - 1, prev_stage))
+    if (have_prev && !pv(g - 1, prev_t))
         return false;
     return true;
 }
@@ -494,7 +604,9 @@ __device__ inline bool gqa_softmax(const DecodeParams &p, char *smem, const GqaL
     const int row = quarter * 32 + lane;     // tile token (S row) and head_dim index (O^T row)
     const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const int S = p.stages;
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.full);
+    uint64_t *kfull = reinterpret_cast<uint64_t *>(smem + L.kfull);
+    uint64_t *vfull = reinterpret_cast<uint64_t *>(smem + L.vfull);
+    uint64_t *kempty = reinterpret_cast<uint64_t *>(smem + L.kempty);
     uint64_t *ifull = reinterpret_cast<uint64_t *>(smem + L.ifull);
     uint64_t *iempty = reinterpret_cast<uint64_t *>(smem + L.iempty);
     uint64_t *sfull = reinterpret_cast<uint64_t *>(smem + L.sfull);
@@ -640,18 +752,22 @@ __device__ inline bool gqa_softmax(const DecodeParams &p, char *smem, const GqaL
             const int stage = static_cast<int>(t % S);
             const int b = static_cast<int>(g & 1u);
             const uint32_t use = (g >> 1) & 1u;
-            if (!mbar_wait_bounded(&full[stage], (t / S) & 1u) || !mbar_wait_bounded(&sfull[b], use))
+            if (!mbar_wait_bounded(&kfull[stage], (t / S) & 1u) || !mbar_wait_bounded(&sfull[b], use))
                 return false;
             tc_fence_after();
             float sc[G];
             tmem_ld<G>(tl + b * 16, sc);
+            const uint32_t mask = meta[stage];
             tmem_wait_ld();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0)
+            // S and the tile's block mask are read: S buffer b and the K half
+            // of the stage may be refilled
+            if (lane == 0) {
                 mbar_arrive(&sfree[b]);
+                mbar_arrive(&kempty[stage]);
+            }
 
-            const uint32_t mask = meta[stage];
             const int j = row / BS;
             const int tok = (it.blk_lo + ti * C::kBpt + j) * BS + (row % BS);
             const bool valid = ((mask >> j) & 1u) && tok >= it.tok_lo && tok < it.tok_hi;
@@ -675,7 +791,11 @@ __device__ inline bool gqa_softmax(const DecodeParams &p, char *smem, const GqaL
                 *reinterpret_cast<uint16_t *>(pb + h * 128 + ((pchunk ^ (h & 7)) << 4) + psub) = hi;
                 *reinterpret_cast<uint16_t *>(pb + (G + h) * 128 + ((pchunk ^ ((G + h) & 7)) << 4) + psub) = lo;
             }
-            if (!valid) {  // p = 0 here; make sure V holds no NaN/Inf for this token
+            // p = 0 for an invalid token; its V row must hold no NaN / Inf, so
+            // it is zeroed once the tile's V has landed
+            if (__any_sync(0xffffffffu, !valid) && !mbar_wait_bounded(&vfull[stage], (t / S) & 1u))
+                return false;
+            if (!valid) {
                 char *vt = stage_buf + static_cast<size_t>(stage) * 2 * C::kTile + C::kTile;
 #pragma unroll
                 for (int bx = 0; bx < 2; ++bx) {
@@ -719,11 +839,14 @@ __global__ void __launch_bounds__(kGqaThreads, 1)
     const GqaLayout L = gqa_smem_layout(p.stages);
     const int warp = threadIdx.x >> 5;
     if (threadIdx.x == 0) {
-        uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.full);
-        uint64_t *empty = reinterpret_cast<uint64_t *>(smem + L.empty);
         for (int i = 0; i < p.stages; ++i) {
-            mbar_init(&full[i], 1);
-            mbar_init(&empty[i], 1);
+            mbar_init(reinterpret_cast<uint64_t *>(smem + L.kfull) + i, 1);
+            mbar_init(reinterpret_cast<uint64_t *>(smem + L.vfull) + i, 1);
+            // the S commit and the softmax warps (block mask read)
+            mbar_init(reinterpret_cast<uint64_t *>(smem + L.kempty) + i, 1 + kGqaSmWarps);
+            mbar_init(reinterpret_cast<uint64_t *>(smem + L.vempty) + i, 1);
+            mbar_init(reinterpret_cast<uint64_t *>(smem + L.zfull) + i, 1);
+            mbar_init(reinterpret_cast<uint64_t *>(smem + L.zfree) + i, 1);
         }
         uint64_t *ifull = reinterpret_cast<uint64_t *>(smem + L.ifull);
         uint64_t *iempty = reinterpret_cast<uint64_t *>(smem + L.iempty);
@@ -763,6 +886,8 @@ __global__ void __launch_bounds__(kGqaThreads, 1)
 
     if (warp == 0) {
         gqa_producer<T, BS, G>(p, &tmk, &tmv, &tmq, smem, L);
+    } else if (warp == 6) {
+        gqa_vproducer<T, BS, G>(p, &tmv, smem, L);
     } else if (warp == 1) {
         bool ok = true;
         if ((threadIdx.x & 31) == 0) {

@@ -71,18 +71,21 @@ __global__ void __launch_bounds__(256)
     }
 }
 
-// One CTA per (sequence, head): merge the prefix pass's partials of its group
-// row with the suffix pass's partials of its own row.
+// One warp per (sequence, head), kReduceRows rows per CTA: merge the prefix
+// pass's partials of its group row with the suffix pass's partials of its own
+// row.  The partitions are taken kBatch at a time, their (m, l) pairs and
+// head_dim slices all loaded before any is used, and folded into a running
+// max, denominator and numerator.
 template <int D>
 __global__ void __launch_bounds__(kReduceThreads)
     prefix_combine_kernel(const DecodeParams pre, const DecodeParams suf, const int32_t *__restrict__ shared_eff,
                           int group_size) {
-    constexpr int kWarps = kReduceThreads / 32;
-    constexpr int kPer = D / 32;
-    __shared__ float red[kWarps];
-    __shared__ float accs[kWarps][D];
-    const long long rowi = blockIdx.x;  // s * H + h
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    constexpr int kPer = D / 32;  // head_dim slice per lane (4 or 2)
+    constexpr int kBatch = 8;
+    const int lane = threadIdx.x & 31;
+    const long long rowi = static_cast<long long>(blockIdx.x) * kReduceRows + (threadIdx.x >> 5);  // s * H + h
+    if (rowi >= static_cast<long long>(suf.num_seqs) * suf.num_heads)
+        return;
     const int H = suf.num_heads, G = suf.num_heads / suf.num_kv_heads;
     const long long s = rowi / H;
     const int h = static_cast<int>(rowi - s * H);
@@ -90,73 +93,71 @@ __global__ void __launch_bounds__(kReduceThreads)
     const int j = static_cast<int>(s - g * group_size);
     const int kvh = h / G, gg = h - kvh * G;
     const long long rowp = (g * suf.num_kv_heads + kvh) * (group_size * G) + j * G + gg;
-    const int eff = shared_eff[g];
+    const int eff = ld_nc_i32(shared_eff + g);
+    const int len = ld_nc_i32(suf.context_lens + s);
     const int np_pre = seq_span(eff, pre.max_len, 0, pre.block_size, pre.bpp).nparts;
-    const int np_suf = seq_span(suf.context_lens[s], suf.max_len, 0, suf.block_size, suf.bpp, eff).nparts;
+    const int np_suf = seq_span(len, suf.max_len, 0, suf.block_size, suf.bpp, eff).nparts;
     const int np = np_pre + np_suf;
     const float2 *ml_pre = reinterpret_cast<const float2 *>(pre.part_ml + rowp * pre.max_parts * 2);
     const float2 *ml_suf = reinterpret_cast<const float2 *>(suf.part_ml + rowi * suf.max_parts * 2);
-    auto ml_at = [&](int q) { return q < np_pre ? ml_pre[q] : ml_suf[q - np_pre]; };
-    auto acc_at = [&](int q) {
-        return q < np_pre ? pre.part_acc + (rowp * pre.max_parts + q) * D
-                          : suf.part_acc + (rowi * suf.max_parts + (q - np_pre)) * D;
-    };
+    const float *acc_pre = pre.part_acc + rowp * pre.max_parts * D + lane * kPer;
+    const float *acc_suf = suf.part_acc + rowi * suf.max_parts * D + lane * kPer;
 
-    float M = -INFINITY;
-    for (int q = tid; q < np; q += kReduceThreads)
-        M = fmaxf(M, ml_at(q).x);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1)
-        M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    if (lane == 0)
-        red[warp] = M;
-    __syncthreads();
-    M = red[0];
-#pragma unroll
-    for (int w = 1; w < kWarps; ++w)
-        M = fmaxf(M, red[w]);
-    __syncthreads();
-    float den = 0.f;
-    if (M != -INFINITY)
-        for (int q = tid; q < np; q += kReduceThreads) {
-            const float2 v = ml_at(q);
-            if (v.x != -INFINITY)
-                den = fmaf(v.y, exp2f(v.x - M), den);
-        }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1)
-        den += __shfl_xor_sync(0xffffffffu, den, o);
-    if (lane == 0)
-        red[warp] = den;
-    float num[kPer];
+    float mw = -INFINITY, dw = 0.f, nw[kPer];
 #pragma unroll
     for (int i = 0; i < kPer; ++i)
-        num[i] = 0.f;
-    if (M != -INFINITY) {
-        for (int q = warp; q < np; q += kWarps) {
-            const float mq = ml_at(q).x;
-            const float sc = mq == -INFINITY ? 0.f : exp2f(mq - M);
-            const float *a = acc_at(q) + lane * kPer;
+        nw[i] = 0.f;
+    for (int q0 = 0; q0 < np; q0 += kBatch) {
+        float2 m[kBatch];
+        float v[kBatch][kPer];
+#pragma unroll
+        for (int b = 0; b < kBatch; ++b) {
+            const int q = q0 + b;
+            m[b] = make_float2(-INFINITY, 0.f);
 #pragma unroll
             for (int i = 0; i < kPer; ++i)
-                num[i] = fmaf(a[i], sc, num[i]);
+                v[b][i] = 0.f;
+            if (q < np) {
+                const bool in_pre = q < np_pre;
+                m[b] = in_pre ? ml_pre[q] : ml_suf[q - np_pre];
+                const float *a = in_pre ? acc_pre + static_cast<long long>(q) * D
+                                        : acc_suf + static_cast<long long>(q - np_pre) * D;
+                if constexpr (kPer == 4) {
+                    const float4 x = *reinterpret_cast<const float4 *>(a);
+                    v[b][0] = x.x, v[b][1] = x.y, v[b][2] = x.z, v[b][3] = x.w;
+                } else {
+                    const float2 x = *reinterpret_cast<const float2 *>(a);
+                    v[b][0] = x.x, v[b][1] = x.y;
+                }
+            }
         }
+        float bm = -INFINITY;
+#pragma unroll
+        for (int b = 0; b < kBatch; ++b)
+            bm = fmaxf(bm, m[b].x);
+        const float mn = fmaxf(mw, bm);
+        if (mn == -INFINITY)
+            continue;
+        const float al = mw == -INFINITY ? 0.f : exp2f(mw - mn);
+        dw *= al;
+#pragma unroll
+        for (int i = 0; i < kPer; ++i)
+            nw[i] *= al;
+#pragma unroll
+        for (int b = 0; b < kBatch; ++b) {
+            if (m[b].x != -INFINITY) {
+                const float sc = exp2f(m[b].x - mn);
+                dw = fmaf(m[b].y, sc, dw);
+#pragma unroll
+                for (int i = 0; i < kPer; ++i)
+                    nw[i] = fmaf(v[b][i], sc, nw[i]);
+            }
+        }
+        mw = mn;
     }
 #pragma unroll
     for (int i = 0; i < kPer; ++i)
-        accs[warp][lane * kPer + i] = num[i];
-    __syncthreads();
-    float dsum = 0.f;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w)
-        dsum += red[w];
-    for (int d = tid; d < D; d += kReduceThreads) {
-        float v = 0.f;
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w)
-            v += accs[w][d];
-        store_out(suf.out, suf.out_dtype, rowi * D + d, dsum > 0.f ? v / dsum : 0.f);
-    }
+        store_out(suf.out, suf.out_dtype, rowi * D + lane * kPer + i, dw > 0.f ? nw[i] / dw : 0.f);
 }
 
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
@@ -325,8 +326,9 @@ extern "C" pa_status pa_decode_shared_prefix(void *out, const void *q, const voi
         return st;
 
     // 4) merge
-    prefix_combine_kernel<128><<<static_cast<unsigned>(static_cast<long long>(num_seqs) * num_heads), kReduceThreads,
-                                 0, cs>>>(pre, suf, shared_eff, group_size);
+    const long long rows = static_cast<long long>(num_seqs) * num_heads;
+    prefix_combine_kernel<128><<<static_cast<unsigned>((rows + kReduceRows - 1) / kReduceRows), kReduceThreads, 0,
+                                 cs>>>(pre, suf, shared_eff, group_size);
     e = cudaGetLastError();
     if (e != cudaSuccess)
         return bad(PA_ERR_CUDA, "shared-prefix combine launch failed");
