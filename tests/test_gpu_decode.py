@@ -36,6 +36,10 @@ EDGE_CASES = [
     ("tc_g4_parts", 3, 8, 2, 128, 16, [700, 129, 2049], 0, 64),
     ("tc_g8_bs8_window", 3, 16, 2, 128, 8, [5000, 77, 1300], 1000, 0),
     ("tc_empty", 3, 8, 1, 128, 8, [0, 300, 0], 0, 0),
+    # many one-tile items of one or two blocks (16-token partitions at block 8),
+    # empty and one-token sequences among them; up to 63 partitions per row
+    ("tc_many_items", 24, 32, 8, 128, 8,
+     [0, 1, 7, 8, 9, 16, 17, 100, 255, 256, 257, 0, 511, 512, 513, 3, 64, 1000, 129, 0, 33, 48, 2, 700], 0, 16),
 ]
 
 
