@@ -18,6 +18,10 @@ Prints ONE JSON line (rank 0).  Key numbers:
   roofline   pa_decode call (decode kernel + partition reduce) timed with
              CUDA events on its stream, against the measured HBM copy peak
   cpu_baseline  the fp64 CPU oracle on the host cores (rank 0, N = 1 only)
+  cache_ops  pa_append_kv (and pa_copy_blocks where the step copies blocks):
+             time per call, algorithmic bytes and GB/s, from CUDA events
+             around each call in a second loop of the same steps (outside
+             the timed region, so the events add nothing to it)
 
 --impl reference times the CPU oracle alone as the reference arm.
 """
@@ -209,19 +213,28 @@ class Step:
         pass
 
     append_first = False   # prefix sharing writes the new tokens before it decodes
+    append_bytes = 0       # algorithmic bytes of the step's append
+    copy_bytes = 0         # and of its block copies (0: the step copies nothing)
 
     def run(self, stream, events=None):
-        """One step; `events` (start, end) bracket the decode call."""
-        self.pre(stream)
+        """One step; `events` maps a part of it ("copy", "append", "decode") to
+        the (start, end) CUDA events that bracket that part."""
+        ev = events or {}
+
+        def part(name, fn):
+            e = ev.get(name)
+            if e:
+                e[0].record(stream)
+            fn(stream)
+            if e:
+                e[1].record(stream)
+
+        part("copy", self.pre)
         if self.append_first:
-            self.post(stream)
-        if events:
-            events[0].record(stream)
-        self.decode(stream)
-        if events:
-            events[1].record(stream)
+            part("append", self.post)
+        part("decode", self.decode)
         if not self.append_first:
-            self.post(stream)
+            part("append", self.post)
 
 
 def _elt(dtype):
@@ -303,6 +316,9 @@ class DecodeAppendStep(Step):
         self.kv_bytes = self.dec_bytes["kv"]
         self.roof_bytes = self.dec_bytes["total"]
         self.launches = (2 if self.ws is not None else 1) + 1
+        T = inp.k_new.shape[0]
+        self.append_bytes = (acc.append_quant_bytes(T, s.num_kv_heads, s.head_dim, elt) if self.kv_format else
+                             acc.append_bytes(T, s.num_kv_heads, s.head_dim, elt))
 
     def decode(self, stream, q=None, bt=None, cl=None):
         s = self.shape
@@ -396,6 +412,7 @@ class WindowStep(DecodeAppendStep):
         self.kv_bytes = self.dec_bytes["kv"]
         self.roof_bytes = self.dec_bytes["total"]
         self.launches = 3
+        self.append_bytes = acc.append_bytes(st.k_new.shape[0], s.num_kv_heads, s.head_dim, _elt(s.dtype))
 
     def oracle_step(self, threads, rows=None):
         import oracle
@@ -452,6 +469,8 @@ class PrefixStep(DecodeAppendStep):
         self.roof_bytes = self.dec_bytes["total"] - (self.kv_bytes - self.unique_kv)
         self.launches = (1 if st.pairs.shape[0] else 0) + 1 + (2 if self.ws is not None else 1)
         self.T = st.slots.numel()
+        self.append_bytes = acc.append_bytes(self.T, s.num_kv_heads, s.head_dim, elt)
+        self.copy_bytes = acc.copy_bytes(int(st.pairs.shape[0]), s.num_kv_heads, block_size, s.head_dim, elt)
         if shared:
             self.name += "_shared"
             self.description += "; decode by pa_decode_shared_prefix (each prompt's whole blocks read once per group)"
@@ -564,6 +583,15 @@ def run_native(args):
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ds = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     de = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    parts = {n: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+             for n in ("append", "copy")}
+
+    def part_events(i):
+        ev = {"append": parts["append"][i]}
+        if st.copy_bytes:
+            ev["copy"] = parts["copy"][i]
+        return ev
+
     es = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     ee = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     flush = (torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
@@ -581,7 +609,7 @@ def run_native(args):
         if flush is None:
             ev0.record(stream)
             for i in range(K):
-                st.run(stream, (ds[i], de[i]))
+                st.run(stream, {"decode": (ds[i], de[i])})
             ev1.record(stream)
         else:
             # the step's K/V would stay in L2: overwrite a buffer larger than L2
@@ -589,8 +617,15 @@ def run_native(args):
             for i in range(K):
                 flush.add_(1)
                 es[i].record(stream)
-                st.run(stream, (ds[i], de[i]))
+                st.run(stream, {"decode": (ds[i], de[i])})
                 ee[i].record(stream)
+        torch.cuda.synchronize(dev)
+        # the cache ops of the same steps, timed one by one in a loop of their
+        # own (their events would add latency to a launch-bound timed step)
+        for i in range(K):
+            if flush is not None:
+                flush.add_(1)
+            st.run(stream, part_events(i))
         torch.cuda.synchronize(dev)
     barrier(world)
     clk = clocks.summary()
@@ -599,6 +634,16 @@ def run_native(args):
     else:
         ms_step = statistics.mean(es[i].elapsed_time(ee[i]) for i in range(K))
     ms_dec = statistics.mean(ds[i].elapsed_time(de[i]) for i in range(K))
+    cache_ops = {}
+    for name, nbytes, what in (("append", st.append_bytes, "pa_append_kv"), ("copy_blocks", st.copy_bytes,
+                                                                            "pa_copy_blocks")):
+        if not nbytes:
+            continue
+        evs = parts["append" if name == "append" else "copy"]
+        ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+        cache_ops[name] = {"call": what + ("_quant" if name == "append" and args.kv_format != "native" else ""),
+                           "ms": round(ms, 5), "algorithmic_bytes": int(nbytes),
+                           "gb_s": round(nbytes / (ms * 1e-3) / 1e9, 1)}
     ms_step_max = max_over_ranks(ms_step, world, dev)
     assert st.err.item() == 0, f"device error word {st.err.item()}"
 
@@ -689,6 +734,7 @@ def run_native(args):
         "seq_layer_steps_per_s": round(world * s.num_seqs / (ms_step_max * 1e-3), 1),
         "hbm_frac_of_step": round(value / peak, 4),
         "decode_ms": round(ms_dec, 5),
+        "cache_ops": cache_ops,
         "roofline": {"bound": "hbm", "kernel": "pa_decode (decode + partition reduce)",
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_kind": f"{peak_kind} (hbm_gbs, STREAM-style copy)",
