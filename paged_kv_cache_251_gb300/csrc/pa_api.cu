@@ -373,8 +373,10 @@ pa_status launch_decode_kernel(DecodeParams &p, int dtype, int head_dim, int G, 
     if (grid < 1)
         grid = 1;
     // the TMA-fed kernels claim their items from a per-launch counter
-    // (balances contexts of mixed lengths)
-    if (gqa_tc || mha)
+    // (balances contexts of mixed lengths) when there are more items than
+    // CTAs; with a CTA for every item, each takes its own (no atomic on the
+    // path of a small, latency-bound launch)
+    if ((gqa_tc || mha) && items_max > grid)
         p.work = work_counter(dev);
     void *args_gqa[] = {&p, &tmk, &tmv, &tmq};
     void *args_mha[] = {&p, &tmk, &tmv};
@@ -430,8 +432,10 @@ pa_status launch_decode_q8_kernel(DecodeParams &p, int cache_dtype, int head_dim
         if (grid < 1)
             grid = 1;
         // items are claimed from a per-launch counter (balances contexts of
-        // mixed lengths); without one they go round-robin
-        p.work = work_counter(dev);
+        // mixed lengths) when there are more items than CTAs; otherwise each
+        // CTA takes its own
+        if (items_max > grid)
+            p.work = work_counter(dev);
         void *args[] = {&p, &tmk, &tmv, &tsk, &tsv};
         e = cudaLaunchKernel(tfn, dim3(static_cast<unsigned>(grid)), dim3(kQ8tThreads), args, smem, cs);
         if (e != cudaSuccess)
@@ -470,7 +474,8 @@ pa_status launch_decode_q8_kernel(DecodeParams &p, int cache_dtype, int head_dim
             grid = items_max;
         if (grid < 1)
             grid = 1;
-        p.work = work_counter(dev);  // items claimed from a per-launch counter
+        if (items_max > grid)
+            p.work = work_counter(dev);  // items claimed from a per-launch counter
         void *args[] = {&p};
         e = cudaLaunchKernel(ffn, dim3(static_cast<unsigned>(grid)), dim3(kQ8fThreads), args, smem, cs);
         if (e != cudaSuccess)

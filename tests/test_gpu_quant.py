@@ -191,14 +191,16 @@ def test_decode_quant_repeated_launches_reuse_item_counters():
     bt, cl = inp.block_tables.cuda(), inp.context_lens.cuda()
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     out = torch.empty(q.shape, dtype=torch.float32, device="cuda")
+    # 32-token partitions: about twice as many items as the GPU has CTAs of
+    # this kernel, so the launches claim from a counter
     ws = torch.empty(pa.pa_decode_workspace_size(s.num_seqs, s.num_heads, s.head_dim, s.block_size,
-                                                  bt.shape[1], 0, 64) // 4 + 4, dtype=torch.float32,
+                                                  bt.shape[1], 0, 32) // 4 + 4, dtype=torch.float32,
                      device="cuda")
     for i in range(5000):
         if i == 4999:
             out.fill_(float("nan"))
         pa.pa_decode_quant(out, q, kp, vp, bt, cl, num_kv_heads=s.num_kv_heads, scale=1.0 / math.sqrt(s.head_dim),
-                           partition_size=64, workspace=ws, err_word=err)
+                           partition_size=32, workspace=ws, err_word=err)
     torch.cuda.synchronize()
     assert int(err.item()) == 0
     compare(out.cpu(), _oracle_decode_quant(inp, pools), torch.float16)
