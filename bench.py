@@ -599,7 +599,8 @@ def run_native(args):
     dev = torch.device("cuda", local)
     st = make_step(args.workload, dev, args.partition, args.table, args.shared_prefix, args.kv_format)
     s = st.shape
-    tag = args.workload + ("" if args.kv_format == "native" else "_" + args.kv_format)
+    tag = (args.workload + ("" if args.kv_format == "native" else "_" + args.kv_format) +
+           ("_shared" if args.shared_prefix else ""))
     stream = torch.cuda.current_stream(dev)
 
     for _ in range(max(args.warmup, 0)):
