@@ -264,8 +264,8 @@ template <> __device__ inline float from_bits16<__half>(uint16_t b) { return __h
 // ---------------------------------------------------------------------------
 
 template <typename T, int BS, int G>
-__device__ inline void gqa_producer(const DecodeParams &p, const CUtensorMap *tmk, const CUtensorMap *tmv,
-                                    const CUtensorMap *tmq, char *smem, const GqaLayout &L) {
+__device__ inline void gqa_producer(const DecodeParams &p, const CUtensorMap *tmk, const CUtensorMap *tmq, char *smem,
+                                    const GqaLayout &L) {
     using C = GqaCfg<T, BS, G>;
     const int lane = threadIdx.x & 31;
     const int S = p.stages;
@@ -885,7 +885,7 @@ __global__ void __launch_bounds__(kGqaThreads, 1)
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + L.tmem);
 
     if (warp == 0) {
-        gqa_producer<T, BS, G>(p, &tmk, &tmv, &tmq, smem, L);
+        gqa_producer<T, BS, G>(p, &tmk, &tmq, smem, L);
     } else if (warp == 6) {
         gqa_vproducer<T, BS, G>(p, &tmv, smem, L);
     } else if (warp == 1) {
