@@ -829,13 +829,18 @@ __device__ inline bool q8t_epilogue(const DecodeParams &p, char *smem, const Q8t
                 }
             }
             tc_fence_before();
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(&ofree[b]);
-            if (ti < ntiles - 1)
+            if (ti < ntiles - 1) {
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&ofree[b]);
                 continue;
+            }
             // merge the quarters holding each kv head:
-            // out = sum_w o_w 2^(m_w - M) / sum_w l_w 2^(m_w - M), M = max_w m_w
+            // out = sum_w o_w 2^(m_w - M) / sum_w l_w 2^(m_w - M), M = max_w m_w.
+            // The item's final state in fbuf slot g & 3 is read before this warp
+            // frees O buffer b: that release lets P V of tile g + 2 and then S
+            // and the softmax of tile g + 4 go ahead, and the softmax rewrites
+            // the slot if tile g + 4 ends an item.
             const float *fb = fbuf + (g & 3u) * 4 * 16;
 #pragma unroll
             for (int h = 0; h < kQ8tHeads; ++h) {
@@ -873,6 +878,9 @@ __device__ inline bool q8t_epilogue(const DecodeParams &p, char *smem, const Q8t
                     }
                 }
             }
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&ofree[b]);
 #pragma unroll
             for (int w = 0; w < 4; ++w)
 #pragma unroll

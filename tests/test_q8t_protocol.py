@@ -13,11 +13,18 @@ only after P V of tile g - 2 has finished, and the factor slot g & 3 only after
 the epilogue of tile g - 4; a stage is refilled only after its tile was fully
 consumed.
 
-Two variants that were tried on the way are kept as negative checks: an
+The epilogue of an item's last tile merges the four quarters from the item's
+final softmax state, which the softmax warps leave in slot g & 3; the model
+checks that the slot still holds that tile's state when the merge has read it.
+
+Three variants that were tried on the way are kept as negative checks: an
 epilogue that waits on the 2-deep P barrier (the softmax warps may complete it
-twice before the epilogue looks), and a single MMA thread that defers each
-tile's P V behind the next S without issuing it before it blocks on an item
-(empty items then fill every item slot).
+twice before the epilogue looks), a single MMA thread that defers each tile's
+P V behind the next S without issuing it before it blocks on an item (empty
+items then fill every item slot), and an epilogue that frees its O buffer
+before the merge has read the final state (P V of tile g + 2, then S and the
+softmax of tile g + 4 may go ahead and rewrite the slot: outputs of a kv head
+came out wrong now and then on the GPU before this was found).
 """
 import random
 
@@ -49,7 +56,7 @@ class Deadlock(AssertionError):
 
 def simulate(items, S, design="final", seed=0):
     """items: tiles per item (0 = an empty item).  design: "final" (the
-    kernel), "pfull_epilogue" or "single_issuer_no_flush"."""
+    kernel), "pfull_epilogue", "single_issuer_no_flush" or "ofree_before_merge"."""
     rng = random.Random(seed)
     SL = 4
     two_issuers = design != "single_issuer_no_flush"
@@ -185,11 +192,14 @@ def simulate(items, S, design="final", seed=0):
                 assert g < 2 or g - 2 in pv_done, f"P buffer {b} overwritten while P V({g - 2}) is pending"
                 assert g < 4 or g - 4 in epi_done, f"factor slot {g & 3} overwritten before epilogue({g - 4})"
                 yield "compute"
+                if ti == nt - 1:
+                    final_slot[g & 3] = g  # the item's final softmax state
                 pfull[b].arrive()
                 afull[g & 3].arrive()
                 g += 1
 
     epi_count = {}
+    final_slot = [None] * 4  # tile whose item's final softmax state each slot holds
 
     def epilogue():
         g = 0
@@ -206,10 +216,18 @@ def simulate(items, S, design="final", seed=0):
                 yield from wait(ofull[b], g // 2, "epilogue ofull")
                 assert g in pv_done
                 yield "read"
+                last = ti == nt - 1
+                if not last or design == "ofree_before_merge":
+                    ofree[b].arrive()
+                if last:
+                    # the item's merge reads its final state from slot g & 3
+                    yield "merge"
+                    assert final_slot[g & 3] == g, f"final-state slot {g & 3} rewritten during the merge of tile {g}"
+                    if design != "ofree_before_merge":
+                        ofree[b].arrive()
                 epi_count[g] = epi_count.get(g, 0) + 1
                 if epi_count[g] == 4:
                     epi_done.add(g)
-                ofree[b].arrive()
                 g += 1
 
     if two_issuers:
@@ -280,6 +298,6 @@ def _fails(design, n=300):
     return bad
 
 
-@pytest.mark.parametrize("design", ["pfull_epilogue", "single_issuer_no_flush"])
+@pytest.mark.parametrize("design", ["pfull_epilogue", "single_issuer_no_flush", "ofree_before_merge"])
 def test_the_rejected_variants_fail_in_the_model(design):
     assert _fails(design) > 0
