@@ -6,7 +6,7 @@ import pytest
 import torch
 
 from paged_kv_cache_251_gb300 import workloads as wl
-from paritylib import compare, make_inputs, oracle_decode, run_decode, shape
+from paritylib import compare, make_inputs, oracle_decode, run_decode, shape, to_cuda
 
 pytestmark = pytest.mark.gpu
 
@@ -151,3 +151,46 @@ def test_full_gqa_batch_is_repeatable():
         got, err = run_decode(inp)
         assert err == 0
         assert torch.equal(got, first)
+
+
+@pytest.mark.parametrize("hkv", [8, 32])
+def test_decode_replayed_from_a_cuda_graph(hkv):
+    """pa_decode captured in a CUDA graph and replayed twenty times (no
+    allocation or host synchronisation on the launch path; the item counter a
+    launch claims from is returned to zero by its last CTA, so every replay
+    starts from zero): every replay gives the eager result bit for bit (the
+    grouped-head tensor-core kernel, hkv = 8) or to fp32 rounding (the MHA
+    kernel, hkv = 32), and the eager result matches the oracle."""
+    from paged_kv_cache_251_gb300 import pa
+    lens = [(37 * i * i + 300 * i) % 2100 + 1 for i in range(64)]  # 64 sequences: more items than CTAs
+    sh = shape("graph", 64, 32, hkv, 128, 16, torch.bfloat16, seed=23)
+    inp = make_inputs(sh, lens)
+    dev = to_cuda(inp)
+    out = torch.empty(dev["q"].shape, dtype=torch.float32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ws = pa.workspace_for(dev["q"], 16, dev["block_tables"].shape[1])
+
+    def call():
+        pa.pa_decode(out, dev["q"], dev["k_cache"], dev["v_cache"], dev["block_tables"], dev["context_lens"],
+                     num_kv_heads=hkv, workspace=ws, err_word=err)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        call()  # eager, on the stream the capture will use
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    eager = out.clone()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        call()
+    for _ in range(20):
+        out.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        if hkv == 8:
+            assert torch.equal(out, eager)
+        else:
+            assert float((out - eager).abs().max()) < 1e-6
+    assert int(err.item()) == 0
+    compare(eager.cpu(), oracle_decode(inp), torch.bfloat16)
