@@ -194,3 +194,41 @@ def test_decode_replayed_from_a_cuda_graph(hkv):
             assert float((out - eager).abs().max()) < 1e-6
     assert int(err.item()) == 0
     compare(eager.cpu(), oracle_decode(inp), torch.bfloat16)
+
+
+def test_concurrent_launches_on_two_streams():
+    """Two decode workloads (the tensor-core and the MHA kernel, each claiming
+    items from a counter) launched ten times each on two streams without a
+    synchronisation in between: launches in flight take different counter
+    pairs, so both keep their single-stream results."""
+    from paged_kv_cache_251_gb300 import pa
+    lens = [(37 * i * i + 300 * i) % 2100 + 1 for i in range(64)]
+    cases = []
+    for hkv, seed in ((8, 29), (32, 31)):
+        inp = make_inputs(shape("streams", 64, 32, hkv, 128, 16, torch.bfloat16, seed=seed), lens)
+        dev = to_cuda(inp)
+        out = torch.empty(dev["q"].shape, dtype=torch.float32, device="cuda")
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        ws = pa.workspace_for(dev["q"], 16, dev["block_tables"].shape[1])
+        cases.append((inp, dev, out, err, ws, hkv, torch.cuda.Stream()))
+
+    def call(c):
+        inp, dev, out, err, ws, hkv, st = c
+        pa.pa_decode(out, dev["q"], dev["k_cache"], dev["v_cache"], dev["block_tables"], dev["context_lens"],
+                     num_kv_heads=hkv, workspace=ws, err_word=err, stream=st)
+
+    alone = []
+    for c in cases:
+        call(c)
+        torch.cuda.synchronize()
+        alone.append(c[2].clone())
+    for c in cases:
+        c[6].wait_stream(torch.cuda.current_stream())
+    for _ in range(10):
+        for c in cases:
+            call(c)
+    torch.cuda.synchronize()
+    for c, ref in zip(cases, alone):
+        assert int(c[3].item()) == 0
+        assert float((c[2] - ref).abs().max()) < 1e-6
+    compare(cases[0][2].cpu(), oracle_decode(cases[0][0]), torch.bfloat16)
