@@ -330,8 +330,7 @@ pa_status launch_decode_kernel(DecodeParams &p, int dtype, int head_dim, int G, 
         fn = dtype == PA_F32   ? decode_mha_kernel_f32(head_dim, block_size)
              : dtype == PA_F16 ? decode_mha_kernel_f16(head_dim, block_size)
                                : decode_mha_kernel_bf16(head_dim, block_size);
-        // stages are owned round-robin by the consumer warps: a multiple of
-        // their count keeps each stage with one warp (no phase aliasing)
+        // the stages form one sub-ring per consumer warp: a multiple of their count
         int S = kMhaStageBudget / (2 * tile);
         S -= S % kMhaWarps;
         S = S < kMhaWarps ? kMhaWarps : (S > 16 ? 16 : S);

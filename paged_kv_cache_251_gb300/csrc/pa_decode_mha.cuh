@@ -14,9 +14,11 @@
 //    conflicts.
 //  - Items (sequence, kv head, partition) flow through a small ring filled by
 //    the producer warp (item_full / item_empty mbarriers); each item's query
-//    row rides on the item_full barrier.  Pipeline stages (one cache block
-//    each) are owned round-robin by the 4 consumer warps, so a warp waits
-//    only for its own blocks.
+//    row rides on the item_full barrier.  The pipeline stages (one cache
+//    block each) form one sub-ring per consumer warp, and block j of every
+//    item goes to warp j % 4: a warp waits only for its own blocks, and which
+//    warp sums which blocks does not depend on the items a CTA ran before,
+//    so the result is the same bits on every run.
 //  - QK: lanes are (part, token) pairs — 16 tokens per round (8 at block size
 //    8), each token's row split over 32 / 16 (or 32 / 8) lanes — and every
 //    lane accumulates its share of the dot product with mixed-precision FMA
@@ -247,8 +249,10 @@ __device__ inline void mha_producer(const DecodeParams &p, const CUtensorMap *tm
     }
 
     ItemScan scan;
-    uint32_t t = 0;  // stages issued
-    int k = 0;       // items issued
+    // blocks issued into each consumer warp's sub-ring of S / 4 stages
+    uint32_t cw[kMhaWarps] = {0, 0, 0, 0};
+    const int S4 = S / kMhaWarps;
+    int k = 0;  // items issued
     bool ok = true;
     const long long hkv = p.num_kv_heads;
 
@@ -287,7 +291,7 @@ __device__ inline void mha_producer(const DecodeParams &p, const CUtensorMap *tm
             it.tok_lo = max(sp.start, blk_lo * BS);
             it.tok_hi = min(sp.end, (blk_lo + nb) * BS);
             it.blk_lo = blk_lo;
-            it.t_first = static_cast<int>(t);
+            it.t_first = 0;  // (stages follow from the block index: sub-ring j % 4)
             it.end = 0;
             items[slot] = it;
             if (nb > 0) {
@@ -310,9 +314,15 @@ __device__ inline void mha_producer(const DecodeParams &p, const CUtensorMap *tm
             tbl[j] = pb;
         }
         __syncwarp();
-        for (int j = 0; j < nb; ++j, ++t) {
-            const int stage = static_cast<int>(t % S);
-            if (!mbar_wait_bounded(&empty[stage], ((t / S) & 1u) ^ 1u)) {
+        for (int j0 = 0; j0 < nb && ok; j0 += kMhaWarps) {
+#pragma unroll
+            for (int w = 0; w < kMhaWarps; ++w) {
+            const int j = j0 + w;
+            if (j >= nb)
+                break;
+            const uint32_t c = cw[w]++;
+            const int stage = w * S4 + static_cast<int>(c % S4);
+            if (!mbar_wait_bounded(&empty[stage], ((c / S4) & 1u) ^ 1u)) {
                 ok = false;
                 break;
             }
@@ -331,6 +341,7 @@ __device__ inline void mha_producer(const DecodeParams &p, const CUtensorMap *tm
                 }
             }
             __syncwarp();
+            }
         }
         if (!ok)
             break;
@@ -340,9 +351,12 @@ __device__ inline void mha_producer(const DecodeParams &p, const CUtensorMap *tm
         // a wait gave up: flag it, then wait (bounded) for our copies in flight
         if (p.err)
             atomicOr(p.err, PA_DEVERR_TIMEOUT);
-        const uint32_t first = t > static_cast<uint32_t>(S) ? t - S : 0;
-        for (uint32_t u = first; u < t; ++u)
-            (void)mbar_wait_bounded(&full[u % S], (u / S) & 1u);
+#pragma unroll
+        for (int w = 0; w < kMhaWarps; ++w) {
+            const uint32_t first = cw[w] > static_cast<uint32_t>(S4) ? cw[w] - S4 : 0;
+            for (uint32_t u = first; u < cw[w]; ++u)
+                (void)mbar_wait_bounded(&full[w * S4 + static_cast<int>(u % S4)], (u / S4) & 1u);
+        }
     }
     claim.finish(p);
     __syncwarp();
@@ -377,6 +391,8 @@ __device__ inline void mha_consumer(const DecodeParams &p, char *smem, const Mha
 
     uint4 q[C::kCpl];
     bool ok = true;
+    const int S4 = S / kMhaWarps;
+    uint32_t c = 0;  // blocks this warp took from its sub-ring
     for (int k = 0;; ++k) {
         const int slot = k % kItemSlots;
         if (!mbar_wait_bounded(&ifull[slot], (k / kItemSlots) & 1)) {
@@ -401,11 +417,9 @@ __device__ inline void mha_consumer(const DecodeParams &p, char *smem, const Mha
         for (int i = 0; i < kDpl; ++i)
             acc[i] = 0.f;
 
-        int j = (warp - it.t_first % kMhaWarps + kMhaWarps) % kMhaWarps;
-        for (; j < it.nb; j += kMhaWarps) {
-            const uint32_t t = static_cast<uint32_t>(it.t_first + j);
-            const int stage = static_cast<int>(t % S);
-            if (!mbar_wait_bounded(&full[stage], (t / S) & 1u)) {
+        for (int j = warp; j < it.nb; j += kMhaWarps, ++c) {
+            const int stage = warp * S4 + static_cast<int>(c % S4);
+            if (!mbar_wait_bounded(&full[stage], (c / S4) & 1u)) {
                 ok = false;
                 break;
             }
@@ -537,10 +551,8 @@ __global__ void __launch_bounds__(kMhaThreads) pa_decode_mha_kernel(const Decode
     char *smem = reinterpret_cast<char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     using C = MhaCfg<T, D, BS>;
     const MhaLayout L = mha_smem_layout(p.stages, C::kTile, C::kRow, D);
-    // Stage t belongs to consumer warp t % 4.  With a stage count that is not a
-    // multiple of 4, one stage would pass between warps, and a warp running a
-    // full ring ahead could see its parity wait satisfied by an older phase of
-    // that stage.  The host never launches such a count; refuse it here too.
+    // The stages are one sub-ring of S / 4 per consumer warp: S must be a
+    // multiple of 4.  The host never launches another count; refuse it here too.
     if (p.stages < kMhaWarps || p.stages % kMhaWarps != 0) {
         if (threadIdx.x == 0 && p.err)
             atomicOr(p.err, PA_DEVERR_BAD_LAUNCH);

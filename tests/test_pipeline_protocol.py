@@ -1,15 +1,18 @@
-"""A model of the stage-ring protocol of the warp-specialised decode kernels
-(the 16-bit MHA kernel and the fast 8-bit kernel), run under random
-interleavings on the CPU.
+"""A model of the stage-ring protocol of the warp-specialised MHA decode
+kernel, run under random interleavings on the CPU.
 
-One producer warp fills a ring of S stages (full / empty mbarriers, a phase
-parity per use) and a ring of 4 item slots; stage t belongs to consumer warp
-t % 4; the 4 consumer warps merge each item through a double-buffered
-exchange.  The model checks that no wait passes before its own data landed,
-that no stage, slot or exchange buffer is overwritten while in use, and that
-nothing deadlocks.  Parity waits alias when one stage passes between warps:
-the launchers therefore choose S as a multiple of the consumer-warp count, and
-the kernels refuse any other S.
+One producer warp fills S stages (full / empty mbarriers, a phase parity per
+use) and a ring of 4 item slots; the 4 consumer warps merge each item through
+a double-buffered exchange.  The stages are one sub-ring of S / 4 per consumer
+warp, and block j of every item goes to sub-ring j % 4 (so a warp sums the
+same blocks of an item whatever the CTA ran before).  The model
+checks that no wait passes before its own data landed, that no stage, slot or
+exchange buffer is overwritten while in use, and that nothing deadlocks.
+
+It also keeps the design of an earlier build, one ring whose stage t belongs
+to warp t % 4: there parity waits alias when one stage passes between warps
+(a stage count that is not a multiple of 4), which once corrupted an 8-bit
+kernel's barrier accounting; that case stays as a negative check.
 """
 import random
 
@@ -44,7 +47,11 @@ class Bar:
         return (self.phase & 1) != parity
 
 
-def simulate(items, S, W=4, slots=4, seed=0):
+def simulate(items, S, W=4, slots=4, seed=0, design="subrings"):
+    """design: "subrings" (the MHA kernel: one sub-ring of S / W stages per
+    consumer warp, block j of every item in sub-ring j % W) or "ring" (stage
+    t of one ring belongs to warp t % W, the item's first block to whichever
+    warp owns the next stage; the 8-bit kernel of an earlier build)."""
     rng = random.Random(seed)
     full = [Bar(1) for _ in range(S)]
     empty = [Bar(1) for _ in range(S)]
@@ -58,6 +65,9 @@ def simulate(items, S, W=4, slots=4, seed=0):
     slot_q_landed = [False] * slots
     item_info = [None] * slots
     copies = []                 # pending async copies: (kind, index, value)
+
+    S4 = S // W
+    cw = [0] * W  # blocks issued into each warp's sub-ring
 
     def producer():
         t = 0
@@ -80,13 +90,21 @@ def simulate(items, S, W=4, slots=4, seed=0):
             else:
                 ifull[slot].arrive()
             for j in range(nb):
-                while not empty[pstage].try_wait(pphase ^ 1):
-                    yield "wait empty"
-                stage = pstage
-                pstage += 1
-                if pstage == S:
-                    pstage = 0
-                    pphase ^= 1
+                if design == "subrings":
+                    w = j % W
+                    c = cw[w]
+                    cw[w] += 1
+                    stage = w * S4 + c % S4
+                    while not empty[stage].try_wait(((c // S4) & 1) ^ 1):
+                        yield "wait empty"
+                else:
+                    while not empty[pstage].try_wait(pphase ^ 1):
+                        yield "wait empty"
+                    stage = pstage
+                    pstage += 1
+                    if pstage == S:
+                        pstage = 0
+                        pphase ^= 1
                 # refill only a stage whose previous use was consumed
                 assert stage_owner[stage] is None, f"stage {stage} refilled while holding t={stage_owner[stage]}"
                 stage_owner[stage] = t
@@ -98,6 +116,7 @@ def simulate(items, S, W=4, slots=4, seed=0):
 
     def consumer(warp):
         k = 0
+        c = 0  # blocks this warp took from its sub-ring
         while True:
             slot = k % slots
             while not ifull[slot].try_wait((k // slots) & 1):
@@ -111,24 +130,39 @@ def simulate(items, S, W=4, slots=4, seed=0):
                 assert slot_q_landed[slot] and slot_item[slot] == k, "q not landed"
             iempty[slot].arrive()
             yield "read item"
-            j = (warp - t_first % W + W) % W
-            t0 = t_first + j
-            stage = t0 % S
-            phase = (t0 // S) & 1
-            while j < nb:
-                while not full[stage].try_wait(phase):
-                    yield "wait full"
-                t = t_first + j
-                assert stage_owner[stage] == t and stage_landed[stage], \
-                    f"warp {warp} t={t}: stage {stage} holds {stage_owner[stage]} landed={stage_landed[stage]}"
-                yield "compute"
-                stage_owner[stage] = None
-                empty[stage].arrive()
-                j += W
-                stage += W
-                if stage >= S:
-                    stage -= S
-                    phase ^= 1
+            if design == "subrings":
+                j = warp  # the same blocks of every item: the warp's sums do not depend on history
+                while j < nb:
+                    stage = warp * S4 + c % S4
+                    while not full[stage].try_wait((c // S4) & 1):
+                        yield "wait full"
+                    t = t_first + j
+                    assert stage_owner[stage] == t and stage_landed[stage], \
+                        f"warp {warp} t={t}: stage {stage} holds {stage_owner[stage]} landed={stage_landed[stage]}"
+                    yield "compute"
+                    stage_owner[stage] = None
+                    empty[stage].arrive()
+                    j += W
+                    c += 1
+            else:
+                j = (warp - t_first % W + W) % W
+                t0 = t_first + j
+                stage = t0 % S
+                phase = (t0 // S) & 1
+                while j < nb:
+                    while not full[stage].try_wait(phase):
+                        yield "wait full"
+                    t = t_first + j
+                    assert stage_owner[stage] == t and stage_landed[stage], \
+                        f"warp {warp} t={t}: stage {stage} holds {stage_owner[stage]} landed={stage_landed[stage]}"
+                    yield "compute"
+                    stage_owner[stage] = None
+                    empty[stage].arrive()
+                    j += W
+                    stage += W
+                    if stage >= S:
+                        stage -= S
+                        phase ^= 1
             b = k & 1
             use = (k >> 1) & 1
             while not mempty[b].try_wait(use ^ 1):
@@ -188,11 +222,12 @@ def _trial(rng, S):
     return items
 
 
+@pytest.mark.parametrize("design", ["subrings", "ring"])
 @pytest.mark.parametrize("S", [4, 8, 12, 16])
-def test_stage_counts_the_launchers_choose_are_safe(S):
+def test_stage_counts_the_launchers_choose_are_safe(S, design):
     rng = random.Random(S)
     for trial in range(150):
-        simulate(_trial(rng, S), S, seed=trial)
+        simulate(_trial(rng, S), S, seed=trial, design=design)
 
 
 def test_a_stage_count_off_the_warp_multiple_aliases_phases():
@@ -203,7 +238,7 @@ def test_a_stage_count_off_the_warp_multiple_aliases_phases():
     for trial in range(60):
         items = [rng.choice([8, 17, 32]) for _ in range(rng.randint(5, 30))]
         try:
-            simulate(items, 11, seed=trial)
+            simulate(items, 11, seed=trial, design="ring")
         except AssertionError:
             failures += 1
     assert failures > 0
