@@ -121,7 +121,7 @@ PA_API size_t pa_decode_workspace_size(int num_seqs, int num_heads, int head_dim
  * attended tokens are read: a sliding window is expressed purely by rewriting
  * table rows (entries of tokens outside the window may hold anything).
  *
- * Arguments (spec order first):
+ * Arguments (the ones every paged decode takes first, in that order):
  *   out           [num_seqs][num_heads][head_dim] of out_dtype (written)
  *   q             [num_seqs][num_heads][head_dim] of dtype
  *   k_cache, v_cache  pool of dtype, layout above
@@ -141,6 +141,11 @@ PA_API size_t pa_decode_workspace_size(int num_seqs, int num_heads, int head_dim
  *                 bytes (may be NULL when that size is 0)
  *   err_word      device uint32 or NULL
  * num_seqs == 0 returns PA_OK without launching.
+ * The same inputs give the same bits on every call: each (sequence, kv head,
+ * partition) is computed in a fixed order whichever CTA takes it, and the
+ * partitions merge in a fixed order.  (A sequence decoded in batches of a
+ * different size may differ in the last bits: the merge picks its layout by
+ * the number of rows.)
  */
 PA_API pa_status pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache,
                     const int32_t *block_tables, const int32_t *context_lens,
