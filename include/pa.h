@@ -77,7 +77,7 @@ typedef struct CUstream_st *pa_stream_t; /* same type as cudaStream_t */
 typedef enum {
     PA_OK = 0,
     PA_ERR_INVALID_ARGUMENT = 1, /* null pointer, negative size, misalignment, bad enum */
-    PA_ERR_UNSUPPORTED = 2,      /* a shape or dtype this build does not implement */
+    PA_ERR_UNSUPPORTED = 2,      /* a shape or dtype the library does not implement */
     PA_ERR_WORKSPACE_TOO_SMALL = 3,
     PA_ERR_CUDA = 4,             /* a CUDA runtime call or launch failed */
     PA_ERR_NO_BLOCKS = 5         /* block manager: the free list is empty */

@@ -3,7 +3,7 @@ the C ABI binding, run the oracle, compare.
 
 Tolerances (attention outputs):
   - fp32 K/V with fp32 out: max-abs <= 1e-5;
-  - fp16 / bf16 K/V: max-abs <= 5e-3 and relative L2 <= 1e-3, judged on fp32
+  - fp16 / bf16 K/V: max-abs <= 5e-3 and relative L2 <= 1e-3, checked on fp32
     out against the fp64 oracle;
   - fp16 / bf16 out: the oracle's result rounded to that type (round to
     nearest even), with the same bounds, except that an element may differ by
