@@ -726,7 +726,7 @@ def run_native(args):
             t0 = time.perf_counter()
             kv_done = st.oracle_step(threads)
             times.append(time.perf_counter() - t0)
-            if time.perf_counter() - t_start + times[-1] > args.cpu_seconds or len(times) >= 20:
+            if time.perf_counter() - t_start + times[-1] > args.cpu_seconds or len(times) >= 100:
                 break
         t_step = statistics.median(times)
         cpu = {"value": kv_done / t_step / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
