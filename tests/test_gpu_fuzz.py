@@ -41,7 +41,7 @@ def _config(i):
     return d, bs, hkv, g, n, _lens(rng, n, bs, max_len), window, part, rng.choice(list(DT))
 
 
-@pytest.mark.parametrize("i", range(40))
+@pytest.mark.parametrize("i", range(120))
 def test_random_decode_configs(i):
     d, bs, hkv, g, n, lens, window, part, dt = _config(i)
     sh = shape(f"fuzz{i}", n, hkv * g, hkv, d, bs, DT[dt], window=window, seed=700 + i)
@@ -65,7 +65,7 @@ def _quant_config(i):
             rng.choice(["int8", "e4m3"]))
 
 
-@pytest.mark.parametrize("i", range(24))
+@pytest.mark.parametrize("i", range(60))
 def test_random_quant_decode_configs(i):
     from paged_kv_cache_251_gb300 import pa
     import oracle
