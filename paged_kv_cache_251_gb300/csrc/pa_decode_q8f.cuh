@@ -46,12 +46,17 @@
 #include "pa_decode.cuh"
 #include "pa_quant.cuh"
 
+#include <type_traits>
+
 namespace pa {
 
 constexpr int kQ8fWarps = 4;  // consumer warps = kv heads per item
 constexpr int kQ8fThreads = (kQ8fWarps + 1) * 32;
 constexpr int kQ8fItemSlots = 4;
 constexpr int kQ8fD = 128;
+// INT8 query rows take the int16 grid while max|q| * d <= 16 * sum |q|
+// (largest element at most 16 times the row's mean magnitude)
+constexpr float kQ8fWideRatio = 16.f;
 
 struct Q8fItem {
     int s, kvh0, nh, part;  // sequence, first kv head, kv heads in the item (<= 4), partition
@@ -145,6 +150,16 @@ __device__ inline uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
     uint32_t h2;
     asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(static_cast<unsigned short>(two_codes)));
     return h2;
+}
+
+// Two of the four INT8 codes of a word as exact fp16 values: the selected
+// bytes, biased to unsigned, become the low mantissa bits of 1024 (fp16
+// 0x6400), and subtracting 1024 + 128 leaves the signed code.  sel 0x4140
+// takes bytes 0 and 1, 0x4342 bytes 2 and 3.
+__device__ inline uint32_t i8x2_to_f16x2(uint32_t four_codes, uint32_t sel) {
+    const uint32_t u = __byte_perm(four_codes ^ 0x80808080u, 0x64646464u, sel);
+    const __half2 h = __hsub2(*reinterpret_cast<const __half2 *>(&u), __half2half2(__ushort_as_half(0x6480u)));
+    return *reinterpret_cast<const uint32_t *>(&h);
 }
 
 // Shared-memory loads at 32-bit shared-window addresses.
@@ -375,8 +390,9 @@ __device__ inline void q8f_consumer(const DecodeParams &p, char *smem, const Q8f
         qk_off[i] = static_cast<uint32_t>(tok * 128 + (part * kCpl + (i + tok) % kCpl) * 16);
     const uint32_t pv_off = static_cast<uint32_t>(wl * kDG);
 
-    uint32_t qp[kQp];  // query pairs of this lane's QK dims: int16x2 (INT8) or f16x2 (E4M3)
+    uint32_t qp[kQp];  // query pairs of this lane's QK dims: int16x2 (INT8) or f16x2 (E4M3, wide INT8)
     float cq = 0.f;    // score factor (query scale * scale * log2 e)
+    bool wide = false; // INT8: this warp's query rows are held as fp16 (exact products), not int16
     bool ok = true;
     for (int k = 0;; ++k) {
         const int slot = k % kQ8fItemSlots;
@@ -392,30 +408,45 @@ __device__ inline void q8f_consumer(const DecodeParams &p, char *smem, const Q8f
             const char *qr = qbuf + (slot * kQ8fWarps + warp) * G * qrow + g * qrow;
             // the row's largest magnitude: this lane's QK dims, then over the
             // parts of its token (they cover the row once)
-            float amax = 0.f;
+            float amax = 0.f, sabs = 0.f;
 #pragma unroll
             for (int c = 0; c < kCpl; ++c) {
                 float f[16];
                 load_q16(qr, p.q_dtype, part * (kQ8fD / kP) + c * 16, f);
 #pragma unroll
-                for (int e = 0; e < 16; ++e)
+                for (int e = 0; e < 16; ++e) {
                     amax = fmaxf(amax, fabsf(f[e]));
+                    if (kI8)
+                        sabs += fabsf(f[e]);
+                }
             }
 #pragma unroll
-            for (int o = 1; o < kP; o <<= 1)
+            for (int o = 1; o < kP; o <<= 1) {
                 amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+                if (kI8)
+                    sabs += __shfl_xor_sync(0xffffffffu, sabs, o);
+            }
             // a row whose largest element is below 1e-30 is read as zero
             if (!(amax > 1e-30f))
                 amax = 0.f;
+            if (kI8) {
+                // the int16 grid (step max|q| / 32767) keeps every element to
+                // within 2^-11 of the row's mean magnitude when max|q| <= 16
+                // mean|q|; a warp holding a row of wider range (a few outlier
+                // elements) takes fp16 products instead, for all of its rows
+                // (exact for fp16 and bf16 queries, as for E4M3 codes)
+                wide = __any_sync(0xffffffffu, amax * static_cast<float>(kQ8fD) > kQ8fWideRatio * sabs);
+            }
             // query pairs in the rotated chunk order: pair 8 i + u holds dims
             // 2u, 2u + 1 of the lane's chunk (i + tok) mod kCpl
             float inv, up = 1.f;
-            if (kI8) {
+            if (kI8 && !wide) {
                 // int16 query: q ~ sq * qi, sq = max|q| / 32767
                 inv = amax > 0.f ? 32767.f / amax : 0.f;
                 cq = amax * (1.f / 32767.f) * p.scale_log2;
             } else {
-                // fp16 query scaled by 2^e so that max |q| * 2^e lies in [2^14, 2^15)
+                // fp16 query (E4M3, or INT8 of wide range) scaled by 2^e so that
+                // max |q| * 2^e lies in [2^14, 2^15)
                 const int e2 = amax > 0.f ? min(126, 14 - ilogbf(amax)) : 0;
                 up = ldexpf(1.f, e2);
                 cq = ldexpf(p.scale_log2, -e2);
@@ -427,7 +458,7 @@ __device__ inline void q8f_consumer(const DecodeParams &p, char *smem, const Q8f
                 load_q16(qr, p.q_dtype, part * (kQ8fD / kP) + ((i + tok) % kCpl) * 16, f);
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
-                    if (kI8) {
+                    if (kI8 && !wide) {
                         const int a = max(-32767, min(32767, __float2int_rn(f[2 * u] * inv)));
                         const int b = max(-32767, min(32767, __float2int_rn(f[2 * u + 1] * inv)));
                         qp[i * 8 + u] = (static_cast<uint32_t>(a) & 0xffffu) | (static_cast<uint32_t>(b) << 16);
@@ -451,180 +482,194 @@ __device__ inline void q8f_consumer(const DecodeParams &p, char *smem, const Q8f
         const uint32_t t0 = static_cast<uint32_t>(it.t_first);
         int stage = static_cast<int>(t0 % S);
         uint32_t phase = (t0 / S) & 1u;
-        for (int j = 0; j < it.nb; ++j) {
-            if (!mbar_wait_bounded(&full[stage], phase)) {
-                ok = false;
-                break;
-            }
-            if (active && valid[stage] && Q8F_OK(stage >= 0 && stage < S, 3)) {
-                const uint32_t kt = stages_a + static_cast<uint32_t>(stage) * stage_bytes + warp * C::kPage;
-                const uint32_t vt = kt + kQ8fWarps * C::kPage;
-                const uint32_t sk = kt + BS * 128;  // the pages' scale rows
-                const uint32_t sv = vt + BS * 128;
-                const int blk = it.blk_lo + j;
-                const int lo = max(it.tok_lo - blk * BS, 0);
-                const int hi = min(it.tok_hi - blk * BS, BS);
+        // the block loop, compiled twice: int16 query products (kExact false)
+        // and, for a warp whose INT8 rows are of wide range, fp16 products
+        auto blocks = [&](auto exact_tag) {
+            constexpr bool kExact = decltype(exact_tag)::value;
+            for (int j = 0; j < it.nb; ++j) {
+                if (!mbar_wait_bounded(&full[stage], phase)) {
+                    ok = false;
+                    break;
+                }
+                if (active && valid[stage] && Q8F_OK(stage >= 0 && stage < S, 3)) {
+                    const uint32_t kt = stages_a + static_cast<uint32_t>(stage) * stage_bytes + warp * C::kPage;
+                    const uint32_t vt = kt + kQ8fWarps * C::kPage;
+                    const uint32_t sk = kt + BS * 128;  // the pages' scale rows
+                    const uint32_t sv = vt + BS * 128;
+                    const int blk = it.blk_lo + j;
+                    const int lo = max(it.tok_lo - blk * BS, 0);
+                    const int hi = min(it.tok_hi - blk * BS, BS);
 
-                // ---- scores of the block's tokens (this lane's head)
-                float sc[kR];
+                    // ---- scores of the block's tokens (this lane's head)
+                    float sc[kR];
 #pragma unroll
-                for (int rd = 0; rd < kR; ++rd) {
-                    const int r = rd * kTpr + tok;
-                    const uint32_t rowa = kt + rd * kTpr * 128;
-                    float x;
-                    if (kI8) {
-                        int a[4] = {0, 0, 0, 0};
+                    for (int rd = 0; rd < kR; ++rd) {
+                        const int r = rd * kTpr + tok;
+                        const uint32_t rowa = kt + rd * kTpr * 128;
+                        float x;
+                        if (kI8 && !kExact) {
+                            int a[4] = {0, 0, 0, 0};
 #pragma unroll
-                        for (int i = 0; i < kCpl; ++i) {
-                            const uint32_t qa = rowa + qk_off[i];
-                            const uint4 w = Q8F_OK(qa >= kt && qa + 16 <= kt + BS * 128 && (qa & 15) == 0, 4)
-                                                ? lds128(qa) : make_uint4(0, 0, 0, 0);
-                            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+                            for (int i = 0; i < kCpl; ++i) {
+                                const uint32_t qa = rowa + qk_off[i];
+                                const uint4 w = Q8F_OK(qa >= kt && qa + 16 <= kt + BS * 128 && (qa & 15) == 0, 4)
+                                                    ? lds128(qa) : make_uint4(0, 0, 0, 0);
+                                const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-                            for (int u = 0; u < 4; ++u) {
-                                a[u] = __dp2a_lo(static_cast<int>(qp[i * 8 + 2 * u]), static_cast<int>(ws[u]), a[u]);
-                                a[u] = __dp2a_hi(static_cast<int>(qp[i * 8 + 2 * u + 1]), static_cast<int>(ws[u]), a[u]);
+                                for (int u = 0; u < 4; ++u) {
+                                    a[u] = __dp2a_lo(static_cast<int>(qp[i * 8 + 2 * u]), static_cast<int>(ws[u]), a[u]);
+                                    a[u] = __dp2a_hi(static_cast<int>(qp[i * 8 + 2 * u + 1]), static_cast<int>(ws[u]), a[u]);
+                                }
                             }
-                        }
-                        int sum = (a[0] + a[1]) + (a[2] + a[3]);
+                            int sum = (a[0] + a[1]) + (a[2] + a[3]);
 #pragma unroll
-                        for (int o = 1; o < kP; o <<= 1)
-                            sum += __shfl_xor_sync(0xffffffffu, sum, o);
-                        x = static_cast<float>(sum);
-                    } else {
-                        float xa[4] = {0.f, 0.f, 0.f, 0.f};
+                            for (int o = 1; o < kP; o <<= 1)
+                                sum += __shfl_xor_sync(0xffffffffu, sum, o);
+                            x = static_cast<float>(sum);
+                        } else {
+                            float xa[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                        for (int i = 0; i < kCpl; ++i) {
-                            const uint4 w = lds128(rowa + qk_off[i]);
-                            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+                            for (int i = 0; i < kCpl; ++i) {
+                                const uint4 w = lds128(rowa + qk_off[i]);
+                                const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-                            for (int u = 0; u < 4; ++u) {
-                                fma2_f16(xa[u], qp[i * 8 + 2 * u], e4m3x2_to_f16x2(ws[u] & 0xffffu));
-                                fma2_f16(xa[u], qp[i * 8 + 2 * u + 1], e4m3x2_to_f16x2(ws[u] >> 16));
+                                for (int u = 0; u < 4; ++u) {
+                                    if (kI8) {
+                                        fma2_f16(xa[u], qp[i * 8 + 2 * u], i8x2_to_f16x2(ws[u], 0x4140u));
+                                        fma2_f16(xa[u], qp[i * 8 + 2 * u + 1], i8x2_to_f16x2(ws[u], 0x4342u));
+                                    } else {
+                                        fma2_f16(xa[u], qp[i * 8 + 2 * u], e4m3x2_to_f16x2(ws[u] & 0xffffu));
+                                        fma2_f16(xa[u], qp[i * 8 + 2 * u + 1], e4m3x2_to_f16x2(ws[u] >> 16));
+                                    }
+                                }
                             }
-                        }
-                        x = (xa[0] + xa[1]) + (xa[2] + xa[3]);
+                            x = (xa[0] + xa[1]) + (xa[2] + xa[3]);
 #pragma unroll
-                        for (int o = 1; o < kP; o <<= 1)
-                            x += __shfl_xor_sync(0xffffffffu, x, o);
+                            for (int o = 1; o < kP; o <<= 1)
+                                x += __shfl_xor_sync(0xffffffffu, x, o);
+                        }
+                        const float skr = Q8F_OK(r >= 0 && r < BS, 6) ? ldsf(sk + r * 4) : 0.f;
+                        sc[rd] = (r >= lo && r < hi) ? x * (cq * skr) : -INFINITY;
                     }
-                    const float skr = Q8F_OK(r >= 0 && r < BS, 6) ? ldsf(sk + r * 4) : 0.f;
-                    sc[rd] = (r >= lo && r < hi) ? x * (cq * skr) : -INFINITY;
-                }
 
-                // ---- one running-max update per block; weights
-                float mb = sc[0];
-#pragma unroll
-                for (int rd = 1; rd < kR; ++rd)
-                    mb = fmaxf(mb, sc[rd]);
-#pragma unroll
-                for (int o = kP; o < kW; o <<= 1)
-                    mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, o));
-                if (mb > m) {
-                    const float alpha = q8f_exp2(m - mb);
-                    l *= alpha;
-#pragma unroll
-                    for (int i = 0; i < kDG; ++i)
-                        acc[i] *= alpha;
-                    m = mb;
-                }
-                float pw[kR];
-#pragma unroll
-                for (int rd = 0; rd < kR; ++rd) {
-                    const float pr = q8f_exp2(sc[rd] - m);
-                    l += pr;
-                    pw[rd] = pr * ldsf(sv + (rd * kTpr + tok) * 4);
-                }
-
-                // ---- P V: this lane's kDG dims of its head
-                if (kI8) {
-                    // rows outside [lo, hi) have weight 0 and so quantised weight 0: the
-                    // integer products ignore whatever those rows hold
-                    float pm = pw[0];
+                    // ---- one running-max update per block; weights
+                    float mb = sc[0];
 #pragma unroll
                     for (int rd = 1; rd < kR; ++rd)
-                        pm = fmaxf(pm, pw[rd]);
+                        mb = fmaxf(mb, sc[rd]);
 #pragma unroll
                     for (int o = kP; o < kW; o <<= 1)
-                        pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, o));
-                    const float inv = pm > 0.f ? __fdividef(32767.f, pm) : 0.f;
-                    const float ps = pm * (1.f / 32767.f);
-                    uint32_t pk[kR];
+                        mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, o));
+                    if (mb > m) {
+                        const float alpha = q8f_exp2(m - mb);
+                        l *= alpha;
 #pragma unroll
-                    for (int rd = 0; rd < kR; ++rd) {
-                        const int pi = min(32767, __float2int_rn(pw[rd] * inv));
-                        const int nb_pi = __shfl_xor_sync(0xffffffffu, pi, kP);  // the next token's lane
-                        pk[rd] = (static_cast<uint32_t>(pi) & 0xffffu) | (static_cast<uint32_t>(nb_pi) << 16);
+                        for (int i = 0; i < kDG; ++i)
+                            acc[i] *= alpha;
+                        m = mb;
                     }
-                    int ai[kDG];
-#pragma unroll
-                    for (int i = 0; i < kDG; ++i)
-                        ai[i] = 0;
+                    float pw[kR];
 #pragma unroll
                     for (int rd = 0; rd < kR; ++rd) {
+                        const float pr = q8f_exp2(sc[rd] - m);
+                        l += pr;
+                        pw[rd] = pr * ldsf(sv + (rd * kTpr + tok) * 4);
+                    }
+
+                    // ---- P V: this lane's kDG dims of its head
+                    if (kI8) {
+                        // rows outside [lo, hi) have weight 0 and so quantised weight 0: the
+                        // integer products ignore whatever those rows hold
+                        float pm = pw[0];
 #pragma unroll
-                        for (int tp = 0; tp < kTpr; tp += 2) {
-                            const int ta = rd * kTpr + tp;  // the pair (ta, ta + 1)
-                            const int pp = static_cast<int>(__shfl_sync(0xffffffffu, pk[rd], gbase + tp * kP));
-                            uint32_t w0[G], w1[G];
-                            const uint32_t a0 = vt + ta * 128 + pv_off;
-                            const uint32_t a1 = vt + (ta + 1) * 128 + pv_off;
-                            if (Q8F_OK(a0 >= vt && a1 + 4 * G <= vt + BS * 128 && (a0 & (4 * G - 1)) == 0 &&
-                                           (a1 & (4 * G - 1)) == 0, 5)) {
-                                lds_pv<G>(a0, w0);
-                                lds_pv<G>(a1, w1);
-                            } else {
+                        for (int rd = 1; rd < kR; ++rd)
+                            pm = fmaxf(pm, pw[rd]);
 #pragma unroll
-                                for (int q4 = 0; q4 < G; ++q4)
-                                    w0[q4] = w1[q4] = 0;
-                            }
+                        for (int o = kP; o < kW; o <<= 1)
+                            pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, o));
+                        const float inv = pm > 0.f ? __fdividef(32767.f, pm) : 0.f;
+                        const float ps = pm * (1.f / 32767.f);
+                        uint32_t pk[kR];
 #pragma unroll
-                            for (int q4 = 0; q4 < G; ++q4) {
-                                const int xl = static_cast<int>(__byte_perm(w0[q4], w1[q4], 0x5140));
-                                const int xh = static_cast<int>(__byte_perm(w0[q4], w1[q4], 0x7362));
-                                ai[4 * q4 + 0] = __dp2a_lo(pp, xl, ai[4 * q4 + 0]);
-                                ai[4 * q4 + 1] = __dp2a_hi(pp, xl, ai[4 * q4 + 1]);
-                                ai[4 * q4 + 2] = __dp2a_lo(pp, xh, ai[4 * q4 + 2]);
-                                ai[4 * q4 + 3] = __dp2a_hi(pp, xh, ai[4 * q4 + 3]);
+                        for (int rd = 0; rd < kR; ++rd) {
+                            const int pi = min(32767, __float2int_rn(pw[rd] * inv));
+                            const int nb_pi = __shfl_xor_sync(0xffffffffu, pi, kP);  // the next token's lane
+                            pk[rd] = (static_cast<uint32_t>(pi) & 0xffffu) | (static_cast<uint32_t>(nb_pi) << 16);
+                        }
+                        int ai[kDG];
+#pragma unroll
+                        for (int i = 0; i < kDG; ++i)
+                            ai[i] = 0;
+#pragma unroll
+                        for (int rd = 0; rd < kR; ++rd) {
+#pragma unroll
+                            for (int tp = 0; tp < kTpr; tp += 2) {
+                                const int ta = rd * kTpr + tp;  // the pair (ta, ta + 1)
+                                const int pp = static_cast<int>(__shfl_sync(0xffffffffu, pk[rd], gbase + tp * kP));
+                                uint32_t w0[G], w1[G];
+                                const uint32_t a0 = vt + ta * 128 + pv_off;
+                                const uint32_t a1 = vt + (ta + 1) * 128 + pv_off;
+                                if (Q8F_OK(a0 >= vt && a1 + 4 * G <= vt + BS * 128 && (a0 & (4 * G - 1)) == 0 &&
+                                               (a1 & (4 * G - 1)) == 0, 5)) {
+                                    lds_pv<G>(a0, w0);
+                                    lds_pv<G>(a1, w1);
+                                } else {
+#pragma unroll
+                                    for (int q4 = 0; q4 < G; ++q4)
+                                        w0[q4] = w1[q4] = 0;
+                                }
+#pragma unroll
+                                for (int q4 = 0; q4 < G; ++q4) {
+                                    const int xl = static_cast<int>(__byte_perm(w0[q4], w1[q4], 0x5140));
+                                    const int xh = static_cast<int>(__byte_perm(w0[q4], w1[q4], 0x7362));
+                                    ai[4 * q4 + 0] = __dp2a_lo(pp, xl, ai[4 * q4 + 0]);
+                                    ai[4 * q4 + 1] = __dp2a_hi(pp, xl, ai[4 * q4 + 1]);
+                                    ai[4 * q4 + 2] = __dp2a_lo(pp, xh, ai[4 * q4 + 2]);
+                                    ai[4 * q4 + 3] = __dp2a_hi(pp, xh, ai[4 * q4 + 3]);
+                                }
                             }
                         }
-                    }
 #pragma unroll
-                    for (int i = 0; i < kDG; ++i)
-                        acc[i] = fmaf(ps, static_cast<float>(ai[i]), acc[i]);
-                } else {
-                    // fp32 products: rows outside [lo, hi) are skipped (they may hold any bits)
+                        for (int i = 0; i < kDG; ++i)
+                            acc[i] = fmaf(ps, static_cast<float>(ai[i]), acc[i]);
+                    } else {
+                        // fp32 products: rows outside [lo, hi) are skipped (they may hold any bits)
 #pragma unroll
-                    for (int rd = 0; rd < kR; ++rd) {
+                        for (int rd = 0; rd < kR; ++rd) {
 #pragma unroll
-                        for (int u = 0; u < kTpr; ++u) {
-                            const int ta = rd * kTpr + u;
-                            const float pu = __shfl_sync(0xffffffffu, pw[rd], gbase + u * kP);
-                            if (ta < lo || ta >= hi)
-                                continue;
-                            uint32_t w[G];
-                            lds_pv<G>(vt + ta * 128 + pv_off, w);
+                            for (int u = 0; u < kTpr; ++u) {
+                                const int ta = rd * kTpr + u;
+                                const float pu = __shfl_sync(0xffffffffu, pw[rd], gbase + u * kP);
+                                if (ta < lo || ta >= hi)
+                                    continue;
+                                uint32_t w[G];
+                                lds_pv<G>(vt + ta * 128 + pv_off, w);
 #pragma unroll
-                            for (int q4 = 0; q4 < G; ++q4) {
-                                const uint32_t h01 = e4m3x2_to_f16x2(w[q4] & 0xffffu);
-                                const uint32_t h23 = e4m3x2_to_f16x2(w[q4] >> 16);
-                                acc[4 * q4 + 0] = fmaf(pu, f16_bits_to_float(h01), acc[4 * q4 + 0]);
-                                acc[4 * q4 + 1] = fmaf(pu, f16_bits_to_float(h01 >> 16), acc[4 * q4 + 1]);
-                                acc[4 * q4 + 2] = fmaf(pu, f16_bits_to_float(h23), acc[4 * q4 + 2]);
-                                acc[4 * q4 + 3] = fmaf(pu, f16_bits_to_float(h23 >> 16), acc[4 * q4 + 3]);
+                                for (int q4 = 0; q4 < G; ++q4) {
+                                    const uint32_t h01 = e4m3x2_to_f16x2(w[q4] & 0xffffu);
+                                    const uint32_t h23 = e4m3x2_to_f16x2(w[q4] >> 16);
+                                    acc[4 * q4 + 0] = fmaf(pu, f16_bits_to_float(h01), acc[4 * q4 + 0]);
+                                    acc[4 * q4 + 1] = fmaf(pu, f16_bits_to_float(h01 >> 16), acc[4 * q4 + 1]);
+                                    acc[4 * q4 + 2] = fmaf(pu, f16_bits_to_float(h23), acc[4 * q4 + 2]);
+                                    acc[4 * q4 + 3] = fmaf(pu, f16_bits_to_float(h23 >> 16), acc[4 * q4 + 3]);
+                                }
                             }
                         }
                     }
                 }
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&empty[stage]);
+                if (++stage == S) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
             }
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(&empty[stage]);
-            if (++stage == S) {
-                stage = 0;
-                phase ^= 1u;
-            }
-        }
+        };
+        if (kI8 && wide)
+            blocks(std::true_type{});
+        else
+            blocks(std::false_type{});
         if (!ok)
             break;
 

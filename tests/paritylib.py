@@ -95,3 +95,26 @@ def compare(got: torch.Tensor, ref: np.ndarray, kv_dtype: torch.dtype):
         assert max_abs <= MAXABS_LOW, f"max-abs {max_abs:.3e} > {MAXABS_LOW}"
         assert rel <= RELL2_LOW, f"rel-L2 {rel:.3e} > {RELL2_LOW}"
     return max_abs, rel
+
+
+def make_groups(prompts, samples, prompt_lens, extra, bs, hkv, d, dtype, seed):
+    """Groups of sequences sharing a prompt, built by the block manager (a
+    prompt, then forks that each append their own tokens), so that members'
+    tables agree on the prompt's whole blocks: (tables, lens, k, v)."""
+    from paged_kv_cache_251_gb300.blocks import BlockManager
+    N = prompts * samples
+    M = max(prompt_lens) // bs + max(extra) // bs + 4
+    nb = N * M + 8
+    bm = BlockManager(nb, bs, N, M, free_order=wl.permutation(seed, 2, nb))
+    for p in range(prompts):
+        first = p * samples
+        bm.add_sequence(first)
+        bm.extend(first, prompt_lens[p])
+        for j in range(1, samples):
+            bm.fork(first, first + j)
+    seqs = [s for s in range(N) for _ in range(extra[s])]
+    slots, pairs = bm.append(seqs)
+    tables, lens = bm.tables()
+    k = wl.normal_tensor(seed, 4, (nb, hkv, bs, d), dtype=dtype)
+    v = wl.normal_tensor(seed, 5, (nb, hkv, bs, d), dtype=dtype)
+    return tables, lens, k, v

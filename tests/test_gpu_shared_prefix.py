@@ -9,29 +9,9 @@ import torch
 
 import oracle
 from paged_kv_cache_251_gb300 import workloads as wl
-from paritylib import compare
+from paritylib import compare, make_groups
 
 pytestmark = pytest.mark.gpu
-
-
-def _groups(prompts, samples, prompt_lens, extra, bs, hkv, d, dtype, seed):
-    from paged_kv_cache_251_gb300.blocks import BlockManager
-    N = prompts * samples
-    M = max(prompt_lens) // bs + max(extra) // bs + 4
-    nb = N * M + 8
-    bm = BlockManager(nb, bs, N, M, free_order=wl.permutation(seed, 2, nb))
-    for p in range(prompts):
-        first = p * samples
-        bm.add_sequence(first)
-        bm.extend(first, prompt_lens[p])
-        for j in range(1, samples):
-            bm.fork(first, first + j)
-    seqs = [s for s in range(N) for _ in range(extra[s])]
-    slots, pairs = bm.append(seqs)
-    tables, lens = bm.tables()
-    k = wl.normal_tensor(seed, 4, (nb, hkv, bs, d), dtype=dtype)
-    v = wl.normal_tensor(seed, 5, (nb, hkv, bs, d), dtype=dtype)
-    return tables, lens, k, v
 
 
 CASES = [
@@ -50,7 +30,7 @@ def test_shared_prefix_matches_oracle_and_pa_decode(case, dtype):
     prompts, samples, H, hkv, bs, plens, extra, part = case
     N = prompts * samples
     extra = extra or wl.randint(7, 1, N, 1, 300).tolist()
-    tables, lens, k, v = _groups(prompts, samples, plens, extra, bs, hkv, 128, dtype, seed=prompts * 31 + bs)
+    tables, lens, k, v = make_groups(prompts, samples, plens, extra, bs, hkv, 128, dtype, seed=prompts * 31 + bs)
     q = wl.normal_tensor(9, 3, (N, H, 128), dtype=dtype)
     shared = torch.tensor([pl // bs * bs for pl in plens], dtype=torch.int32)
     out = torch.full((N, H, 128), float("nan"), device="cuda")
@@ -71,7 +51,7 @@ def test_shared_length_beyond_a_member_is_clamped_and_flagged():
     from paged_kv_cache_251_gb300 import pa
     bs, hkv, H = 16, 4, 8
     # group 0: a 320-token prompt (20 whole blocks); member 0 adds nothing, member 1 adds 50 tokens
-    tables, lens, k, v = _groups(2, 2, [320, 100], [0, 50, 3, 1], bs, hkv, 128, torch.bfloat16, seed=3)
+    tables, lens, k, v = make_groups(2, 2, [320, 100], [0, 50, 3, 1], bs, hkv, 128, torch.bfloat16, seed=3)
     q = wl.normal_tensor(9, 3, (4, H, 128), dtype=torch.bfloat16)
     # claim more sharing than member 0's context (used: its 320 tokens, where the
     # tables still agree), and a length that is not whole blocks (used: 32)
