@@ -241,6 +241,177 @@ def _elt(dtype):
     return torch.tensor([], dtype=dtype).element_size()
 
 
+def describe(name, kv_format=None, tokens=None, pairs=None, shared=False):
+    """The workload's description (the same words in both arms' JSON lines)."""
+    if name == "tiny":
+        d = ("tiny: 4 seqs x 4 MHA heads, head_dim 64, block 16, fp32, context ~ U[1, 100], "
+             "64-block pool shuffled; step = pa_decode + pa_append_kv (launch-bound by size)")
+    elif name == "tiny_scaled":
+        d = ("tiny_scaled: the tiny shape (4 MHA heads, head_dim 64, block 16, fp32) with 4096 "
+             "seqs, context ~ U[1, 2048], exact-need pool shuffled; step = pa_decode + pa_append_kv")
+    elif name == "opt13b":
+        d = ("opt13b: 64 seqs x 40 MHA heads, head_dim 128, block 16, fp16, context ~ U[512, 2048], "
+             "exact-need pool shuffled; step = pa_decode + pa_append_kv (1 token/seq)")
+    elif name == "gqa":
+        d = ("gqa: 256 seqs, 32 q / 8 kv heads, head_dim 128, block 16, bf16, lognormal context "
+             "(median 1024, sigma 1) clipped to [16, 8192], 95%-full shuffled pool; "
+             "step = pa_decode + pa_append_kv (1 token/seq)")
+    elif name == "window":
+        d = ("window: 4 seqs x 131072 logical tokens, 32 q / 8 kv heads, head_dim 128, bf16, block 16, "
+             "window 32768 over rings of 2049 physical blocks (table rewrite, no K/V movement), "
+             "512-token partitions + LSE reduce; step = pa_decode + pa_append_kv (1 token/seq)")
+    else:
+        bs = int(name[len("prefix_bs"):].split("_")[0])
+        d = (f"prefix: 32 prompts x 2000 tokens shared by 8 samples each (256 samples), U{{1..256}} new "
+             f"tokens per sample ({tokens} in all), 40 MHA heads, head_dim 128, fp16, "
+             f"block {bs}, {pairs} copy-on-write pairs; step = pa_copy_blocks + pa_append_kv + pa_decode")
+        if shared:
+            d += "; decode by pa_decode_shared_prefix (each prompt's whole blocks read once per group)"
+    if kv_format:
+        d += (f"; 8-bit cache: {kv_format.upper()} codes + one fp32 scale per (token, kv head) row in "
+              f"(block, kv head) pages, step = pa_decode_quant + pa_append_kv_quant")
+    return d
+
+
+def _decode_inputs(name, device, shuffle):
+    """The seeded inputs of the opt13b / gqa / tiny / tiny_scaled workloads."""
+    from paged_kv_cache_251_gb300 import workloads as wl
+    if name == "tiny":
+        return wl.decode_inputs(wl.SHAPES["tiny"], device=device, num_blocks=64, shuffle=shuffle)
+    if name == "gqa":
+        return wl.decode_inputs(wl.SHAPES["gqa"], device=device, room_for_append=True, fill=0.95, shuffle=shuffle)
+    return wl.decode_inputs(wl.SHAPES[name], device=device, shuffle=shuffle)
+
+
+class OracleStep:
+    """A workload's step as the CPU oracle runs it: the CPU baseline of the
+    native arm and the whole of the reference arm.  Its inputs come from the
+    seeded generator (workloads.py) and its block tables, slots and
+    copy-on-write pairs from the oracle's own models (oracle.locate,
+    oracle.RingModel, oracle.CowModel); nothing here loads the CUDA library or
+    its host block manager."""
+
+    def __init__(self, name, table="shuffled", kv_format="native", shared=False):
+        import oracle
+        from paged_kv_cache_251_gb300 import workloads as wl
+        self.oracle = oracle
+        self.kv_format = None if kv_format == "native" else kv_format
+        self.window = 0
+        self.pairs = None
+        if name in ("opt13b", "gqa", "tiny", "tiny_scaled"):
+            inp = _decode_inputs(name, "cpu", table == "shuffled")
+            s = self.shape = inp.shape
+            self.tables, self.lens = inp.block_tables, inp.context_lens
+            slots = []
+            for i in range(s.num_seqs):
+                phys, off = oracle.locate(self.tables[i].tolist(), s.block_size, int(self.lens[i]))
+                slots.append(phys * s.block_size + off)
+            self.slots = torch.tensor(slots, dtype=torch.int64)
+            self.q, self.k_new, self.v_new = inp.q, inp.k_new, inp.v_new
+            if self.kv_format:
+                self.k, self.v = wl.quant_pools(inp, self.kv_format)
+            else:
+                self.k, self.v = inp.k_cache, inp.v_cache
+            self.description = describe(name, kv_format=self.kv_format)
+        elif self.kv_format:
+            raise SystemExit("--kv-format applies to the opt13b, gqa, tiny and tiny_scaled workloads")
+        elif name == "window":
+            self._window()
+        else:
+            self._prefix(int(name[len("prefix_bs"):]), shared)
+            self.description = describe(name, tokens=self.slots.numel(), pairs=self.pairs.shape[0], shared=shared)
+
+    def _window(self, context=131072, window=None):
+        from paged_kv_cache_251_gb300 import workloads as wl
+        s = self.shape = wl.SHAPES["window"]
+        bs, W = s.block_size, (s.window if window is None else window)
+        R = -(-W // bs) + 1
+        nb = s.num_seqs * R
+        M = -(-context // bs) + 8
+        order = wl.permutation(s.seed, 2, nb).tolist()
+        self.tables = torch.full((s.num_seqs, M), -1, dtype=torch.int32)
+        slots = []
+        for i in range(s.num_seqs):
+            ring = self.oracle.RingModel(bs, order[i * R:(i + 1) * R], M)
+            for t in range(context):
+                ring.write(t)
+            self.tables[i] = torch.tensor(ring.table, dtype=torch.int32)  # before token L is placed
+            slots.append(ring.write(context))
+        self.lens = torch.full((s.num_seqs,), context, dtype=torch.int32)
+        self.slots = torch.tensor(slots, dtype=torch.int64)
+        self.window = W
+        kv_shape = (nb, s.num_kv_heads, bs, s.head_dim)
+        self.q = wl.normal_tensor(s.seed, 3, (s.num_seqs, s.num_heads, s.head_dim), dtype=s.dtype)
+        self.k = wl.normal_tensor(s.seed, 4, kv_shape, dtype=s.dtype)
+        self.v = wl.normal_tensor(s.seed, 5, kv_shape, dtype=s.dtype)
+        self.k_new = wl.normal_tensor(s.seed, 6, (s.num_seqs, s.num_kv_heads, s.head_dim), dtype=s.dtype)
+        self.v_new = wl.normal_tensor(s.seed, 7, (s.num_seqs, s.num_kv_heads, s.head_dim), dtype=s.dtype)
+        self.description = describe("window")
+
+    def _prefix(self, bs, shared, prompts=32, samples=8, prompt_len=2000, max_new=256):
+        from paged_kv_cache_251_gb300 import workloads as wl
+        base = wl.SHAPES["prefix"]
+        s = self.shape = wl.Shape(base.name, prompts * samples, base.num_heads, base.num_kv_heads, base.head_dim,
+                                  bs, base.dtype, seed=base.seed + bs)
+        n_new = wl.prefix_draws(base.seed, prompts * samples, 1, max_new)
+        per_prompt = -(-prompt_len // bs)
+        M = -(-(prompt_len + max_new) // bs) + 1
+        nb = prompts * per_prompt + prompts * samples * (-(-max_new // bs) + 1)
+        cow = self.oracle.CowModel(bs, wl.permutation(s.seed, 2, nb).tolist())
+        length = [0] * (prompts * samples)
+        for p in range(prompts):
+            first = p * samples
+            cow.add_sequence(first)
+            for t in range(prompt_len):
+                cow.write(first, t)
+            for j in range(samples):
+                length[first + j] = prompt_len
+                if j:
+                    cow.fork(first, first + j)
+        slots, pairs = [], []
+        for sid in range(prompts * samples):
+            for _ in range(int(n_new[sid])):
+                slot, copy = cow.write(sid, length[sid])
+                length[sid] += 1
+                slots.append(slot)
+                if copy:
+                    pairs.append(copy)
+        self.tables = torch.full((prompts * samples, M), -1, dtype=torch.int32)
+        for sid, row in cow.tables.items():
+            self.tables[sid, :len(row)] = torch.tensor(row, dtype=torch.int32)
+        self.lens = torch.tensor(length, dtype=torch.int32)
+        self.slots = torch.tensor(slots, dtype=torch.int64)
+        self.pairs = torch.tensor(pairs, dtype=torch.int64).reshape(-1, 2)
+        T = len(slots)
+        kv_shape = (nb, s.num_kv_heads, bs, s.head_dim)
+        self.q = wl.normal_tensor(s.seed, 3, (s.num_seqs, s.num_heads, s.head_dim), dtype=s.dtype)
+        self.k = wl.normal_tensor(s.seed, 4, kv_shape, dtype=s.dtype)
+        self.v = wl.normal_tensor(s.seed, 5, kv_shape, dtype=s.dtype)
+        self.k_new = wl.normal_tensor(s.seed, 6, (T, s.num_kv_heads, s.head_dim), dtype=s.dtype)
+        self.v_new = wl.normal_tensor(s.seed, 7, (T, s.num_kv_heads, s.head_dim), dtype=s.dtype)
+
+    def run(self, threads, rows=None):
+        """One step (copies, append, decode of the first `rows` sequences);
+        returns the K/V bytes the decode read."""
+        orc, s = self.oracle, self.shape
+        n = s.num_seqs if rows is None else rows
+        prefix = self.pairs is not None        # prefix sharing writes its tokens before it decodes
+        if prefix:
+            orc.copy_blocks(self.k, self.v, self.pairs)
+            orc.append_kv(self.k, self.v, self.k_new, self.v_new, self.slots)
+        orc.paged_attention(self.q[:n], self.k, self.v, self.tables[:n], self.lens[:n], num_kv_heads=s.num_kv_heads,
+                            scale=1.0 / math.sqrt(s.head_dim), window=self.window, threads=threads)
+        if self.kv_format:
+            orc.append_kv_quant(self.k, self.v, self.k_new, self.v_new, self.slots)
+        elif not prefix:
+            orc.append_kv(self.k, self.v, self.k_new, self.v_new, self.slots)
+        toks = self.lens[:n].to(torch.int64)
+        if self.window:
+            toks = toks.clamp_max(self.window)
+        per_tok = 2 * s.num_kv_heads * (s.head_dim + 4 if self.kv_format else s.head_dim * _elt(s.dtype))
+        return int(toks.sum()) * per_tok
+
+
 class DecodeAppendStep(Step):
     """pa_decode over every sequence's L tokens, then pa_append_kv of token L
     (the slot the host block manager assigns); idempotent step."""
@@ -255,24 +426,8 @@ class DecodeAppendStep(Step):
         from paged_kv_cache_251_gb300.blocks import BlockManager
         self.pa = pa
         self.name = name
-        if name == "tiny":
-            inp = wl.decode_inputs(wl.SHAPES["tiny"], device=device, num_blocks=64, shuffle=shuffle)
-            self.description = ("tiny: 4 seqs x 4 MHA heads, head_dim 64, block 16, fp32, context ~ U[1, 100], "
-                                "64-block pool shuffled; step = pa_decode + pa_append_kv (launch-bound by size)")
-        elif name == "tiny_scaled":
-            inp = wl.decode_inputs(wl.SHAPES["tiny_scaled"], device=device, shuffle=shuffle)
-            self.description = ("tiny_scaled: the tiny shape (4 MHA heads, head_dim 64, block 16, fp32) with 4096 "
-                                "seqs, context ~ U[1, 2048], exact-need pool shuffled; step = pa_decode + pa_append_kv")
-        elif name == "opt13b":
-            inp = wl.decode_inputs(wl.SHAPES["opt13b"], device=device, shuffle=shuffle)
-            self.description = ("opt13b: 64 seqs x 40 MHA heads, head_dim 128, block 16, fp16, context ~ U[512, 2048], "
-                                "exact-need pool shuffled; step = pa_decode + pa_append_kv (1 token/seq)")
-        else:
-            inp = wl.decode_inputs(wl.SHAPES["gqa"], device=device, room_for_append=True, fill=0.95,
-                                   shuffle=shuffle)
-            self.description = ("gqa: 256 seqs, 32 q / 8 kv heads, head_dim 128, block 16, bf16, lognormal context "
-                                "(median 1024, sigma 1) clipped to [16, 8192], 95%-full shuffled pool; "
-                                "step = pa_decode + pa_append_kv (1 token/seq)")
+        inp = _decode_inputs(name, device, shuffle)
+        self.description = describe(name)
         s = self.shape = inp.shape
         # the host block manager replays each sequence's blocks in table order and
         # assigns the slot of the appended token (position L)
@@ -305,9 +460,7 @@ class DecodeAppendStep(Step):
             # (the 16-bit pools are dropped); the new tokens are quantised on append
             self.k_cache = self.v_cache = inp.k_cache = inp.v_cache = None
             self.kq, self.vq = wl.quant_pools(inp, self.kv_format, device=device)
-            self.description += (f"; 8-bit cache: {self.kv_format.upper()} codes + one fp32 scale per "
-                                 f"(token, kv head) row in (block, kv head) pages, "
-                                 f"step = pa_decode_quant + pa_append_kv_quant")
+            self.description = describe(name, kv_format=self.kv_format)
             self.dec_bytes = acc.decode_bytes(inp.context_lens, s.num_heads, s.num_kv_heads, s.head_dim,
                                               s.block_size, 1, out_elt_bytes=4, q_elt_bytes=elt, row_scale_bytes=4)
         else:
@@ -385,28 +538,6 @@ class DecodeAppendStep(Step):
             self.out_host.copy_(self.out, non_blocking=True)
         stream.wait_stream(side)
 
-    def oracle_step(self, threads, rows=None):
-        """The same step on the CPU oracle (host copies made on first use);
-        rows limits the decode to the first `rows` sequences."""
-        import oracle
-        s = self.shape
-        n = s.num_seqs if rows is None else rows
-        if self.kv_format:
-            if not hasattr(self, "_h"):
-                self._h = [t.cpu() for t in (self.q, self.kq, self.vq, self.k_new, self.v_new)]
-            q, kq, vq, kn, vn = self._h
-            oracle.paged_attention(q[:n], kq, vq, self.inp.block_tables[:n], self.inp.context_lens[:n],
-                                   num_kv_heads=s.num_kv_heads, scale=1.0 / math.sqrt(s.head_dim), threads=threads)
-            oracle.append_kv_quant(kq, vq, kn, vn, self.host["slots"])
-            return int(self.inp.context_lens[:n].to(torch.int64).sum()) * 2 * s.num_kv_heads * (s.head_dim + 4)
-        if not hasattr(self, "_h"):
-            self._h = [t.cpu() for t in (self.q, self.k_cache, self.v_cache, self.k_new, self.v_new)]
-        q, k, v, kn, vn = self._h
-        oracle.paged_attention(q[:n], k, v, self.inp.block_tables[:n], self.inp.context_lens[:n],
-                               num_kv_heads=s.num_kv_heads, scale=1.0 / math.sqrt(s.head_dim), threads=threads)
-        oracle.append_kv(k, v, kn, vn, self.host["slots"])
-        return int(self.inp.context_lens[:n].to(torch.int64).sum()) * 2 * s.num_kv_heads * s.head_dim * _elt(s.dtype)
-
 
 class WindowStep(DecodeAppendStep):
     """Sliding window: pa_decode with window 32768 (512-token partitions +
@@ -419,9 +550,7 @@ class WindowStep(DecodeAppendStep):
         from paged_kv_cache_251_gb300 import accounting as acc
         self.pa = pa
         self.name = "window"
-        self.description = ("window: 4 seqs x 131072 logical tokens, 32 q / 8 kv heads, head_dim 128, bf16, block 16, "
-                            "window 32768 over rings of 2049 physical blocks (table rewrite, no K/V movement), "
-                            "512-token partitions + LSE reduce; step = pa_decode + pa_append_kv (1 token/seq)")
+        self.description = describe("window")
         st = scenarios.window_state(device=device)
         s = self.shape = st.shape
         self.window = s.window
@@ -442,19 +571,6 @@ class WindowStep(DecodeAppendStep):
         self.launches = 3
         self.append_bytes = acc.append_bytes(st.k_new.shape[0], s.num_kv_heads, s.head_dim, _elt(s.dtype))
 
-    def oracle_step(self, threads, rows=None):
-        import oracle
-        if not hasattr(self, "_h"):
-            self._h = [t.cpu() for t in (self.q, self.k_cache, self.v_cache, self.k_new, self.v_new)]
-        q, k, v, kn, vn = self._h
-        s = self.shape
-        n = s.num_seqs if rows is None else rows
-        oracle.paged_attention(q[:n], k, v, self.inp.block_tables[:n], self.inp.context_lens[:n],
-                               num_kv_heads=s.num_kv_heads, scale=1.0 / math.sqrt(s.head_dim), window=self.window,
-                               threads=threads)
-        oracle.append_kv(k, v, kn, vn, self.host["slots"])
-        return n * self.window * 2 * s.num_kv_heads * s.head_dim * _elt(s.dtype)
-
 
 class PrefixStep(DecodeAppendStep):
     """Prefix sharing: pa_copy_blocks (copy-on-write of the partly filled last
@@ -472,10 +588,7 @@ class PrefixStep(DecodeAppendStep):
         self.name = f"prefix_bs{block_size}"
         st = scenarios.prefix_state(block_size, device=device)
         s = self.shape = st.shape
-        self.description = (f"prefix: 32 prompts x 2000 tokens shared by 8 samples each (256 samples), U{{1..256}} new "
-                            f"tokens per sample ({st.slots.numel()} in all), 40 MHA heads, head_dim 128, fp16, "
-                            f"block {block_size}, {st.pairs.shape[0]} copy-on-write pairs; step = pa_copy_blocks + "
-                            f"pa_append_kv + pa_decode")
+        self.description = describe(self.name, tokens=st.slots.numel(), pairs=st.pairs.shape[0])
         self.window = 0
         self.inp = type("I", (), {"block_tables": st.block_tables, "context_lens": st.context_lens})
         self.q, self.k_cache, self.v_cache, self.k_new, self.v_new = st.q, st.k_cache, st.v_cache, st.k_new, st.v_new
@@ -501,7 +614,7 @@ class PrefixStep(DecodeAppendStep):
         self.copy_bytes = acc.copy_bytes(int(st.pairs.shape[0]), s.num_kv_heads, block_size, s.head_dim, elt)
         if shared:
             self.name += "_shared"
-            self.description += "; decode by pa_decode_shared_prefix (each prompt's whole blocks read once per group)"
+            self.description = describe(self.name, tokens=st.slots.numel(), pairs=st.pairs.shape[0], shared=True)
             self.group = st.samples
             self.shared_lens = torch.full((st.prompts,), st.prompt_len // block_size * block_size,
                                           dtype=torch.int32, device=device)
@@ -531,19 +644,6 @@ class PrefixStep(DecodeAppendStep):
         self.post(stream, k_new=dev["k_new"], v_new=dev["v_new"], slots=dev["slots"])
         self.decode(stream, q=dev["q"], bt=dev["block_tables"], cl=dev["context_lens"])
         self.out_host.copy_(self.out, non_blocking=True)
-
-    def oracle_step(self, threads, rows=None):
-        import oracle
-        if not hasattr(self, "_h"):
-            self._h = [t.cpu() for t in (self.q, self.k_cache, self.v_cache, self.k_new, self.v_new)]
-        q, k, v, kn, vn = self._h
-        s = self.shape
-        n = s.num_seqs if rows is None else rows
-        oracle.copy_blocks(k, v, self.host["pairs"])
-        oracle.append_kv(k, v, kn, vn, self.host["slots"])
-        oracle.paged_attention(q[:n], k, v, self.inp.block_tables[:n], self.inp.context_lens[:n],
-                               num_kv_heads=s.num_kv_heads, scale=1.0 / math.sqrt(s.head_dim), threads=threads)
-        return int(self.inp.context_lens[:n].to(torch.int64).sum()) * 2 * s.num_kv_heads * s.head_dim * _elt(s.dtype)
 
 
 WORKLOADS = ["opt13b", "gqa", "window", "prefix_bs8", "prefix_bs16", "prefix_bs32", "tiny", "tiny_scaled"]
@@ -720,11 +820,12 @@ def run_native(args):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         threads = os.cpu_count() or 1
+        ost = OracleStep(args.workload, args.table, args.kv_format, args.shared_prefix)
         times, reps, kv_done = [], 0, 0
         t_start = time.perf_counter()
         while True:
             t0 = time.perf_counter()
-            kv_done = st.oracle_step(threads)
+            kv_done = ost.run(threads)
             times.append(time.perf_counter() - t0)
             if time.perf_counter() - t_start + times[-1] > args.cpu_seconds or len(times) >= 100:
                 break
@@ -844,23 +945,23 @@ def run_reference(args):
     world, rank, _ = dist_env()
     if rank != 0:
         return  # the reference arm runs on rank 0 only
-    st = make_step(args.workload, "cpu", args.partition, args.table, kv_format=args.kv_format)
+    st = OracleStep(args.workload, args.table, args.kv_format, args.shared_prefix)
     s = st.shape
     threads = os.cpu_count() or 1
     # size the per-step sample so the whole run stays within a few minutes
     total_steps = max(1, args.steps + args.warmup)
     probe = min(2, s.num_seqs)
     t0 = time.perf_counter()
-    st.oracle_step(threads, rows=probe)
+    st.run(threads, rows=probe)
     per_seq = (time.perf_counter() - t0) / probe
     budget = 150.0 / total_steps
     n = max(1, min(s.num_seqs, int(budget / max(per_seq, 1e-9))))
     for _ in range(args.warmup):
-        st.oracle_step(threads, rows=n)
+        st.run(threads, rows=n)
     times, kv = [], 0
     for _ in range(args.steps):
         t0 = time.perf_counter()
-        kv = st.oracle_step(threads, rows=n)
+        kv = st.run(threads, rows=n)
         times.append(time.perf_counter() - t0)
     dt = statistics.mean(times) if times else float("nan")
     value = kv / dt / 1e9
@@ -870,8 +971,10 @@ def run_reference(args):
         "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (same seeded workload as the native arm)",
-        "config": {"workload": st.description, "num_seqs_sampled": n, "num_heads": s.num_heads,
-                   "num_kv_heads": s.num_kv_heads, "head_dim": s.head_dim, "block_size": s.block_size},
+        "config": {"workload": st.description, "num_seqs": s.num_seqs, "num_heads": s.num_heads,
+                   "num_kv_heads": s.num_kv_heads, "head_dim": s.head_dim, "block_size": s.block_size,
+                   "window": st.window, "block_order": args.table, "kv_format": args.kv_format},
+        "sequences_sampled_per_step": n,
         "impl": "reference",
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
                          "sample": sample},

@@ -34,8 +34,18 @@
  * caller unless stated otherwise; the library allocates nothing, keeps no
  * per-call state and never synchronises: all work is enqueued on `stream`
  * (a cudaStream_t; NULL means the legacy default stream).  The functions are
- * thread-safe.  The only state is a per-device cache of SM count and kernel
- * occupancy, filled on first use.
+ * thread-safe.  The library's state: a per-device cache of SM count and
+ * kernel occupancy, filled on first use, and a pool of item counters in
+ * device memory (module scope, zero when the library loads).  A decode
+ * kernel that claims its items from a counter takes a {next item, CTAs done}
+ * pair for its launch and its last CTA returns it to zero.  Eager launches
+ * take pairs round-robin from 4096, so at most 4096 decode launches may be in
+ * flight at once.  A launch captured into a CUDA graph keeps its pair for
+ * every replay, so it takes one of another 4096 pairs for good (no eager or
+ * other captured launch ever shares it); once those are spent, captured
+ * launches schedule their items statically (the same results).  Two
+ * instances of one captured graph must not run at the same time (they would
+ * share the counter, as they share out and the workspace).
  *
  * Layouts (row-major, densely packed):
  *   q, out           [num_seqs][num_heads][head_dim]
@@ -198,7 +208,9 @@ PA_API size_t pa_decode_shared_prefix_workspace_size(int num_seqs, int num_heads
  * pa_decode_noalloc_max_scratch() bytes (32 MiB), which every GPU that loads
  * the library holds until the process exits.
  *  - A shape whose pa_decode_workspace_size() exceeds that size is rejected
- *    with PA_ERR_WORKSPACE_TOO_SMALL before anything is launched.
+ *    with PA_ERR_WORKSPACE_TOO_SMALL before anything is launched, once every
+ *    other argument has passed pa_decode's checks (a bad argument is
+ *    reported as itself first).
  *  - The first call on a device looks up the array's device address
  *    (cudaGetSymbolAddress, with that device current) and caches it; make
  *    that first call before any stream capture.

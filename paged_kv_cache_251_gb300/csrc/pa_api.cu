@@ -261,18 +261,30 @@ void set_last_error_detail(const char *why) { g_detail = why; }
 
 // Item counters for the kernels that claim their items (DecodeParams::work):
 // zero when the module loads, and every launch returns its pair to zero.
-// Launches take pairs round-robin, so launches in flight at the same time (up
-// to kWorkSlots) never share one.
+// Eager launches take pairs round-robin from the first kWorkSlots, so
+// launches in flight at the same time (up to kWorkSlots of them) never share
+// one.  A launch captured into a CUDA graph keeps its pair for every replay,
+// so it takes one of the next kCapturedSlots pairs for good: no eager launch
+// and no other captured launch ever gets it.  Once those are spent, captured
+// launches run without a counter (each CTA takes a fixed stride of items:
+// the same results, less even balance).
 constexpr int kWorkSlots = 4096;
+constexpr int kCapturedSlots = 4096;
 constexpr int kMaxDevices = 64;
-__device__ unsigned int g_work[2 * kWorkSlots];
+__device__ unsigned int g_work[2 * (kWorkSlots + kCapturedSlots)];
 
-unsigned int *work_counter(int device) {
+unsigned int *work_counter(int device, cudaStream_t stream) {
     static unsigned int *base[kMaxDevices] = {};
     static std::mutex mu;
     static std::atomic<unsigned int> next{0};
+    static std::atomic<int> next_captured[kMaxDevices] = {};
     if (device < 0 || device >= kMaxDevices)
         return nullptr;
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return nullptr;  // status unknown: no counter
+    }
     {
         std::lock_guard<std::mutex> lock(mu);
         if (!base[device]) {
@@ -281,6 +293,10 @@ unsigned int *work_counter(int device) {
                 return nullptr;
             base[device] = static_cast<unsigned int *>(ptr);
         }
+    }
+    if (cap != cudaStreamCaptureStatusNone) {
+        const int k = next_captured[device].fetch_add(1);
+        return k < kCapturedSlots ? base[device] + 2 * (kWorkSlots + k) : nullptr;
     }
     return base[device] + 2 * (next.fetch_add(1u) % kWorkSlots);
 }
@@ -376,7 +392,7 @@ pa_status launch_decode_kernel(DecodeParams &p, int dtype, int head_dim, int G, 
     // CTAs; with a CTA for every item, each takes its own (no atomic on the
     // path of a small, latency-bound launch)
     if ((gqa_tc || mha) && items_max > grid)
-        p.work = work_counter(dev);
+        p.work = work_counter(dev, cs);
     void *args_gqa[] = {&p, &tmk, &tmv, &tmq};
     void *args_mha[] = {&p, &tmk, &tmv};
     void *args[] = {&p};
@@ -434,7 +450,7 @@ pa_status launch_decode_q8_kernel(DecodeParams &p, int cache_dtype, int head_dim
         // mixed lengths) when there are more items than CTAs; otherwise each
         // CTA takes its own
         if (items_max > grid)
-            p.work = work_counter(dev);
+            p.work = work_counter(dev, cs);
         void *args[] = {&p, &tmk, &tmv, &tsk, &tsv};
         e = cudaLaunchKernel(tfn, dim3(static_cast<unsigned>(grid)), dim3(kQ8tThreads), args, smem, cs);
         if (e != cudaSuccess)
@@ -474,7 +490,7 @@ pa_status launch_decode_q8_kernel(DecodeParams &p, int cache_dtype, int head_dim
         if (grid < 1)
             grid = 1;
         if (items_max > grid)
-            p.work = work_counter(dev);  // items claimed from a per-launch counter
+            p.work = work_counter(dev, cs);  // items claimed from a per-launch counter
         void *args[] = {&p};
         e = cudaLaunchKernel(ffn, dim3(static_cast<unsigned>(grid)), dim3(kQ8fThreads), args, smem, cs);
         if (e != cudaSuccess)

@@ -70,6 +70,14 @@ extern "C" pa_status pa_decode_noalloc(void *out, const void *q, const void *k_c
     const size_t need = pa_decode_workspace_size(num_seqs, num_heads, head_dim, block_size, max_blocks_per_seq,
                                                  window, partition_size);
     if (need > kNoAllocScratchBytes) {
+        // pa_decode without a workspace checks every other argument first and
+        // launches nothing: a bad argument is reported as itself, and only a
+        // valid call comes back as too large for the scratch
+        const pa_status st = pa_decode(out, q, k_cache, v_cache, block_tables, context_lens, num_seqs, num_heads,
+                                       num_kv_heads, head_dim, block_size, scale, window, dtype, out_dtype,
+                                       max_blocks_per_seq, num_blocks, partition_size, nullptr, 0, err_word, stream);
+        if (st != PA_ERR_WORKSPACE_TOO_SMALL)
+            return st;
         const std::string why = "pa_decode_noalloc needs " + std::to_string(need) +
                                 " bytes of scratch for this shape; its built-in scratch holds " +
                                 std::to_string(kNoAllocScratchBytes) +

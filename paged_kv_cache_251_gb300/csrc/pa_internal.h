@@ -45,7 +45,7 @@ const void *decode_q8t_kernel_e4m3(int group, int block_size);
 // A zeroed {next item, CTAs done} counter pair for one launch on `device` of
 // a kernel that claims its items (the launch returns it to zero); nullptr if
 // unavailable.
-unsigned int *work_counter(int device);
+unsigned int *work_counter(int device, cudaStream_t stream);
 
 cudaError_t launch_append(const void *k, const void *v, const int64_t *slots, void *k_cache, void *v_cache,
                           int num_tokens, int num_kv_heads, int row_bytes, int block_size, int num_blocks,

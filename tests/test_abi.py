@@ -165,3 +165,37 @@ def test_append_quant_host_validation(lib):
     assert call(sl=0x3004) == 1
     assert call(d=32) == 2
     assert call(bs=4) == 2
+
+
+def test_noalloc_reports_bad_arguments_before_the_scratch_limit(lib):
+    """pa_decode_noalloc on a shape too large for its built-in scratch: a bad
+    argument is reported as itself, and only a valid call comes back as
+    PA_ERR_WORKSPACE_TOO_SMALL (nothing is launched on either path)."""
+    INV, UNS, WS = 1, 2, 3
+    P, I = ctypes.c_void_p, ctypes.c_int
+    f = lib.pa_decode_noalloc
+    f.restype = I
+    f.argtypes = [P, P, P, P, P, P, I, I, I, I, I, ctypes.c_float, I, I, I, I, I, I, P, P]
+    lim = lib.pa_decode_noalloc_max_scratch
+    lim.restype = ctypes.c_size_t
+    ws = lib.pa_decode_workspace_size
+    ws.restype = ctypes.c_size_t
+    ws.argtypes = [I] * 7
+    # 4096 seqs x 64 heads x d 128, 64-token partitions over 512-block rows: far beyond the scratch
+    big = dict(out=0x1000, q=0x2000, k=0x3000, v=0x4000, bt=0x5000, cl=0x6000, N=4096, H=64, Hkv=64, d=128,
+               bs=16, scale=0.088, window=0, dtype=1, out_dtype=0, M=512, nb=64, part=64, err=None, stream=None)
+    assert ws(4096, 64, 128, 16, 512, 0, 64) > lim()
+
+    def call(**o):
+        a = dict(big, **o)
+        return f(a["out"], a["q"], a["k"], a["v"], a["bt"], a["cl"], a["N"], a["H"], a["Hkv"], a["d"], a["bs"],
+                 a["scale"], a["window"], a["dtype"], a["out_dtype"], a["M"], a["nb"], a["part"], a["err"],
+                 a["stream"])
+
+    assert call() == WS
+    assert call(q=0) == INV
+    assert call(k=0x3008) == INV
+    assert call(dtype=9) == INV
+    assert call(H=48, Hkv=16) == UNS               # a group of 3
+    assert call(nb=0) == INV
+    assert call(scale=float("nan")) == INV

@@ -65,3 +65,52 @@ def test_bench_defaults_and_peak_file():
     assert a.gpus == 1 and a.steps >= 1 and a.warmup >= 3 and a.impl == "native"
     peak, kind = bench.hbm_peak()
     assert peak > 1000 and kind in ("measured", "fallback")
+
+
+def test_reference_arm_loads_no_product_code():
+    """bench.py --impl reference runs the oracle on inputs from the seeded
+    generator and the oracle's own block-table models: the CUDA library and
+    its host block manager are never loaded."""
+    import subprocess
+    import sys
+    root = Path(__file__).resolve().parent.parent
+    code = (
+        "import json, sys, io, contextlib, bench\n"
+        "buf = io.StringIO()\n"
+        "with contextlib.redirect_stdout(buf):\n"
+        "    bench.main(['--impl', 'reference', '--workload', 'tiny', '--steps', '1', '--warmup', '1'])\n"
+        "line = json.loads(buf.getvalue().strip().splitlines()[-1])\n"
+        "maps = open('/proc/self/maps').read()\n"
+        "print(json.dumps({'impl': line['impl'], 'value': line['value'],\n"
+        "                  'libpa': 'libpa.so' in maps, 'liboracle': 'liboracle.so' in maps,\n"
+        "                  'mods': [m for m in sys.modules if m.startswith('paged_kv_cache_251_gb300.')]}))\n")
+    r = subprocess.run([sys.executable, "-c", code], cwd=root, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr
+    got = json.loads(r.stdout.strip().splitlines()[-1])
+    assert got["impl"] == "reference" and got["value"] > 0
+    assert got["liboracle"] and not got["libpa"]
+    assert set(got["mods"]) <= {"paged_kv_cache_251_gb300.workloads"}
+
+
+def test_oracle_step_tables_match_the_block_manager():
+    """The reference arm's tables, slots and copy-on-write pairs (oracle
+    models) equal the native arm's (the C++ block manager) on small versions
+    of the window and prefix-sharing workloads, and its append slots equal
+    the block tables' translation of position L."""
+    from paged_kv_cache_251_gb300 import scenarios
+    ws = scenarios.window_state(context=4096, window=1024)
+    slots, _ = ws.manager.append(list(range(ws.shape.num_seqs)))
+    ost = bench.OracleStep.__new__(bench.OracleStep)
+    import oracle
+    ost.oracle = oracle
+    ost._window(context=4096, window=1024)
+    assert torch.equal(ost.tables[:, :ws.block_tables.shape[1]], ws.block_tables)
+    assert torch.equal(ost.lens, ws.context_lens) and torch.equal(ost.slots, slots)
+    for bs in (8, 32):
+        ps = scenarios.prefix_state(bs, prompts=4, samples=3, prompt_len=100, max_new=40)
+        ost = bench.OracleStep.__new__(bench.OracleStep)
+        ost.oracle = oracle
+        ost._prefix(bs, False, prompts=4, samples=3, prompt_len=100, max_new=40)
+        assert torch.equal(ost.tables, ps.block_tables) and torch.equal(ost.lens, ps.context_lens)
+        assert torch.equal(ost.slots, ps.slots) and torch.equal(ost.pairs, ps.pairs)
+        assert (ost.pairs.shape[0] > 0) == (100 % bs != 0)

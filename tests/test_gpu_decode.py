@@ -231,6 +231,55 @@ def test_concurrent_launches_on_two_streams():
     compare(cases[0][2].cpu(), oracle_decode(cases[0][0]), torch.bfloat16)
 
 
+def test_graph_replays_overlap_more_than_4096_eager_launches():
+    """A decode captured in a CUDA graph keeps its item counter for every
+    replay, and eager launches take theirs round-robin from 4096 others, so
+    the two never share one.  The graph (the MHA kernel) is replayed 100
+    times on one stream while 4200 eager decodes (the tensor-core kernel; more
+    launches than round-robin counters) run on another: every replay's output
+    equals the eager result of the same inputs bit for bit, and both match
+    the oracle."""
+    from paged_kv_cache_251_gb300 import pa
+    lens = [(37 * i * i + 300 * i) % 2100 + 1 for i in range(64)]   # more items than CTAs: counters in use
+    cases = []
+    for hkv, seed in ((32, 41), (8, 43)):
+        inp = make_inputs(shape("overlap", 64, 32, hkv, 128, 16, torch.bfloat16, seed=seed), lens)
+        dev = to_cuda(inp)
+        out = torch.empty(dev["q"].shape, dtype=torch.float32, device="cuda")
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        ws = pa.workspace_for(dev["q"], 16, dev["block_tables"].shape[1])
+        cases.append((inp, dev, out, err, ws, hkv))
+
+    def call(c):
+        inp, dev, out, err, ws, hkv = c
+        pa.pa_decode(out, dev["q"], dev["k_cache"], dev["v_cache"], dev["block_tables"], dev["context_lens"],
+                     num_kv_heads=hkv, workspace=ws, err_word=err)
+
+    call(cases[0])
+    torch.cuda.synchronize()
+    ref_a = cases[0][2].clone()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        call(cases[0])
+    sa, sb = torch.cuda.Stream(), torch.cuda.Stream()
+    worst = torch.zeros((), dtype=torch.float32, device="cuda")
+    sa.wait_stream(torch.cuda.current_stream())
+    sb.wait_stream(torch.cuda.current_stream())
+    for i in range(4200):
+        with torch.cuda.stream(sb):
+            call(cases[1])
+        if i % 42 == 0:
+            with torch.cuda.stream(sa):
+                cases[0][2].fill_(float("nan"))
+                graph.replay()
+                torch.maximum(worst, (cases[0][2] - ref_a).abs().amax().nan_to_num(float("inf")), out=worst)
+    torch.cuda.synchronize()
+    assert float(worst.item()) == 0.0
+    assert int(cases[0][3].item()) == 0 and int(cases[1][3].item()) == 0
+    compare(ref_a.cpu(), oracle_decode(cases[0][0]), torch.bfloat16)
+    compare(cases[1][2].cpu(), oracle_decode(cases[1][0]), torch.bfloat16)
+
+
 def test_full_opt13b_batch_is_repeatable():
     """The MHA kernel on the full OPT-13B-shaped batch (items claimed from a
     counter), decoded twelve times: block j of every item is summed by
