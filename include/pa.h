@@ -146,7 +146,10 @@ PA_API size_t pa_decode_workspace_size(int num_seqs, int num_heads, int head_dim
  *                 context_lens[s] <= max_blocks_per_seq * block_size
  *   num_blocks    pool size, for the bounds check of table entries
  *   partition_size  tokens per context partition, a multiple of block_size,
- *                 at most 256 blocks; 0 = default (512 tokens)
+ *                 at most 256 blocks; 0 = default: 1024 tokens for grouped
+ *                 heads (2, 4 or 8 per kv head) with fp16 / bf16 K/V and
+ *                 head_dim 128 (the tensor-core kernel), else 512 tokens
+ *                 (pa_decode_workspace_size with 0 covers both)
  *   workspace, workspace_bytes  scratch of at least pa_decode_workspace_size()
  *                 bytes (may be NULL when that size is 0)
  *   err_word      device uint32 or NULL

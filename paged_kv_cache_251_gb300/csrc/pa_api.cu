@@ -218,10 +218,25 @@ pa_status q8_page_tensor_map(CUtensorMap *map, const void *base, int block_size,
 }
 
 constexpr int kDefaultPartition = 512;
+// The tensor-core grouped-head kernel pays more per item (query load, the
+// merge of its four quarters, partials): its default partition is twice as
+// long.  pa_decode_workspace_size(..., 0) sizes for the shorter one, which
+// needs at least as much.
+constexpr int kGqaDefaultPartition = 1024;
 constexpr int kQ8fStageBudget = 48 * 1024;
 constexpr int kMhaStageBudget = 64 * 1024;
 constexpr int kGqaStages = 3;
 constexpr int kStageBudget = 48 * 1024;
+
+// Whether pa_decode of this shape takes the tensor-core grouped-head kernel
+// (16-bit K/V, head_dim 128, query groups of 2, 4 or 8; the pool and batch
+// size limits of launch_decode_kernel aside).
+bool gqa_tensor_core_path(int num_heads, int num_kv_heads, int head_dim, int dtype) {
+    if (num_kv_heads <= 0 || num_heads % num_kv_heads != 0)
+        return false;
+    const int G = num_heads / num_kv_heads;
+    return (G == 2 || G == 4 || G == 8) && head_dim == 128 && (dtype == PA_F16 || dtype == PA_BF16);
+}
 
 struct DecodePlan {
     int bpp = 0;
@@ -548,6 +563,8 @@ pa_status pa_decode(void *out, const void *q, const void *k_cache, const void *v
                     int max_blocks_per_seq, int num_blocks, int partition_size, void *workspace,
                     size_t workspace_bytes, uint32_t *err_word, pa_stream_t stream) {
     g_detail.clear();
+    if (partition_size == 0 && gqa_tensor_core_path(num_heads, num_kv_heads, head_dim, dtype))
+        partition_size = kGqaDefaultPartition;
     DecodePlan plan;
     pa_status st = plan_decode(num_seqs, num_heads, head_dim, block_size, max_blocks_per_seq, window,
                                partition_size, &plan);
@@ -728,6 +745,8 @@ pa_status pa_decode_quant(void *out, const void *q, const void *k_cache, const v
                           int max_blocks_per_seq, int num_blocks, int partition_size, void *workspace,
                           size_t workspace_bytes, uint32_t *err_word, pa_stream_t stream) {
     g_detail.clear();
+    if (partition_size == 0 && gqa_tensor_core_path(num_heads, num_kv_heads, head_dim, dtype))
+        partition_size = kGqaDefaultPartition;
     DecodePlan plan;
     pa_status st = plan_decode(num_seqs, num_heads, head_dim, block_size, max_blocks_per_seq, window,
                                partition_size, &plan);

@@ -30,6 +30,7 @@ namespace pa {
 namespace {
 
 constexpr int kDefaultPartitionTokens = 512;
+constexpr int kGqaDefaultPartitionTokens = 1024;  // the prefix pass (tensor-core kernel)
 
 __global__ void __launch_bounds__(256)
     prefix_prep_kernel(const int32_t *__restrict__ context_lens, const int32_t *__restrict__ shared_lens,
@@ -305,6 +306,13 @@ extern "C" pa_status pa_decode_shared_prefix(void *out, const void *q, const voi
     pre.num_kv_heads = num_kv_heads;
     pre.part_acc = reinterpret_cast<float *>(ws + pl.pre_off);
     pre.part_ml = pre.part_acc + acc_floats;
+    if (partition_size == 0) {
+        // the prefix pass runs the tensor-core grouped-head kernel: its default
+        // partition is twice as long (fewer partials; the region sized for the
+        // shorter one holds them with its own row stride)
+        pre.bpp = kGqaDefaultPartitionTokens / block_size;
+        pre.max_parts = (pre.max_blocks_per_seq / group_size + pre.bpp - 1) / pre.bpp;
+    }
     pa_status st = launch_decode_kernel(pre, dtype, head_dim, Gp, cs);
     if (st != PA_OK)
         return st;
