@@ -318,7 +318,10 @@ PA_API pa_status pa_append_kv_quant(const void *k, const void *v, const int64_t 
  * pa_decode over an 8-bit cache: the same attention with every cached
  * element read as code * scale of its row.  q (dtype PA_F32 / PA_F16 /
  * PA_BF16) and out as pa_decode; cache_dtype PA_I8 or PA_E4M3; the workspace
- * is pa_decode_workspace_size() bytes, as for pa_decode.
+ * is pa_decode_workspace_size() bytes, as for pa_decode.  partition_size 0
+ * selects 1024 tokens for E4M3 pages with fp16 / bf16 queries in groups of 2
+ * or 4, head_dim 128, block size 16 or 32 and a multiple of 4 kv heads (the
+ * tensor-core kernel), else 512 tokens.
  */
 PA_API pa_status pa_decode_quant(void *out, const void *q, const void *k_cache, const void *v_cache,
                                  const int32_t *block_tables, const int32_t *context_lens, int num_seqs,

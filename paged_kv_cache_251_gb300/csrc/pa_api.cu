@@ -218,9 +218,9 @@ pa_status q8_page_tensor_map(CUtensorMap *map, const void *base, int block_size,
 }
 
 constexpr int kDefaultPartition = 512;
-// The tensor-core grouped-head kernel pays more per item (query load, the
-// merge of its four quarters, partials): its default partition is twice as
-// long.  pa_decode_workspace_size(..., 0) sizes for the shorter one, which
+// The tensor-core kernels (grouped heads over 16-bit K/V, and over E4M3
+// pages) pay more per item (query load, the merge of the quarters, partials):
+// their default partition is twice as long.  pa_decode_workspace_size(..., 0) sizes for the shorter one, which
 // needs at least as much.
 constexpr int kGqaDefaultPartition = 1024;
 constexpr int kQ8fStageBudget = 48 * 1024;
@@ -236,6 +236,18 @@ bool gqa_tensor_core_path(int num_heads, int num_kv_heads, int head_dim, int dty
         return false;
     const int G = num_heads / num_kv_heads;
     return (G == 2 || G == 4 || G == 8) && head_dim == 128 && (dtype == PA_F16 || dtype == PA_BF16);
+}
+
+// Whether pa_decode_quant of this shape takes the tensor-core E4M3 kernel
+// (the pool and batch size limits of launch_decode_q8_kernel aside).
+bool q8t_tensor_core_path(int num_heads, int num_kv_heads, int head_dim, int block_size, int q_dtype,
+                          int cache_dtype) {
+    if (num_kv_heads <= 0 || num_heads % num_kv_heads != 0)
+        return false;
+    const int G = num_heads / num_kv_heads;
+    return cache_dtype == PA_E4M3 && head_dim == 128 && G >= 2 && G <= kQ8tMaxG &&
+           (block_size == 16 || block_size == 32) && num_kv_heads % kQ8tHeads == 0 &&
+           (q_dtype == PA_F16 || q_dtype == PA_BF16);
 }
 
 struct DecodePlan {
@@ -326,7 +338,7 @@ static cudaError_t launch_reduce(DecodeParams &p, int head_dim, long long rows, 
     const bool wide = rows < 8LL * sms || p.max_parts > 32;
     void *args[] = {&p};
     const long long grid = wide ? rows : (rows + kReduceRows - 1) / kReduceRows;
-    return cudaLaunchKernel(reduce_kernel(head_dim, wide), dim3(static_cast<unsigned>(grid)),
+    return launch_dependent(reduce_kernel(head_dim, wide), dim3(static_cast<unsigned>(grid)),
                             dim3(wide ? kReduceWideThreads : kReduceThreads), args, 0, cs);
 }
 
@@ -745,7 +757,8 @@ pa_status pa_decode_quant(void *out, const void *q, const void *k_cache, const v
                           int max_blocks_per_seq, int num_blocks, int partition_size, void *workspace,
                           size_t workspace_bytes, uint32_t *err_word, pa_stream_t stream) {
     g_detail.clear();
-    if (partition_size == 0 && gqa_tensor_core_path(num_heads, num_kv_heads, head_dim, dtype))
+    if (partition_size == 0 &&
+        q8t_tensor_core_path(num_heads, num_kv_heads, head_dim, block_size, dtype, cache_dtype))
         partition_size = kGqaDefaultPartition;
     DecodePlan plan;
     pa_status st = plan_decode(num_seqs, num_heads, head_dim, block_size, max_blocks_per_seq, window,

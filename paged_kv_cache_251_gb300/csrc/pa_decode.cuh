@@ -76,25 +76,20 @@ struct DecodeParams {
 struct ItemClaim {
     long long w = 0;        // the current item
     unsigned int ahead = 0;  // the next one (lane 0)
+    // the first item is the CTA's own (no round trip before the first copy);
+    // the counter numbers the later ones from gridDim.x up
     __device__ void start(const DecodeParams &p) {
         const int lane = threadIdx.x & 31;
-        if (p.work) {
-            unsigned int v = 0;
-            if (lane == 0)
-                v = atomicAdd(p.work, 1u);
-            w = __shfl_sync(0xffffffffu, v, 0);
-            if (lane == 0)
-                ahead = atomicAdd(p.work, 1u);
-        } else {
-            w = blockIdx.x;
-        }
+        w = blockIdx.x;
+        if (p.work && lane == 0)
+            ahead = gridDim.x + atomicAdd(p.work, 1u);
     }
     __device__ void next(const DecodeParams &p) {
         const int lane = threadIdx.x & 31;
         if (p.work) {
             w = __shfl_sync(0xffffffffu, ahead, 0);
             if (lane == 0)
-                ahead = atomicAdd(p.work, 1u);
+                ahead = gridDim.x + atomicAdd(p.work, 1u);
         } else {
             w += gridDim.x;
         }
@@ -654,6 +649,7 @@ __device__ inline void decode_consumer(const DecodeParams &p, char *smem, const 
 
 template <typename T, int D, int G>
 __global__ void __launch_bounds__(kDecodeThreads) pa_decode_kernel(const DecodeParams p) {
+    pdl_launch_dependents();  // the partition merge may be launched now (it waits for this grid)
     extern __shared__ __align__(128) char smem[];
     using C = DecodeCfg<T, D, G>;
     const SmemLayout L = decode_smem_layout(p.stages, p.block_size * C::kRow, C::kRow, G, D);
@@ -698,6 +694,7 @@ constexpr int kReduceRows = kReduceThreads / 32;
 template <int D>
 __global__ void __launch_bounds__(kReduceThreads) pa_reduce_kernel(const DecodeParams p) {
     // (the host takes this layout only for max_parts <= 32: lane q holds partition q)
+    pdl_wait();
     constexpr int kPer = D / 32;  // head_dim slice per lane (4 or 2)
     constexpr int kBatch = 8;     // partitions whose slices are loaded before any is used
     const int lane = threadIdx.x & 31;
@@ -766,6 +763,7 @@ __global__ void __launch_bounds__(kReduceThreads) pa_reduce_kernel(const DecodeP
 
 template <int D>
 __global__ void __launch_bounds__(kReduceWideThreads) pa_reduce_wide_kernel(const DecodeParams p) {
+    pdl_wait();
     constexpr int kWarps = kReduceWideThreads / 32;
     constexpr int kPer = D / 32;  // head_dim slice per lane (4 or 2)
     constexpr int kBatch = 8;     // partitions of one warp whose slices are loaded before any is used

@@ -833,6 +833,7 @@ template <typename T, int BS, int G>
 __global__ void __launch_bounds__(kGqaThreads, 1)
     pa_decode_gqa_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmk,
                          const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmq) {
+    pdl_launch_dependents();  // the partition merge may be launched now (it waits for this grid)
     extern __shared__ __align__(1024) char smem_raw[];
     char *smem = reinterpret_cast<char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     using C = GqaCfg<T, BS, G>;

@@ -83,6 +83,7 @@ __global__ void __launch_bounds__(kReduceThreads)
                           int group_size) {
     constexpr int kPer = D / 32;  // head_dim slice per lane (4 or 2)
     constexpr int kBatch = 8;
+    pdl_wait();
     const int lane = threadIdx.x & 31;
     const long long rowi = static_cast<long long>(blockIdx.x) * kReduceRows + (threadIdx.x >> 5);  // s * H + h
     if (rowi >= static_cast<long long>(suf.num_seqs) * suf.num_heads)
@@ -335,9 +336,11 @@ extern "C" pa_status pa_decode_shared_prefix(void *out, const void *q, const voi
 
     // 4) merge
     const long long rows = static_cast<long long>(num_seqs) * num_heads;
-    prefix_combine_kernel<128><<<static_cast<unsigned>((rows + kReduceRows - 1) / kReduceRows), kReduceThreads, 0,
-                                 cs>>>(pre, suf, shared_eff, group_size);
-    e = cudaGetLastError();
+    int gs = group_size;
+    void *cargs[] = {&pre, &suf, &shared_eff, &gs};
+    e = launch_dependent(reinterpret_cast<const void *>(&prefix_combine_kernel<128>),
+                         dim3(static_cast<unsigned>((rows + kReduceRows - 1) / kReduceRows)), dim3(kReduceThreads),
+                         cargs, 0, cs);
     if (e != cudaSuccess)
         return bad(PA_ERR_CUDA, "shared-prefix combine launch failed");
     return PA_OK;

@@ -387,12 +387,13 @@ __device__ inline bool q8t_qconvert(const DecodeParams &p, char *smem, const Q8t
         const int slot = static_cast<int>(k % kQ8tItemSlots);
         if (!mbar_wait_bounded(&iempty[slot], static_cast<uint32_t>((k / kQ8tItemSlots) & 1) ^ 1u))
             return false;
-        // the next item: from the launch's shared counter (each CTA takes the
-        // next unclaimed one when it has room), else round-robin
-        if (p.work) {
+        // the next item: the CTA's own first, then from the launch's shared
+        // counter (each CTA takes the next unclaimed one when it has room;
+        // the counter numbers them from gridDim.x up), else round-robin
+        if (p.work && k > 0) {
             unsigned int v = 0;
             if (lane == 0)
-                v = atomicAdd(p.work, 1u);
+                v = gridDim.x + atomicAdd(p.work, 1u);
             w = __shfl_sync(0xffffffffu, v, 0);
         } else if (k > 0) {
             w += gridDim.x;
@@ -898,6 +899,7 @@ __global__ void __launch_bounds__(kQ8tThreads, 1)
     pa_decode_q8t_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmk,
                          const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tsk,
                          const __grid_constant__ CUtensorMap tsv) {
+    pdl_launch_dependents();  // the partition merge may be launched now (it waits for this grid)
     extern __shared__ __align__(1024) char smem_raw[];
     char *smem = reinterpret_cast<char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     using C = Q8tCfg<BS, G>;

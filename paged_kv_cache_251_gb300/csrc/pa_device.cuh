@@ -65,6 +65,14 @@ __device__ inline uint32_t smem_addr(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// Programmatic dependent launch: a decode kernel lets the kernel that merges
+// its partials be launched while it runs (launch_dependents, once per CTA at
+// its start); that kernel, launched with programmatic stream serialization,
+// waits for the whole decode grid and its memory (wait) before it reads
+// anything.  Both are no-ops without such a launch.
+__device__ inline void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ inline void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ inline uint64_t globaltimer_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

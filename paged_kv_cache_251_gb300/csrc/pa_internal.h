@@ -10,6 +10,25 @@ namespace pa {
 
 struct DecodeParams;
 
+// Launch `fn` so that it may be scheduled while the kernel before it on
+// `stream` still runs (programmatic stream serialization; that kernel signals
+// launch_dependents).  `fn` must execute griddepcontrol.wait before it reads
+// anything the earlier kernel writes.
+inline cudaError_t launch_dependent(const void *fn, dim3 grid, dim3 block, void **args, size_t smem,
+                                    cudaStream_t stream) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelExC(&cfg, fn, args);
+}
+
 // Decode kernel entry (as a function pointer for cudaLaunchKernel) for one
 // element type, head_dim and query-group size; nullptr if not built.
 const void *decode_kernel_f32(int head_dim, int group);
