@@ -61,8 +61,10 @@ def parse_args(argv=None):
     ap.add_argument("--partition", type=int, default=0, help="pa_decode partition_size (0 = default)")
     ap.add_argument("--shared-prefix", action="store_true",
                     help="prefix workloads: decode with pa_decode_shared_prefix (shared blocks read once per group)")
-    ap.add_argument("--table", choices=["shuffled", "identity"], default="shuffled",
-                    help="block hand-out order (identity: each sequence's blocks adjacent in memory)")
+    ap.add_argument("--table", choices=["shuffled", "identity", "contiguous"], default="shuffled",
+                    help="block hand-out order (identity: each sequence's blocks adjacent in memory; contiguous: "
+                         "the same values in non-paged [N][H_kv][L][d] caches decoded by pa_decode_contiguous, "
+                         "no block table and no append; opt13b / gqa / tiny_scaled)")
     ap.add_argument("--kv-format", choices=["native", "int8", "e4m3"], default="native",
                     help="opt13b / gqa / tiny_scaled: 8-bit cache (codes + one fp32 scale per row), decoded by "
                          "pa_decode_quant and appended by pa_append_kv_quant")
@@ -418,7 +420,7 @@ class DecodeAppendStep(Step):
 
     kv_format = None
 
-    def __init__(self, name, device, partition, shuffle=True, kv_format="native"):
+    def __init__(self, name, device, partition, shuffle=True, kv_format="native", contiguous=False):
         super().__init__(device, partition)
         self.kv_format = None if kv_format == "native" else kv_format
         from paged_kv_cache_251_gb300 import pa
@@ -472,9 +474,40 @@ class DecodeAppendStep(Step):
         T = inp.k_new.shape[0]
         self.append_bytes = (acc.append_quant_bytes(T, s.num_kv_heads, s.head_dim, elt) if self.kv_format else
                              acc.append_bytes(T, s.num_kv_heads, s.head_dim, elt))
+        self.contiguous = contiguous
+        if contiguous:
+            self._to_contiguous()
+
+    def _to_contiguous(self):
+        """The pool's values gathered into contiguous caches [N][H_kv][L][d]
+        (L = the table width in tokens): decode reads them with no block
+        table; the step has no append (its slots belong to the paged pool)."""
+        s = self.shape
+        bs = s.block_size
+        L = self.bt.shape[1] * bs
+        held = self.inp.blocks_held.tolist()
+        self.kc = torch.zeros((s.num_seqs, s.num_kv_heads, L, s.head_dim), dtype=s.dtype, device=self.device)
+        self.vc = torch.zeros_like(self.kc)
+        for i in range(s.num_seqs):
+            blocks = self.bt[i, :held[i]].long()
+            for src, dst in ((self.k_cache, self.kc), (self.v_cache, self.vc)):
+                dst[i, :, :held[i] * bs] = src[blocks].permute(1, 0, 2, 3).reshape(s.num_kv_heads, -1, s.head_dim)
+        from paged_kv_cache_251_gb300 import accounting as acc
+        n = self.pa.pa_decode_workspace_size(s.num_seqs, s.num_heads, s.head_dim, 16, L // 16, 0, self.partition)
+        self.ws_c = None if n == 0 else torch.empty((n + 15) // 16 * 4, dtype=torch.float32, device=self.device)
+        self.append_bytes = 0
+        self.launches = 2 if self.ws_c is not None else 1
+        self.description += ("; contiguous caches [N][H_kv][L][d] holding the same values, decoded by "
+                             "pa_decode_contiguous (no block table); no append")
 
     def decode(self, stream, q=None, bt=None, cl=None):
         s = self.shape
+        if getattr(self, "contiguous", False):
+            self.pa.pa_decode_contiguous(self.out, self.q if q is None else q, self.kc, self.vc,
+                                         self.cl if cl is None else cl, num_kv_heads=s.num_kv_heads,
+                                         partition_size=self.partition, workspace=self.ws_c, err_word=self.err,
+                                         stream=stream)
+            return
         if self.kv_format:
             self.pa.pa_decode_quant(self.out, self.q if q is None else q, self.kq, self.vq,
                                     self.bt if bt is None else bt, self.cl if cl is None else cl,
@@ -487,6 +520,8 @@ class DecodeAppendStep(Step):
                           stream=stream)
 
     def post(self, stream, k_new=None, v_new=None, slots=None):
+        if getattr(self, "contiguous", False):
+            return
         kn = self.k_new if k_new is None else k_new
         vn = self.v_new if v_new is None else v_new
         sl = self.slots if slots is None else slots
@@ -650,8 +685,11 @@ WORKLOADS = ["opt13b", "gqa", "window", "prefix_bs8", "prefix_bs16", "prefix_bs3
 
 
 def make_step(name, device, partition, table="shuffled", shared=False, kv_format="native"):
+    if table == "contiguous" and (name not in ("opt13b", "gqa", "tiny_scaled") or kv_format != "native"):
+        raise SystemExit("--table contiguous applies to the 16/32-bit opt13b, gqa and tiny_scaled workloads")
     if name in ("opt13b", "gqa", "tiny", "tiny_scaled"):
-        return DecodeAppendStep(name, device, partition, shuffle=(table == "shuffled"), kv_format=kv_format)
+        return DecodeAppendStep(name, device, partition, shuffle=(table == "shuffled"), kv_format=kv_format,
+                                contiguous=(table == "contiguous"))
     if kv_format != "native":
         raise SystemExit("--kv-format applies to the opt13b, gqa, tiny and tiny_scaled workloads")
     if name == "window":

@@ -234,6 +234,28 @@ PA_API pa_status pa_decode_noalloc(void *out, const void *q, const void *k_cache
 PA_API size_t pa_decode_noalloc_max_scratch(void);
 
 /*
+ * Decode attention over CONTIGUOUS (non-paged) caches, the baseline for the
+ * cost of the block table [B 踩过的坑: the lookup makes the attention kernel
+ * 20-26% slower].  The same attention as pa_decode (window, partitions,
+ * output dtypes, error word), with no block table: sequence s's token t of
+ * kv head h is row t of
+ *   k_cache, v_cache [num_seqs][num_kv_heads][max_context_len][head_dim].
+ * The kernels are pa_decode's (one query head per kv head: the MHA kernel;
+ * 2, 4 or 8 with fp16 / bf16 K/V and head_dim 128: the tensor-core kernel,
+ * which moves each 128-token tile of a kv head with one copy); the cache is
+ * cut into 16-token blocks, so max_context_len must be a positive multiple of
+ * 16 and the workspace is pa_decode_workspace_size(num_seqs, num_heads,
+ * head_dim, 16, max_context_len / 16, window, partition_size) bytes.  Other
+ * shapes return PA_ERR_UNSUPPORTED.  context_lens[s] > max_context_len is
+ * clamped and flagged (PA_DEVERR_BAD_LEN).
+ */
+PA_API pa_status pa_decode_contiguous(void *out, const void *q, const void *k_cache, const void *v_cache,
+                                      const int32_t *context_lens, int num_seqs, int num_heads, int num_kv_heads,
+                                      int head_dim, int max_context_len, float scale, int window, pa_dtype dtype,
+                                      pa_dtype out_dtype, int partition_size, void *workspace,
+                                      size_t workspace_bytes, uint32_t *err_word, pa_stream_t stream);
+
+/*
  * Append [B 核心要点, 案例 2]: for every token i with slot = slot_mapping[i] >= 0
  *   k_cache[slot / block_size][h][slot % block_size][:] = k[i][h][:]   (all h)
  *   v_cache[...] = v[i][h][:]

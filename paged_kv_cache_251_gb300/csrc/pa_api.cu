@@ -151,9 +151,11 @@ pa_status kv_tensor_map(CUtensorMap *map, const void *base, int dtype, int head_
 
 // 5-D view of a 16-bit K or V cache with head_dim 128 for the tensor-core
 // kernel: [tile = block * H_kv + head][row / 8][half][row % 8][64 elements];
-// one box is a whole (block, head) tile and lands in shared memory as 8-row
-// groups of both 128-byte halves (128-byte swizzle).
-pa_status kv_tensor_map_groups(CUtensorMap *map, const void *base, int dtype, int block_size, long long tiles) {
+// one box is `box_tiles` consecutive whole (block, head) tiles (1 for a paged
+// cache; a contiguous cache's tiles of one kv head are consecutive) and lands
+// in shared memory as 8-row groups of both 128-byte halves (128-byte swizzle).
+pa_status kv_tensor_map_groups(CUtensorMap *map, const void *base, int dtype, int block_size, long long tiles,
+                               int box_tiles = 1) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
     cudaError_t e = tensor_map_encoder(&enc);
     if (e != cudaSuccess || !enc)
@@ -162,7 +164,7 @@ pa_status kv_tensor_map_groups(CUtensorMap *map, const void *base, int dtype, in
     const cuuint64_t row = 256;  // bytes per token row (128 x 2 bytes)
     cuuint64_t dims[5] = {64, 8, 2, static_cast<cuuint64_t>(block_size / 8), static_cast<cuuint64_t>(tiles)};
     cuuint64_t strides[4] = {row, 128, 8 * row, row * block_size};
-    cuuint32_t box[5] = {64, 8, 2, static_cast<cuuint32_t>(block_size / 8), 1};
+    cuuint32_t box[5] = {64, 8, 2, static_cast<cuuint32_t>(block_size / 8), static_cast<cuuint32_t>(box_tiles)};
     cuuint32_t estr[5] = {1, 1, 1, 1, 1};
     CUresult r = enc(map, dt, 5, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -223,6 +225,8 @@ constexpr int kDefaultPartition = 512;
 // their default partition is twice as long.  pa_decode_workspace_size(..., 0) sizes for the shorter one, which
 // needs at least as much.
 constexpr int kGqaDefaultPartition = 1024;
+// The block size contiguous caches are cut into (their tiles: TMA boxes).
+constexpr int kContiguousBlock = 16;
 constexpr int kQ8fStageBudget = 48 * 1024;
 constexpr int kMhaStageBudget = 64 * 1024;
 constexpr int kGqaStages = 3;
@@ -346,7 +350,11 @@ pa_status launch_decode_kernel(DecodeParams &p, int dtype, int head_dim, int G, 
     const int block_size = p.block_size;
     const int row = head_dim * elt_bytes(dtype);
     const int tile = block_size * row;
-    const long long tiles = static_cast<long long>(p.num_blocks) * p.num_kv_heads;
+    // a paged pool holds num_blocks x H_kv tiles; a contiguous cache
+    // num_seqs x H_kv x max_blocks_per_seq
+    const long long tiles = p.contiguous
+                                ? static_cast<long long>(p.num_seqs) * p.num_kv_heads * p.max_blocks_per_seq
+                                : static_cast<long long>(p.num_blocks) * p.num_kv_heads;
     // MHA takes the TMA-tensor kernel; its 3-D tensor map addresses tiles with
     // a 32-bit coordinate, so very large pools use the general kernel.
     const bool mha = (G == 1 && tiles <= INT_MAX);
@@ -356,7 +364,10 @@ pa_status launch_decode_kernel(DecodeParams &p, int dtype, int head_dim, int G, 
     const void *fn;
     size_t smem;
     int threads;
-    CUtensorMap tmk, tmv, tmq;
+    CUtensorMap tmk, tmv, tmq, tmkw, tmvw;
+    if (p.contiguous && !gqa_tc && !mha)
+        return fail(PA_ERR_UNSUPPORTED, "contiguous caches take one query head per kv head, or 2, 4 or 8 with "
+                                        "fp16 / bf16 K/V and head_dim 128");
     if (gqa_tc) {
         fn = dtype == PA_F16 ? decode_gqa_kernel_f16(block_size, G) : decode_gqa_kernel_bf16(block_size, G);
         p.stages = kGqaStages;
@@ -367,6 +378,14 @@ pa_status launch_decode_kernel(DecodeParams &p, int dtype, int head_dim, int G, 
             ts = kv_tensor_map_groups(&tmv, p.v_cache, dtype, block_size, tiles);
         if (ts == PA_OK)
             ts = q_tensor_map(&tmq, p.q, dtype, head_dim, static_cast<long long>(p.num_seqs) * p.num_heads, G);
+        tmkw = tmk;
+        tmvw = tmv;
+        if (ts == PA_OK && p.contiguous) {
+            // a whole 128-token tile of a contiguous cache in one copy
+            ts = kv_tensor_map_groups(&tmkw, p.k_cache, dtype, block_size, tiles, kTileTokens / block_size);
+            if (ts == PA_OK)
+                ts = kv_tensor_map_groups(&tmvw, p.v_cache, dtype, block_size, tiles, kTileTokens / block_size);
+        }
         if (ts != PA_OK)
             return ts;
     } else if (mha) {
@@ -420,7 +439,7 @@ pa_status launch_decode_kernel(DecodeParams &p, int dtype, int head_dim, int G, 
     // path of a small, latency-bound launch)
     if ((gqa_tc || mha) && items_max > grid)
         p.work = work_counter(dev, cs);
-    void *args_gqa[] = {&p, &tmk, &tmv, &tmq};
+    void *args_gqa[] = {&p, &tmk, &tmv, &tmq, &tmkw, &tmvw};
     void *args_mha[] = {&p, &tmk, &tmv};
     void *args[] = {&p};
     e = cudaLaunchKernel(fn, dim3(static_cast<unsigned>(grid)), dim3(threads),
@@ -748,6 +767,88 @@ size_t pa_quant_page_bytes(int head_dim, int block_size) {
     if (!head_dim_ok(head_dim) || !block_size_ok(block_size))
         return 0;
     return static_cast<size_t>(q8_page_bytes(block_size, head_dim));
+}
+
+pa_status pa_decode_contiguous(void *out, const void *q, const void *k_cache, const void *v_cache,
+                               const int32_t *context_lens, int num_seqs, int num_heads, int num_kv_heads,
+                               int head_dim, int max_context_len, float scale, int window, pa_dtype dtype,
+                               pa_dtype out_dtype, int partition_size, void *workspace, size_t workspace_bytes,
+                               uint32_t *err_word, pa_stream_t stream) {
+    g_detail.clear();
+    constexpr int kBs = kContiguousBlock;
+    if (max_context_len <= 0 || max_context_len % kBs != 0)
+        return fail(PA_ERR_INVALID_ARGUMENT, "max_context_len must be a positive multiple of 16");
+    const int mb = max_context_len / kBs;
+    if (partition_size == 0 && gqa_tensor_core_path(num_heads, num_kv_heads, head_dim, dtype))
+        partition_size = kGqaDefaultPartition;
+    DecodePlan plan;
+    pa_status st = plan_decode(num_seqs, num_heads, head_dim, kBs, mb, window, partition_size, &plan);
+    if (st != PA_OK)
+        return st;
+    if (num_seqs == 0)
+        return PA_OK;
+    if (!out || !q || !k_cache || !v_cache || !context_lens)
+        return fail(PA_ERR_INVALID_ARGUMENT, "null pointer");
+    if (num_kv_heads <= 0 || num_heads % num_kv_heads != 0)
+        return fail(PA_ERR_INVALID_ARGUMENT, "num_heads must be a multiple of num_kv_heads");
+    const int G = num_heads / num_kv_heads;
+    if (G != 1 && G != 2 && G != 4 && G != 8)
+        return fail(PA_ERR_UNSUPPORTED, "num_heads / num_kv_heads must be 1, 2, 4 or 8");
+    if (!dtype_ok(dtype) || !dtype_ok(out_dtype))
+        return fail(PA_ERR_INVALID_ARGUMENT, "unknown dtype");
+    if (G > 1 && !gqa_tensor_core_path(num_heads, num_kv_heads, head_dim, dtype))
+        return fail(PA_ERR_UNSUPPORTED, "contiguous caches with grouped heads take fp16 / bf16 K/V and head_dim 128");
+    if (!std::isfinite(scale))
+        return fail(PA_ERR_INVALID_ARGUMENT, "scale must be finite");
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
+        return fail(PA_ERR_INVALID_ARGUMENT, "q, k_cache and v_cache must be 16-byte aligned");
+    if ((reinterpret_cast<uintptr_t>(out) & (elt_bytes(out_dtype) - 1)) != 0)
+        return fail(PA_ERR_INVALID_ARGUMENT, "out is not aligned to its element size");
+    if (static_cast<long long>(num_seqs) * num_kv_heads * mb > INT_MAX)
+        return fail(PA_ERR_UNSUPPORTED, "contiguous cache too large for 32-bit tile indices");
+    if (plan.workspace > 0 && (workspace == nullptr || workspace_bytes < plan.workspace))
+        return fail(PA_ERR_WORKSPACE_TOO_SMALL, "workspace smaller than pa_decode_workspace_size()");
+    if (plan.workspace > 0 && !aligned16(workspace))
+        return fail(PA_ERR_INVALID_ARGUMENT, "workspace must be 16-byte aligned");
+
+    DecodeParams p;
+    p.out = out;
+    p.q = q;
+    p.k_cache = k_cache;
+    p.v_cache = v_cache;
+    p.block_tables = nullptr;  // never read: block b of a sequence is its b-th tile
+    p.context_lens = context_lens;
+    const size_t acc_floats = static_cast<size_t>(num_seqs) * num_heads * plan.max_parts * head_dim;
+    p.part_acc = plan.workspace ? static_cast<float *>(workspace) : nullptr;
+    p.part_ml = plan.workspace ? static_cast<float *>(workspace) + acc_floats : nullptr;
+    p.err = err_word;
+    p.num_seqs = num_seqs;
+    p.num_heads = num_heads;
+    p.num_kv_heads = num_kv_heads;
+    p.block_size = kBs;
+    p.window = window;
+    p.max_blocks_per_seq = mb;
+    p.max_len = max_context_len;
+    p.num_blocks = mb;  // logical block ids stand in for table entries
+    p.bpp = plan.bpp;
+    p.max_parts = plan.max_parts;
+    p.out_dtype = out_dtype;
+    p.stages = 0;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.start_tok = nullptr;
+    p.force_partial = 0;
+    p.q_dtype = dtype;
+    p.contiguous = 1;
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    const pa_status ls = launch_decode_kernel(p, dtype, head_dim, G, cs);
+    if (ls != PA_OK)
+        return ls;
+    if (plan.max_parts > 1) {
+        const cudaError_t e = launch_reduce(p, head_dim, static_cast<long long>(num_seqs) * num_heads, cs);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "reduce launch");
+    }
+    return PA_OK;
 }
 
 pa_status pa_decode_quant(void *out, const void *q, const void *k_cache, const void *v_cache,

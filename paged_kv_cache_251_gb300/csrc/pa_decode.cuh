@@ -66,7 +66,18 @@ struct DecodeParams {
     // done}, zero before the launch and returned to zero by its last CTA;
     // nullptr: items go round-robin over the CTAs.
     unsigned int *work = nullptr;
+    // 1: the caches are contiguous, [num_seqs][num_kv_heads][max_len][D]
+    // (no block table: block b of sequence s and kv head h is tile
+    // (s * num_kv_heads + h) * max_blocks_per_seq + b); the MHA and
+    // tensor-core grouped-head kernels only
+    int contiguous = 0;
 };
+
+// Tile index (into the [tiles][block_size][D] view of a cache) of table entry
+// or logical block `pb` of sequence s and kv head h.
+__device__ inline int kv_tile(const DecodeParams &p, int s, int h, int pb) {
+    return p.contiguous ? (s * p.num_kv_heads + h) * p.max_blocks_per_seq + pb : pb * p.num_kv_heads + h;
+}
 
 // Items of a persistent decode kernel, for its producer warp: from the
 // launch's counter (DecodeParams::work), each claimed one item ahead so the
@@ -182,7 +193,7 @@ __device__ inline void prepare_item(const DecodeParams &p, int block_size, ItemS
 #pragma unroll
     for (int i = 0; i < kMaxBpp / 32; ++i) {
         const int j = lane + 32 * i;
-        n.tb[i] = j < n.nb ? ld_nc_i32(row + j) : -1;
+        n.tb[i] = j < n.nb ? (p.contiguous ? n.blk_lo + j : ld_nc_i32(row + j)) : -1;
     }
 }
 

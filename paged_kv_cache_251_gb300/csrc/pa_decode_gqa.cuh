@@ -67,6 +67,7 @@ template <typename T, int BS, int G> struct GqaCfg {
     static constexpr int kTile = kTileTokens / 8 * kGroupBytes;  // 32 KB
     static constexpr int kBlockBytes = BS * kRow;                // one block: all rows, both halves
     static constexpr int kOpBytes = 2 * 16 * 128;        // Q or P operand: 2 boxes x 16 rows x 128 B
+    static constexpr uint32_t kFullMask = (1u << kBpt) - 1u;  // every block of a tile
     static_assert(sizeof(T) == 2, "tensor-core path takes 16-bit K/V");
     static_assert(G == 2 || G == 4 || G == 8, "query group");
 };
@@ -264,8 +265,8 @@ template <> __device__ inline float from_bits16<__half>(uint16_t b) { return __h
 // ---------------------------------------------------------------------------
 
 template <typename T, int BS, int G>
-__device__ inline void gqa_producer(const DecodeParams &p, const CUtensorMap *tmk, const CUtensorMap *tmq, char *smem,
-                                    const GqaLayout &L) {
+__device__ inline void gqa_producer(const DecodeParams &p, const CUtensorMap *tmk, const CUtensorMap *tmkw,
+                                    const CUtensorMap *tmq, char *smem, const GqaLayout &L) {
     using C = GqaCfg<T, BS, G>;
     const int lane = threadIdx.x & 31;
     const int S = p.stages;
@@ -355,7 +356,10 @@ __device__ inline void gqa_producer(const DecodeParams &p, const CUtensorMap *tm
             const int bj = ti * C::kBpt + lane;
             const bool mine = lane < C::kBpt && bj < nb && tbl[bj] >= 0;
             const uint32_t mask = __ballot_sync(0xffffffffu, mine);
-            const int z = mine ? tbl[bj] * p.num_kv_heads + kvh : 0;
+            const int z = mine ? kv_tile(p, s, kvh, tbl[bj]) : 0;
+            // a contiguous cache holds a whole tile's blocks in consecutive
+            // tiles: one copy brings all of them
+            const bool wide = p.contiguous && mask == C::kFullMask;
             if (lane < C::kBpt)
                 zid[stage * kGqaMaxBpt + lane] = z;
             if (lane == 0) {
@@ -367,9 +371,9 @@ __device__ inline void gqa_producer(const DecodeParams &p, const CUtensorMap *tm
                     mbar_arrive(&kfull[stage]);
             }
             __syncwarp();
-            if (mine)
-                tma_load_5d(stage_buf + static_cast<size_t>(stage) * 2 * C::kTile + lane * C::kBlockBytes, tmk, z,
-                            &kfull[stage], policy);
+            if (wide ? lane == 0 : mine)
+                tma_load_5d(stage_buf + static_cast<size_t>(stage) * 2 * C::kTile + lane * C::kBlockBytes,
+                            wide ? tmkw : tmk, z, &kfull[stage], policy);
             if (lane == 0)
                 mbar_arrive(&zfull[stage]);
             __syncwarp();
@@ -413,7 +417,8 @@ __device__ inline void gqa_producer(const DecodeParams &p, const CUtensorMap *tm
 // then the V copies into the V half of the tile's stage once P V of tile
 // t - S finished.
 template <typename T, int BS, int G>
-__device__ inline void gqa_vproducer(const DecodeParams &p, const CUtensorMap *tmv, char *smem, const GqaLayout &L) {
+__device__ inline void gqa_vproducer(const DecodeParams &p, const CUtensorMap *tmv, const CUtensorMap *tmvw, char *smem,
+                                     const GqaLayout &L) {
     using C = GqaCfg<T, BS, G>;
     const int lane = threadIdx.x & 31;
     const int S = p.stages;
@@ -453,9 +458,10 @@ __device__ inline void gqa_vproducer(const DecodeParams &p, const CUtensorMap *t
                 mbar_arrive(&vfull[stage]);
         }
         __syncwarp();
-        if ((mask >> lane) & 1u)
-            tma_load_5d(stage_buf + static_cast<size_t>(stage) * 2 * C::kTile + C::kTile + lane * C::kBlockBytes, tmv,
-                        z, &vfull[stage], policy);
+        const bool wide = p.contiguous && mask == C::kFullMask;
+        if (wide ? lane == 0 : ((mask >> lane) & 1u) != 0)
+            tma_load_5d(stage_buf + static_cast<size_t>(stage) * 2 * C::kTile + C::kTile + lane * C::kBlockBytes,
+                        wide ? tmvw : tmv, z, &vfull[stage], policy);
         __syncwarp();
     }
     if (!ok && lane == 0) {
@@ -832,7 +838,8 @@ __device__ inline bool gqa_softmax(const DecodeParams &p, char *smem, const GqaL
 template <typename T, int BS, int G>
 __global__ void __launch_bounds__(kGqaThreads, 1)
     pa_decode_gqa_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmk,
-                         const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmq) {
+                         const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmq,
+                         const __grid_constant__ CUtensorMap tmkw, const __grid_constant__ CUtensorMap tmvw) {
     pdl_launch_dependents();  // the partition merge may be launched now (it waits for this grid)
     extern __shared__ __align__(1024) char smem_raw[];
     char *smem = reinterpret_cast<char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -886,9 +893,9 @@ __global__ void __launch_bounds__(kGqaThreads, 1)
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + L.tmem);
 
     if (warp == 0) {
-        gqa_producer<T, BS, G>(p, &tmk, &tmq, smem, L);
+        gqa_producer<T, BS, G>(p, &tmk, &tmkw, &tmq, smem, L);
     } else if (warp == 6) {
-        gqa_vproducer<T, BS, G>(p, &tmv, smem, L);
+        gqa_vproducer<T, BS, G>(p, &tmv, &tmvw, smem, L);
     } else if (warp == 1) {
         bool ok = true;
         if ((threadIdx.x & 31) == 0) {

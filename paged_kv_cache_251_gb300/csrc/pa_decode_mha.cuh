@@ -305,7 +305,7 @@ __device__ inline void mha_producer(const DecodeParams &p, const CUtensorMap *tm
         // block-table slice of the item -> shared memory, entries range-checked
         const int32_t *row = p.block_tables + static_cast<long long>(s) * p.max_blocks_per_seq + blk_lo;
         for (int j = lane; j < nb; j += 32) {
-            int pb = ld_nc_i32(row + j);
+            int pb = p.contiguous ? blk_lo + j : ld_nc_i32(row + j);
             if (pb < 0 || pb >= p.num_blocks) {
                 pb = -1;
                 if (p.err)
@@ -333,7 +333,7 @@ __device__ inline void mha_producer(const DecodeParams &p, const CUtensorMap *tm
                     mbar_arrive_expect_tx(&full[stage], 2 * C::kTile);
                     char *dk = stage_buf + static_cast<size_t>(stage) * 2 * C::kTile;
                     char *dv = dk + C::kTile;
-                    const int z = pb * p.num_kv_heads + kvh;
+                    const int z = kv_tile(p, s, kvh, pb);
                     tma_load_4d(dk, tmk, z, &full[stage], policy);
                     tma_load_4d(dv, tmv, z, &full[stage], policy);
                 } else {

@@ -41,6 +41,8 @@ def _load():
     lib.pa_decode.restype = I
     lib.pa_decode_noalloc.argtypes = [P, P, P, P, P, P, I, I, I, I, I, F, I, I, I, I, I, I, P, P]
     lib.pa_decode_noalloc.restype = I
+    lib.pa_decode_contiguous.argtypes = [P, P, P, P, P, I, I, I, I, I, F, I, I, I, I, P, SZ, P, P]
+    lib.pa_decode_contiguous.restype = I
     lib.pa_decode_noalloc_max_scratch.argtypes = []
     lib.pa_decode_noalloc_max_scratch.restype = SZ
     lib.pa_append_kv.argtypes = [P, P, P, P, P, I, I, I, I, I, I, P, P]
@@ -203,6 +205,34 @@ def pa_decode_noalloc(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor,
                                   _ptr(context_lens), N, H, num_kv_heads, d, bs, float(scale), int(window),
                                   DTYPE_CODE[q.dtype], DTYPE_CODE[out.dtype], block_tables.shape[1], nb,
                                   int(partition_size), _ptr(err_word), _stream(stream)))
+    return out
+
+
+def pa_decode_contiguous(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                         context_lens: torch.Tensor, num_kv_heads: int | None = None, scale: float | None = None,
+                         window: int = 0, partition_size: int = 0, workspace: torch.Tensor | None = None,
+                         err_word: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """pa_decode over contiguous caches [N, H_kv, L, d] (no block table; see
+    include/pa.h)."""
+    _cuda(out, q, k_cache, v_cache, context_lens, workspace, err_word)
+    N, H, d = q.shape
+    n2, hkv, L, d2 = k_cache.shape
+    if num_kv_heads is None:
+        num_kv_heads = hkv
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if context_lens.dtype != torch.int32:
+        raise TypeError("context_lens must be int32")
+    if q.dtype != k_cache.dtype or v_cache.dtype != k_cache.dtype:
+        raise TypeError("q, k_cache and v_cache must share one dtype")
+    if workspace is None:
+        n = pa_decode_workspace_size(N, H, d, 16, max(1, L // 16), window, partition_size)
+        workspace = None if n == 0 else torch.empty((n + 15) // 16 * 4, dtype=torch.float32, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(_lib.pa_decode_contiguous(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(context_lens), N, H,
+                                     num_kv_heads, d, L, float(scale), int(window), DTYPE_CODE[q.dtype],
+                                     DTYPE_CODE[out.dtype], int(partition_size), _ptr(workspace), ws_bytes,
+                                     _ptr(err_word), _stream(stream)))
     return out
 
 

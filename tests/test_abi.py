@@ -199,3 +199,28 @@ def test_noalloc_reports_bad_arguments_before_the_scratch_limit(lib):
     assert call(H=48, Hkv=16) == UNS               # a group of 3
     assert call(nb=0) == INV
     assert call(scale=float("nan")) == INV
+
+
+def test_contiguous_decode_host_validation(lib):
+    INV, UNS, WS = 1, 2, 3
+    P, I = ctypes.c_void_p, ctypes.c_int
+    f = lib.pa_decode_contiguous
+    f.restype = I
+    f.argtypes = [P, P, P, P, P, I, I, I, I, I, ctypes.c_float, I, I, I, I, P, ctypes.c_size_t, P, P]
+    ok = dict(out=0x1000, q=0x2000, k=0x3000, v=0x4000, cl=0x6000, N=4, H=8, Hkv=2, d=128, L=256, scale=0.088,
+              window=0, dtype=2, out_dtype=0, part=0, ws=None, wsb=0, err=None, stream=None)
+
+    def call(**o):
+        a = dict(ok, **o)
+        return f(a["out"], a["q"], a["k"], a["v"], a["cl"], a["N"], a["H"], a["Hkv"], a["d"], a["L"], a["scale"],
+                 a["window"], a["dtype"], a["out_dtype"], a["part"], a["ws"], a["wsb"], a["err"], a["stream"])
+
+    assert call(N=0) == 0
+    assert call(L=100) == INV                     # not a multiple of 16
+    assert call(L=0) == INV
+    assert call(cl=0) == INV
+    assert call(k=0x3008) == INV
+    assert call(H=12, Hkv=4) == UNS               # a group of 3
+    assert call(dtype=0) == UNS                   # fp32 with grouped heads
+    assert call(d=64) == UNS                      # head_dim 64 with grouped heads
+    assert call(L=16 * 1000) == WS                # several partitions need a workspace
