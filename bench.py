@@ -713,6 +713,36 @@ def traffic_from_profile(name: str, kernel_hash: str):
     return None, None
 
 
+def host_call_times(st, stream, calls=100):
+    """Host time of one decode call, in microseconds: through the Python
+    binding (st.decode) and, for pa_decode, through the C ABI alone (ctypes
+    with the arguments marshalled once).  The loops only submit work: they
+    do not wait for the GPU, which runs behind them."""
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(calls):
+        st.decode(stream)
+    t_py = (time.perf_counter() - t0) / calls
+    torch.cuda.synchronize()
+    out = {"python_binding": round(t_py * 1e6, 2)}
+    if type(st) is DecodeAppendStep and not st.kv_format and not getattr(st, "contiguous", False):
+        pa, s = st.pa, st.shape
+        lib = pa._lib
+        args = (pa._ptr(st.out), pa._ptr(st.q), pa._ptr(st.k_cache), pa._ptr(st.v_cache), pa._ptr(st.bt),
+                pa._ptr(st.cl), s.num_seqs, s.num_heads, s.num_kv_heads, s.head_dim, s.block_size,
+                1.0 / math.sqrt(s.head_dim), st.window, pa.DTYPE_CODE[s.dtype], pa.DTYPE_CODE[st.out.dtype],
+                st.bt.shape[1], st.k_cache.shape[0], st.partition, pa._ptr(st.ws),
+                0 if st.ws is None else st.ws.numel() * st.ws.element_size(), pa._ptr(st.err), pa._stream(stream))
+        f = lib.pa_decode
+        t0 = time.perf_counter()
+        for _ in range(calls):
+            f(*args)
+        t_c = (time.perf_counter() - t0) / calls
+        torch.cuda.synchronize()
+        out["c_abi"] = round(t_c * 1e6, 2)
+    return out
+
+
 def kernel_source_hash() -> str:
     import hashlib
     h = hashlib.sha256()
@@ -854,6 +884,7 @@ def run_native(args):
     ms_e2e = max_over_ranks(e0.elapsed_time(e1) / K, world, dev)
     e2e_diff = float((st.out_host.double() - out_device_path.cpu().double()).abs().max())
     assert e2e_diff <= 1e-4, f"the end-to-end output differs from the device-resident path's by {e2e_diff}"
+    host_us = host_call_times(st, stream)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -919,6 +950,7 @@ def run_native(args):
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms_e2e, 5),
                 "api": "paged_kv_cache_251_gb300.pa (ctypes binding of libpa)",
                 "max_abs_diff_vs_device_path": e2e_diff},
+        "host_us_per_decode_call": host_us,
         "gpu_launches": K * st.launches,
         "clocks": clk,
         "parity_sampled_max_abs": parity,
@@ -967,6 +999,67 @@ def run_swap(args):
     assert err.item() == 0
     t_out = statistics.mean(ev[3 * i].elapsed_time(ev[3 * i + 1]) for i in range(K))
     t_in = statistics.mean(ev[3 * i + 1].elapsed_time(ev[3 * i + 2]) for i in range(K))
+
+    # the copy engines instead of the kernel: one cudaMemcpyAsync (a torch
+    # copy) per contiguous run of blocks, K and V; the bench's pairs are a
+    # random permutation (runs of one block), and the same block count as one
+    # run of consecutive blocks
+    def ce_copy(src_k, src_v, dst_k, dst_v, runs):
+        for a, b, n in runs:
+            dst_k[b:b + n].copy_(src_k[a:a + n], non_blocking=True)
+            dst_v[b:b + n].copy_(src_v[a:a + n], non_blocking=True)
+
+    def as_runs(pairs):
+        runs, p = [], pairs.cpu().tolist()
+        for a, b in p:
+            if runs and runs[-1][0] + runs[-1][2] == a and runs[-1][1] + runs[-1][2] == b:
+                runs[-1][2] += 1
+            else:
+                runs.append([a, b, 1])
+        return runs
+
+    ce = {}
+    first = 0
+    for label, pairs_out in (("permuted", out_pairs), ("one_run", torch.stack([torch.arange(first, first + nblk),
+                                                                                torch.arange(nblk)], 1))):
+        r_out = as_runs(pairs_out)
+        r_in = [[b, a, n] for a, b, n in r_out]
+        for _ in range(2):
+            ce_copy(inp.k_cache, inp.v_cache, hk, hv, r_out)
+            ce_copy(hk, hv, inp.k_cache, inp.v_cache, r_in)
+        torch.cuda.synchronize(dev)
+        cev = [torch.cuda.Event(enable_timing=True) for _ in range(3 * K)]
+        t_host = time.perf_counter()
+        for i in range(K):
+            cev[3 * i].record(stream)
+            ce_copy(inp.k_cache, inp.v_cache, hk, hv, r_out)
+            cev[3 * i + 1].record(stream)
+            ce_copy(hk, hv, inp.k_cache, inp.v_cache, r_in)
+            cev[3 * i + 2].record(stream)
+        t_host = (time.perf_counter() - t_host) / (2 * K)
+        torch.cuda.synchronize(dev)
+        co = statistics.mean(cev[3 * i].elapsed_time(cev[3 * i + 1]) for i in range(K))
+        ci = statistics.mean(cev[3 * i + 1].elapsed_time(cev[3 * i + 2]) for i in range(K))
+        ce[label] = {"copies_per_direction": 2 * len(r_out), "out_gbs": round(bytes_dir / (co * 1e-3) / 1e9, 2),
+                     "in_gbs": round(bytes_dir / (ci * 1e-3) / 1e9, 2), "ms_out": round(co, 4), "ms_in": round(ci, 4),
+                     "host_ms_per_direction": round(t_host * 1e3, 3)}
+    # the kernel on one run of consecutive blocks, for the same comparison
+    kp_out = torch.stack([torch.arange(first, first + nblk), torch.arange(nblk)], 1).contiguous().to(dev)
+    kp_in = kp_out.flip(1).contiguous()
+    for _ in range(2):
+        pa.pa_swap_blocks(kp_out, inp.k_cache, inp.v_cache, hk, hv, err_word=err)
+        pa.pa_swap_blocks(kp_in, hk, hv, inp.k_cache, inp.v_cache, err_word=err)
+    kev = [torch.cuda.Event(enable_timing=True) for _ in range(3 * K)]
+    for i in range(K):
+        kev[3 * i].record(stream)
+        pa.pa_swap_blocks(kp_out, inp.k_cache, inp.v_cache, hk, hv, err_word=err)
+        kev[3 * i + 1].record(stream)
+        pa.pa_swap_blocks(kp_in, hk, hv, inp.k_cache, inp.v_cache, err_word=err)
+        kev[3 * i + 2].record(stream)
+    torch.cuda.synchronize(dev)
+    assert err.item() == 0
+    ko = statistics.mean(kev[3 * i].elapsed_time(kev[3 * i + 1]) for i in range(K))
+    ki = statistics.mean(kev[3 * i + 1].elapsed_time(kev[3 * i + 2]) for i in range(K))
     line = {"metric": "KV block swap GB/s (HBM <-> pinned host memory)", "value": round(
         2 * bytes_dir / ((t_out + t_in) * 1e-3) / 1e9, 2), "unit": "GB/s", "n_gpus": 1, "steps": K,
         "warmup": max(args.warmup, 3), "higher_is_better": True, "dtype": "f16", "data": "synthetic",
@@ -974,7 +1067,10 @@ def run_swap(args):
                                "host memory and back, pa_swap_blocks", "blocks": nblk},
         "swap_out_gbs": round(bytes_dir / (t_out * 1e-3) / 1e9, 2),
         "swap_in_gbs": round(bytes_dir / (t_in * 1e-3) / 1e9, 2),
-        "ms_out": round(t_out, 4), "ms_in": round(t_in, 4), "gpu_launches": 2 * K, "impl": "native"}
+        "ms_out": round(t_out, 4), "ms_in": round(t_in, 4),
+        "kernel_one_run": {"out_gbs": round(bytes_dir / (ko * 1e-3) / 1e9, 2),
+                           "in_gbs": round(bytes_dir / (ki * 1e-3) / 1e9, 2)},
+        "copy_engine": ce, "gpu_launches": 2 * K, "impl": "native"}
     if rank == 0:
         print(json.dumps(line), flush=True)
 

@@ -442,7 +442,7 @@ pa_status launch_decode_kernel(DecodeParams &p, int dtype, int head_dim, int G, 
     void *args_gqa[] = {&p, &tmk, &tmv, &tmq, &tmkw, &tmvw};
     void *args_mha[] = {&p, &tmk, &tmv};
     void *args[] = {&p};
-    e = cudaLaunchKernel(fn, dim3(static_cast<unsigned>(grid)), dim3(threads),
+    e = launch_dependent(fn, dim3(static_cast<unsigned>(grid)), dim3(threads),
                          gqa_tc ? args_gqa : (mha ? args_mha : args), smem, cs);
     if (e != cudaSuccess)
         return cuda_fail(e, "decode launch");
@@ -498,7 +498,7 @@ pa_status launch_decode_q8_kernel(DecodeParams &p, int cache_dtype, int head_dim
         if (items_max > grid)
             p.work = work_counter(dev, cs);
         void *args[] = {&p, &tmk, &tmv, &tsk, &tsv};
-        e = cudaLaunchKernel(tfn, dim3(static_cast<unsigned>(grid)), dim3(kQ8tThreads), args, smem, cs);
+        e = launch_dependent(tfn, dim3(static_cast<unsigned>(grid)), dim3(kQ8tThreads), args, smem, cs);
         if (e != cudaSuccess)
             return cuda_fail(e, "decode launch");
         return PA_OK;
@@ -538,7 +538,7 @@ pa_status launch_decode_q8_kernel(DecodeParams &p, int cache_dtype, int head_dim
         if (items_max > grid)
             p.work = work_counter(dev, cs);  // items claimed from a per-launch counter
         void *args[] = {&p};
-        e = cudaLaunchKernel(ffn, dim3(static_cast<unsigned>(grid)), dim3(kQ8fThreads), args, smem, cs);
+        e = launch_dependent(ffn, dim3(static_cast<unsigned>(grid)), dim3(kQ8fThreads), args, smem, cs);
         if (e != cudaSuccess)
             return cuda_fail(e, "decode launch");
         return PA_OK;
@@ -567,7 +567,7 @@ pa_status launch_decode_q8_kernel(DecodeParams &p, int cache_dtype, int head_dim
     if (grid < 1)
         grid = 1;
     void *args[] = {&p};
-    e = cudaLaunchKernel(fn, dim3(static_cast<unsigned>(grid)), dim3(kDecodeThreads), args, smem, cs);
+    e = launch_dependent(fn, dim3(static_cast<unsigned>(grid)), dim3(kDecodeThreads), args, smem, cs);
     if (e != cudaSuccess)
         return cuda_fail(e, "decode launch");
     return PA_OK;

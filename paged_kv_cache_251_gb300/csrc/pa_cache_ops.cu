@@ -36,6 +36,8 @@ __global__ void __launch_bounds__(256) append_kernel(const uint4 *__restrict__ k
                                                      uint4 *v_cache, long long num_tokens, int num_kv_heads,
                                                      int chunks_per_row, int block_size, long long pool_slots,
                                                      uint32_t *err) {
+    pdl_launch_dependents();
+    pdl_wait();
     const long long per_token = static_cast<long long>(num_kv_heads) * chunks_per_row;
     const long long total = num_tokens * per_token;
     for (long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; idx < total;
@@ -75,6 +77,8 @@ __global__ void __launch_bounds__(256) append_quant_kernel(const char *__restric
                                                            int in_dtype, int block_size, long long pool_slots,
                                                            uint32_t *err) {
     constexpr int E = D / 32;
+    pdl_launch_dependents();
+    pdl_wait();
     const int lane = threadIdx.x & 31;
     const long long rows = num_tokens * num_kv_heads;
     const long long warps = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
@@ -132,6 +136,8 @@ __global__ void __launch_bounds__(256) copy_blocks_kernel(const int64_t *__restr
                                                           uint4 *k_cache, uint4 *v_cache,
                                                           long long chunks_per_block, long long num_blocks,
                                                           uint32_t *err) {
+    pdl_launch_dependents();
+    pdl_wait();
     uint4 *cache = blockIdx.z == 0 ? k_cache : v_cache;
     for (int pi = blockIdx.y; pi < num_pairs; pi += gridDim.y) {
         const long long src = pairs[2 * pi], dst = pairs[2 * pi + 1];
@@ -168,6 +174,8 @@ __global__ void __launch_bounds__(256) swap_blocks_kernel(const int64_t *__restr
                                                           const uint4 *src_k, const uint4 *src_v, uint4 *dst_k,
                                                           uint4 *dst_v, long long chunks_per_block,
                                                           long long src_blocks, long long dst_blocks, uint32_t *err) {
+    pdl_launch_dependents();
+    pdl_wait();
     const uint4 *src_pool = blockIdx.z == 0 ? src_k : src_v;
     uint4 *dst_pool = blockIdx.z == 0 ? dst_k : dst_v;
     for (int pi = blockIdx.y; pi < num_pairs; pi += gridDim.y) {
@@ -217,10 +225,12 @@ cudaError_t launch_swap_blocks(const int64_t *pairs, int num_pairs, const void *
     if (gy > 65535)
         gy = 65535;
     dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(gy), 2);
-    swap_blocks_kernel<<<grid, 256, 0, stream>>>(pairs, num_pairs, static_cast<const uint4 *>(src_k),
-                                                 static_cast<const uint4 *>(src_v), static_cast<uint4 *>(dst_k),
-                                                 static_cast<uint4 *>(dst_v), chunks, src_blocks, dst_blocks, err);
-    return cudaGetLastError();
+    const uint4 *sk = static_cast<const uint4 *>(src_k), *sv = static_cast<const uint4 *>(src_v);
+    uint4 *dk = static_cast<uint4 *>(dst_k), *dv = static_cast<uint4 *>(dst_v);
+    long long ck = chunks, sb = src_blocks, db = dst_blocks;
+    int np = num_pairs;
+    void *args[] = {&pairs, &np, &sk, &sv, &dk, &dv, &ck, &sb, &db, &err};
+    return launch_dependent(reinterpret_cast<const void *>(&swap_blocks_kernel), grid, dim3(256), args, 0, stream);
 }
 
 cudaError_t launch_append(const void *k, const void *v, const int64_t *slots, void *k_cache, void *v_cache,
@@ -234,11 +244,13 @@ cudaError_t launch_append(const void *k, const void *v, const int64_t *slots, vo
         blocks = cap;
     if (blocks < 1)
         blocks = 1;
-    append_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-        static_cast<const uint4 *>(k), static_cast<const uint4 *>(v), slots, static_cast<uint4 *>(k_cache),
-        static_cast<uint4 *>(v_cache), num_tokens, num_kv_heads, cpr, block_size,
-        static_cast<long long>(num_blocks) * block_size, err);
-    return cudaGetLastError();
+    const uint4 *ka = static_cast<const uint4 *>(k), *va = static_cast<const uint4 *>(v);
+    uint4 *kc = static_cast<uint4 *>(k_cache), *vc = static_cast<uint4 *>(v_cache);
+    long long nt = num_tokens, pool_slots = static_cast<long long>(num_blocks) * block_size;
+    int hkv = num_kv_heads, c = cpr, bs = block_size;
+    void *args[] = {&ka, &va, &slots, &kc, &vc, &nt, &hkv, &c, &bs, &pool_slots, &err};
+    return launch_dependent(reinterpret_cast<const void *>(&append_kernel), dim3(static_cast<unsigned>(blocks)),
+                            dim3(256), args, 0, stream);
 }
 
 cudaError_t launch_append_quant(const void *k, const void *v, const int64_t *slots, void *k_pages, void *v_pages,
@@ -251,17 +263,17 @@ cudaError_t launch_append_quant(const void *k, const void *v, const int64_t *slo
         blocks = cap;
     if (blocks < 1)
         blocks = 1;
-    const long long pool_slots = static_cast<long long>(num_blocks) * block_size;
-#define PA_APPEND_Q(F, D)                                                                                      \
-    append_quant_kernel<F, D><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(                              \
-        static_cast<const char *>(k), static_cast<const char *>(v), slots, static_cast<uint8_t *>(k_pages),    \
-        static_cast<uint8_t *>(v_pages), num_tokens, num_kv_heads, in_dtype, block_size, pool_slots, err)
-    if (cache_dtype == PA_I8)
-        head_dim == 128 ? PA_APPEND_Q(kFmtI8, 128) : PA_APPEND_Q(kFmtI8, 64);
-    else
-        head_dim == 128 ? PA_APPEND_Q(kFmtE4M3, 128) : PA_APPEND_Q(kFmtE4M3, 64);
-#undef PA_APPEND_Q
-    return cudaGetLastError();
+    long long pool_slots = static_cast<long long>(num_blocks) * block_size, nt = num_tokens;
+    const char *ka = static_cast<const char *>(k), *va = static_cast<const char *>(v);
+    uint8_t *kp = static_cast<uint8_t *>(k_pages), *vp = static_cast<uint8_t *>(v_pages);
+    int hkv = num_kv_heads, dt = in_dtype, bs = block_size;
+    void *args[] = {&ka, &va, &slots, &kp, &vp, &nt, &hkv, &dt, &bs, &pool_slots, &err};
+    const void *fn = cache_dtype == PA_I8
+                         ? (head_dim == 128 ? reinterpret_cast<const void *>(&append_quant_kernel<kFmtI8, 128>)
+                                            : reinterpret_cast<const void *>(&append_quant_kernel<kFmtI8, 64>))
+                         : (head_dim == 128 ? reinterpret_cast<const void *>(&append_quant_kernel<kFmtE4M3, 128>)
+                                            : reinterpret_cast<const void *>(&append_quant_kernel<kFmtE4M3, 64>));
+    return launch_dependent(fn, dim3(static_cast<unsigned>(blocks)), dim3(256), args, 0, stream);
 }
 
 cudaError_t launch_copy_blocks(const int64_t *pairs, int num_pairs, void *k_cache, void *v_cache,
@@ -281,9 +293,11 @@ cudaError_t launch_copy_blocks(const int64_t *pairs, int num_pairs, void *k_cach
     if (gy > 65535)
         gy = 65535;
     dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(gy), 2);
-    copy_blocks_kernel<<<grid, 256, 0, stream>>>(pairs, num_pairs, static_cast<uint4 *>(k_cache),
-                                                 static_cast<uint4 *>(v_cache), chunks, num_blocks, err);
-    return cudaGetLastError();
+    uint4 *kc = static_cast<uint4 *>(k_cache), *vc = static_cast<uint4 *>(v_cache);
+    long long ck = chunks, nb = num_blocks;
+    int np = num_pairs;
+    void *args[] = {&pairs, &np, &kc, &vc, &ck, &nb, &err};
+    return launch_dependent(reinterpret_cast<const void *>(&copy_blocks_kernel), grid, dim3(256), args, 0, stream);
 }
 
 }  // namespace pa

@@ -660,7 +660,10 @@ __device__ inline void decode_consumer(const DecodeParams &p, char *smem, const 
 
 template <typename T, int D, int G>
 __global__ void __launch_bounds__(kDecodeThreads) pa_decode_kernel(const DecodeParams p) {
-    pdl_launch_dependents();  // the partition merge may be launched now (it waits for this grid)
+    // the next kernel on the stream may be launched now (it waits for this
+    // grid); this one waits for the kernel before it
+    pdl_launch_dependents();
+    pdl_wait();
     extern __shared__ __align__(128) char smem[];
     using C = DecodeCfg<T, D, G>;
     const SmemLayout L = decode_smem_layout(p.stages, p.block_size * C::kRow, C::kRow, G, D);
@@ -705,6 +708,7 @@ constexpr int kReduceRows = kReduceThreads / 32;
 template <int D>
 __global__ void __launch_bounds__(kReduceThreads) pa_reduce_kernel(const DecodeParams p) {
     // (the host takes this layout only for max_parts <= 32: lane q holds partition q)
+    pdl_launch_dependents();
     pdl_wait();
     constexpr int kPer = D / 32;  // head_dim slice per lane (4 or 2)
     constexpr int kBatch = 8;     // partitions whose slices are loaded before any is used
@@ -774,6 +778,7 @@ __global__ void __launch_bounds__(kReduceThreads) pa_reduce_kernel(const DecodeP
 
 template <int D>
 __global__ void __launch_bounds__(kReduceWideThreads) pa_reduce_wide_kernel(const DecodeParams p) {
+    pdl_launch_dependents();
     pdl_wait();
     constexpr int kWarps = kReduceWideThreads / 32;
     constexpr int kPer = D / 32;  // head_dim slice per lane (4 or 2)

@@ -547,7 +547,10 @@ template <typename T, int D, int BS>
 __global__ void __launch_bounds__(kMhaThreads) pa_decode_mha_kernel(const DecodeParams p,
                                                                    const __grid_constant__ CUtensorMap tmk,
                                                                    const __grid_constant__ CUtensorMap tmv) {
-    pdl_launch_dependents();  // the partition merge may be launched now (it waits for this grid)
+    // the next kernel on the stream may be launched now (it waits for this
+    // grid); this one waits for the kernel before it
+    pdl_launch_dependents();
+    pdl_wait();
     extern __shared__ __align__(1024) char smem_raw[];
     char *smem = reinterpret_cast<char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     using C = MhaCfg<T, D, BS>;

@@ -37,6 +37,8 @@ __global__ void __launch_bounds__(256)
                        int32_t *shared_eff, int32_t *start_tok, const uint4 *__restrict__ q, uint4 *qv,
                        int num_groups, int group_size, int num_heads, int num_kv_heads, int chunks_per_row,
                        int block_size, int max_len, uint32_t *err) {
+    pdl_launch_dependents();
+    pdl_wait();
     const long long tid = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
     const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
     for (long long g = tid; g < num_groups; g += stride) {
@@ -83,6 +85,7 @@ __global__ void __launch_bounds__(kReduceThreads)
                           int group_size) {
     constexpr int kPer = D / 32;  // head_dim slice per lane (4 or 2)
     constexpr int kBatch = 8;
+    pdl_launch_dependents();
     pdl_wait();
     const int lane = threadIdx.x & 31;
     const long long rowi = static_cast<long long>(blockIdx.x) * kReduceRows + (threadIdx.x >> 5);  // s * H + h
@@ -271,10 +274,14 @@ extern "C" pa_status pa_decode_shared_prefix(void *out, const void *q, const voi
         blocks = 4096;
     if (blocks < 1)
         blocks = 1;
-    prefix_prep_kernel<<<static_cast<unsigned>(blocks), 256, 0, cs>>>(
-        context_lens, shared_lens, shared_eff, start_tok, static_cast<const uint4 *>(q), static_cast<uint4 *>(qv),
-        num_groups, group_size, num_heads, num_kv_heads, cpr, block_size, max_len, err_word);
-    cudaError_t e = cudaGetLastError();
+    const uint4 *qs = static_cast<const uint4 *>(q);
+    uint4 *qvs = static_cast<uint4 *>(qv);
+    int ng = num_groups, gsz = group_size, nh = num_heads, nkv = num_kv_heads, cprr = cpr, bsz = block_size,
+        ml = max_len;
+    void *pargs[] = {&context_lens, &shared_lens, &shared_eff, &start_tok, &qs, &qvs, &ng, &gsz, &nh, &nkv,
+                     &cprr, &bsz, &ml, &err_word};
+    cudaError_t e = launch_dependent(reinterpret_cast<const void *>(&prefix_prep_kernel),
+                                     dim3(static_cast<unsigned>(blocks)), dim3(256), pargs, 0, cs);
     if (e != cudaSuccess)
         return bad(PA_ERR_CUDA, "shared-prefix prep launch failed");
 

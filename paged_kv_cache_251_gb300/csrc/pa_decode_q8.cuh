@@ -408,7 +408,10 @@ __device__ inline void q8_consumer(const DecodeParams &p, char *smem, const Smem
 
 template <int Fmt, int D, int G>
 __global__ void __launch_bounds__(kDecodeThreads) pa_decode_q8_kernel(const DecodeParams p) {
-    pdl_launch_dependents();  // the partition merge may be launched now (it waits for this grid)
+    // the next kernel on the stream may be launched now (it waits for this
+    // grid); this one waits for the kernel before it
+    pdl_launch_dependents();
+    pdl_wait();
     extern __shared__ __align__(128) char smem[];
     const SmemLayout L = q8_smem_layout(p.stages, p.block_size, G, D);
     if (threadIdx.x == 0) {

@@ -712,7 +712,10 @@ template <int G> struct Q8fOccupancy {
 
 template <int Fmt, int G, int BS>
 __global__ void __launch_bounds__(kQ8fThreads, Q8fOccupancy<G>::kMinBlocks) pa_decode_q8f_kernel(const DecodeParams p) {
-    pdl_launch_dependents();  // the partition merge may be launched now (it waits for this grid)
+    // the next kernel on the stream may be launched now (it waits for this
+    // grid); this one waits for the kernel before it
+    pdl_launch_dependents();
+    pdl_wait();
     extern __shared__ __align__(128) char smem_raw[];
     char *smem = reinterpret_cast<char *>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
     const int qrow = kQ8fD * (p.q_dtype == PA_F32 ? 4 : 2);
