@@ -713,6 +713,18 @@ def traffic_from_profile(name: str, kernel_hash: str):
     return None, None
 
 
+def default_partition(s, kv_format):
+    """The partition the library takes for partition_size 0 (include/pa.h):
+    1024 tokens where a tensor-core kernel runs, else 512."""
+    G = s.num_heads // s.num_kv_heads
+    if kv_format == "native":
+        tc = G in (2, 4, 8) and s.head_dim == 128 and s.dtype in (torch.float16, torch.bfloat16)
+    else:
+        tc = (kv_format == "e4m3" and s.head_dim == 128 and G in (2, 4) and s.block_size in (16, 32)
+              and s.num_kv_heads % 4 == 0 and s.dtype in (torch.float16, torch.bfloat16))
+    return 1024 if tc else 512
+
+
 def host_call_times(st, stream, calls=100):
     """Host time of one decode call, in microseconds: through the Python
     binding (st.decode) and, for pa_decode, through the C ABI alone (ctypes
@@ -928,7 +940,8 @@ def run_native(args):
             "num_seqs": s.num_seqs, "num_heads": s.num_heads, "num_kv_heads": s.num_kv_heads,
             "head_dim": s.head_dim, "block_size": s.block_size, "window": st.window,
             "context_tokens": st.dec_bytes["attended_tokens"],
-            "partition_size": st.partition or 512, "accumulate": "f32", "out_dtype": "f32",
+            "partition_size": st.partition or default_partition(s, args.kv_format), "accumulate": "f32",
+            "out_dtype": "f32",
             "block_order": args.table, "kv_format": args.kv_format,
             "l2": (f"no flush: the K/V read per step ({st.kv_bytes / 1e9:.2f} GB) is larger than L2 (129 MB)"
                    if flush is None else
