@@ -120,12 +120,63 @@ cudaError_t tensor_map_encoder(PFN_cuTensorMapEncodeTiled_v12000 *fn) {
     return g_encode_err;
 }
 
+// Encoded tensor maps, cached per thread: a map is a function of its base
+// address, element type and shape alone, so a repeated call (the same cache,
+// queries and shapes, as in a decode loop) reuses the encoding instead of
+// calling cuTensorMapEncodeTiled again.  16 entries, least recently used out.
+struct TmKey {
+    int kind;
+    const void *base;
+    long long a, b, c, d, e;
+    bool operator==(const TmKey &o) const {
+        return kind == o.kind && base == o.base && a == o.a && b == o.b && c == o.c && d == o.d && e == o.e;
+    }
+};
+struct TmCache {
+    static constexpr int kEntries = 16;
+    TmKey key[kEntries];
+    CUtensorMap map[kEntries];
+    unsigned use[kEntries];
+    unsigned clock = 0;
+    int n = 0;
+};
+thread_local TmCache t_tm;
+
+bool tm_lookup(const TmKey &k, CUtensorMap *out) {
+    for (int i = 0; i < t_tm.n; ++i) {
+        if (t_tm.key[i] == k) {
+            *out = t_tm.map[i];
+            t_tm.use[i] = ++t_tm.clock;
+            return true;
+        }
+    }
+    return false;
+}
+
+void tm_store(const TmKey &k, const CUtensorMap &m) {
+    int slot = t_tm.n;
+    if (slot == TmCache::kEntries) {
+        slot = 0;
+        for (int i = 1; i < TmCache::kEntries; ++i)
+            if (t_tm.use[i] < t_tm.use[slot])
+                slot = i;
+    } else {
+        ++t_tm.n;
+    }
+    t_tm.key[slot] = k;
+    t_tm.map[slot] = m;
+    t_tm.use[slot] = ++t_tm.clock;
+}
+
 // 4-D view of a K or V cache [num_blocks * H_kv][block_size][head_dim] as
 // [tile][128-byte segment of the row][row][elements of the segment]; one box is
 // a whole (block, head) tile and lands in shared memory as one 128-byte-wide,
 // block_size-row box per segment (128-byte swizzle).
 pa_status kv_tensor_map(CUtensorMap *map, const void *base, int dtype, int head_dim, int block_size,
                         long long tiles) {
+    const TmKey key{1, base, dtype, head_dim, block_size, tiles, 0};
+    if (tm_lookup(key, map))
+        return PA_OK;
     PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
     cudaError_t e = tensor_map_encoder(&enc);
     if (e != cudaSuccess || !enc)
@@ -146,6 +197,7 @@ pa_status kv_tensor_map(CUtensorMap *map, const void *base, int dtype, int head_
     if (r != CUDA_SUCCESS)
         return fail(PA_ERR_INVALID_ARGUMENT, "cuTensorMapEncodeTiled rejected the cache layout (code " +
                                                  std::to_string(static_cast<int>(r)) + ")");
+    tm_store(key, *map);
     return PA_OK;
 }
 
@@ -156,6 +208,9 @@ pa_status kv_tensor_map(CUtensorMap *map, const void *base, int dtype, int head_
 // in shared memory as 8-row groups of both 128-byte halves (128-byte swizzle).
 pa_status kv_tensor_map_groups(CUtensorMap *map, const void *base, int dtype, int block_size, long long tiles,
                                int box_tiles = 1) {
+    const TmKey key{2, base, dtype, block_size, tiles, box_tiles, 0};
+    if (tm_lookup(key, map))
+        return PA_OK;
     PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
     cudaError_t e = tensor_map_encoder(&enc);
     if (e != cudaSuccess || !enc)
@@ -171,12 +226,16 @@ pa_status kv_tensor_map_groups(CUtensorMap *map, const void *base, int dtype, in
     if (r != CUDA_SUCCESS)
         return fail(PA_ERR_INVALID_ARGUMENT, "cuTensorMapEncodeTiled rejected the grouped cache view (code " +
                                                  std::to_string(static_cast<int>(r)) + ")");
+    tm_store(key, *map);
     return PA_OK;
 }
 
 // 2-D view of q [num_seqs * num_heads][head_dim] with a box of one 128-byte
 // row segment x `group` rows (the query heads of one kv head), 128-byte swizzle.
 pa_status q_tensor_map(CUtensorMap *map, const void *base, int dtype, int head_dim, long long rows, int group) {
+    const TmKey key{3, base, dtype, head_dim, rows, group, 0};
+    if (tm_lookup(key, map))
+        return PA_OK;
     PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
     cudaError_t e = tensor_map_encoder(&enc);
     if (e != cudaSuccess || !enc)
@@ -192,6 +251,7 @@ pa_status q_tensor_map(CUtensorMap *map, const void *base, int dtype, int head_d
     if (r != CUDA_SUCCESS)
         return fail(PA_ERR_INVALID_ARGUMENT,
                     "cuTensorMapEncodeTiled rejected the query layout (code " + std::to_string(static_cast<int>(r)) + ")");
+    tm_store(key, *map);
     return PA_OK;
 }
 
@@ -200,6 +260,9 @@ pa_status q_tensor_map(CUtensorMap *map, const void *base, int dtype, int head_d
 // code rows of 4 adjacent pages (128-byte swizzle); scales: a box is the
 // 4 * block_size scale bytes of the same 4 pages (no swizzle).
 pa_status q8_page_tensor_map(CUtensorMap *map, const void *base, int block_size, long long pages, bool scales) {
+    const TmKey key{4, base, block_size, pages, scales ? 1 : 0, 0, 0};
+    if (tm_lookup(key, map))
+        return PA_OK;
     PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
     cudaError_t e = tensor_map_encoder(&enc);
     if (e != cudaSuccess || !enc)
@@ -216,6 +279,7 @@ pa_status q8_page_tensor_map(CUtensorMap *map, const void *base, int block_size,
     if (r != CUDA_SUCCESS)
         return fail(PA_ERR_INVALID_ARGUMENT, "cuTensorMapEncodeTiled rejected the 8-bit page layout (code " +
                                                  std::to_string(static_cast<int>(r)) + ")");
+    tm_store(key, *map);
     return PA_OK;
 }
 
@@ -228,6 +292,10 @@ constexpr int kGqaDefaultPartition = 1024;
 // The block size contiguous caches are cut into (their tiles: TMA boxes).
 constexpr int kContiguousBlock = 16;
 constexpr int kQ8fStageBudget = 48 * 1024;
+// Grouped heads: 3 stages of 4 kv heads' pages at block 16 (17.4 KB each; 3 CTAs
+// per SM still fit).  Measured on the GQA INT8 batch: 2 stages 0.200 ms, 3
+// stages 0.197 ms, 4 stages 0.226 ms (2 CTAs per SM).
+constexpr int kQ8fGroupStageBudget = 56 * 1024;
 constexpr int kMhaStageBudget = 64 * 1024;
 constexpr int kGqaStages = 3;
 constexpr int kStageBudget = 48 * 1024;
@@ -515,7 +583,7 @@ pa_status launch_decode_q8_kernel(DecodeParams &p, int cache_dtype, int head_dim
         // a stage holds the K and V pages of 4 kv heads; every consumer warp
         // reads every stage
         const int stage = 2 * kQ8fWarps * q8_page_bytes(p.block_size, kQ8fD);
-        int S = kQ8fStageBudget / stage;
+        int S = (G > 1 ? kQ8fGroupStageBudget : kQ8fStageBudget) / stage;
         S = S < 2 ? 2 : (S > 8 ? 8 : S);
         p.stages = S;
         const size_t smem = q8f_smem_layout(S, p.block_size, G, kQ8fD * (p.q_dtype == PA_F32 ? 4 : 2)).total;
