@@ -807,9 +807,12 @@ __device__ inline bool gqa_softmax(const DecodeParams &p, char *smem, const GqaL
                 for (int bx = 0; bx < 2; ++bx) {
                     uint4 *dst = reinterpret_cast<uint4 *>(vt + (row >> 3) * C::kGroupBytes + bx * C::kHalfBytes +
                                                            (row & 7) * 128);
+                    // chunk order rotated by the row: the lanes of a store cover
+                    // eight chunk positions, i.e. all 32 banks (rows 128 bytes
+                    // apart would otherwise all hit the same four)
 #pragma unroll
                     for (int c = 0; c < 8; ++c)
-                        dst[c] = make_uint4(0, 0, 0, 0);
+                        dst[(c + row) & 7] = make_uint4(0, 0, 0, 0);
                 }
             }
             fence_async_smem();
