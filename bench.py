@@ -70,6 +70,8 @@ def parse_args(argv=None):
                          "pa_decode_quant and appended by pa_append_kv_quant")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU baseline budget")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-others", action="store_true",
+                    help="default run: skip the timing of the other workloads (other_workloads in the JSON line)")
     return ap.parse_args(argv)
 
 
@@ -770,6 +772,79 @@ def kernel_source_hash() -> str:
 # arms
 
 
+# The other workloads, timed after the headline one in a default run (one
+# GPU), so that one record carries every workload: (label, workload,
+# kv_format, shared-prefix decode)
+OTHER_WORKLOADS = [
+    ("tiny", "tiny", "native", False),
+    ("tiny_scaled", "tiny_scaled", "native", False),
+    ("gqa", "gqa", "native", False),
+    ("window", "window", "native", False),
+    ("prefix_bs16_shared", "prefix_bs16", "native", True),
+    ("opt13b_int8", "opt13b", "int8", False),
+    ("opt13b_e4m3", "opt13b", "e4m3", False),
+    ("gqa_int8", "gqa", "int8", False),
+    ("gqa_e4m3", "gqa", "e4m3", False),
+]
+
+
+def time_workload(st, dev, steps, warmup, soak_s=0.3):
+    """Decode-call and step times of a workload's step (CUDA events on the
+    launching stream; L2 flushed before each step when its K/V would fit)."""
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(max(warmup, 3)):
+        st.run(stream)
+    torch.cuda.synchronize(dev)
+    flush = (torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+             if int(st.kv_bytes) < 2 * L2_BYTES else None)
+    ds = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    de = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    es = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ee = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    with ClockSampler(dev.index) as clocks:
+        t_soak = time.perf_counter()
+        while time.perf_counter() - t_soak < soak_s:
+            for _ in range(20):
+                st.run(stream)
+            torch.cuda.synchronize(dev)
+        for i in range(steps):
+            if flush is not None:
+                flush.add_(1)
+            es[i].record(stream)
+            st.run(stream, {"decode": (ds[i], de[i])})
+            ee[i].record(stream)
+        torch.cuda.synchronize(dev)
+    assert st.err.item() == 0, f"device error word {st.err.item()}"
+    ms_dec = statistics.mean(ds[i].elapsed_time(de[i]) for i in range(steps))
+    ms_step = statistics.mean(es[i].elapsed_time(ee[i]) for i in range(steps))
+    return ms_dec, ms_step, clocks.summary(), flush is not None
+
+
+def measure_others(dev, steps, warmup):
+    peak, peak_kind = hbm_peak()
+    out = {}
+    for label, name, kv_format, shared in OTHER_WORKLOADS:
+        st = make_step(name, dev, 0, "shuffled", shared, kv_format)
+        ms_dec, ms_step, clk, flushed = time_workload(st, dev, steps, warmup)
+        s = st.shape
+        achieved = st.roof_bytes / (ms_dec * 1e-3) / 1e9
+        out[label] = {
+            "workload": st.description,
+            "decode_ms": round(ms_dec, 5), "ms_per_step": round(ms_step, 5),
+            "kv_gb_s": round(st.kv_bytes / (ms_step * 1e-3) / 1e9, 2),
+            "roofline_frac": round(achieved / peak, 4), "algorithmic_bytes_per_decode": int(st.roof_bytes),
+            "seq_layer_steps_per_s": round(s.num_seqs / (ms_step * 1e-3), 1),
+            "partition_size": default_partition(s, kv_format) if name != "window" else 512,
+            "l2_flushed_per_step": flushed, "clocks": clk,
+        }
+        if hasattr(st, "unique_kv"):
+            out[label]["bytes_note"] = "unique K/V bytes (each shared prompt block counted once)"
+        del st
+        torch.cuda.synchronize(dev)
+        torch.cuda.empty_cache()
+    return out
+
+
 def run_native(args):
     world, rank, local = dist_env()
     dist_init(world)
@@ -916,6 +991,11 @@ def run_native(args):
                          f"cache ops), median of {len(times)} runs on {threads} host threads",
                "seconds_per_step": t_step}
 
+    others = None
+    if (rank == 0 and world == 1 and not args.no_others and args.workload == "opt13b" and args.table == "shuffled"
+            and args.kv_format == "native" and args.partition == 0):
+        others = measure_others(dev, K, args.warmup)
+
     peak, peak_kind = hbm_peak()
     achieved = st.roof_bytes / (ms_dec * 1e-3) / 1e9
     khash = kernel_source_hash()
@@ -969,6 +1049,8 @@ def run_native(args):
         "parity_sampled_max_abs": parity,
         "impl": "native",
     }
+    if others is not None:
+        line["other_workloads"] = others
     if hasattr(st, "unique_kv"):
         line["config"]["unique_kv_bytes"] = st.unique_kv
         line["roofline"]["bytes_note"] = "unique K/V bytes (each shared prompt block counted once)"
