@@ -79,3 +79,33 @@ def test_contiguous_context_beyond_the_cache_is_clamped_and_flagged():
     got, err = _contiguous(inp, kc, vc, 0, 0, context_lens=torch.tensor([L + 50, 40], dtype=torch.int32))
     assert err & 16
     compare(got, oracle_decode(inp, context_lens=torch.tensor([L, 40], dtype=torch.int32)), BF16)
+
+
+def _random_case(i):
+    import random
+    rng = random.Random(5100 + i)
+    g = rng.choice([1, 2, 4, 8])
+    hkv = rng.choice([1, 2, 4])
+    d = 128 if g > 1 else rng.choice([64, 128])
+    dt = rng.choice([F16, BF16]) if g > 1 else rng.choice([F16, BF16, F32])
+    n = rng.randint(1, 6)
+    max_len = rng.choice([40, 300, 1500, 4000])
+    lens = [rng.choice([0, 1, 15, 16, 17, 127, 128, 129, rng.randint(1, max_len)]) for _ in range(n)]
+    window = rng.choice([0, 0, rng.randint(1, max_len)])
+    part = rng.choice([0, 0, 16 * rng.randint(1, 16), 16 * rng.randint(32, 128)])
+    return f"rand{i}", n, hkv * g, hkv, d, dt, lens, window, part
+
+
+@pytest.mark.parametrize("i", range(30))
+def test_contiguous_random_configs_equal_paged_decode(i):
+    """Seeded random shapes, lengths, windows and partitions: the contiguous
+    decode equals pa_decode over the same values in a paged pool, bit for
+    bit, and matches the oracle."""
+    name, n, h, hkv, d, dt, lens, window, part = _random_case(i)
+    inp, kc, vc = _inputs(name, n, h, hkv, d, dt, lens, window)
+    got, err = _contiguous(inp, kc, vc, part, window)
+    assert err == 0
+    paged, perr = run_decode(inp, partition_size=part)
+    assert perr == 0
+    assert torch.equal(got, paged)
+    compare(got, oracle_decode(inp), dt)
