@@ -391,6 +391,13 @@ __device__ inline bool q8t_qconvert(const DecodeParams &p, char *smem, const Q8t
         // counter (each CTA takes the next unclaimed one when it has room;
         // the counter numbers them from gridDim.x up), else round-robin
         if (p.work && k > 0) {
+            // item k is claimed once the producer took item k - 1 (its record
+            // completes that slot's phase; this warp arrived for it already):
+            // a CTA holds at most one claimed item it has not started, so the
+            // launch's last items go to the CTAs that run out of work first
+            const int ps = static_cast<int>((k - 1) % kQ8tItemSlots);
+            if (!mbar_wait_bounded(&ifull[ps], static_cast<uint32_t>(((k - 1) / kQ8tItemSlots) & 1)))
+                return false;
             unsigned int v = 0;
             if (lane == 0)
                 v = gridDim.x + atomicAdd(p.work, 1u);

@@ -17,6 +17,11 @@ The epilogue of an item's last tile merges the four quarters from the item's
 final softmax state, which the softmax warps leave in slot g & 3; the model
 checks that the slot still holds that tile's state when the merge has read it.
 
+The query converter claims item k only once the producer has taken item
+k - 1, so a CTA holds at most one claimed item it has not started (claimed up
+to four ahead, the launch's last items sat queued behind other items in a few
+CTAs while the rest had none).
+
 Three variants that were tried on the way are kept as negative checks: an
 epilogue that waits on the 2-deep P barrier (the softmax warps may complete it
 twice before the epilogue looks), a single MMA thread that defers each tile's
@@ -56,7 +61,9 @@ class Deadlock(AssertionError):
 
 def simulate(items, S, design="final", seed=0):
     """items: tiles per item (0 = an empty item).  design: "final" (the
-    kernel), "pfull_epilogue", "single_issuer_no_flush" or "ofree_before_merge"."""
+    kernel), "claim_ahead", "pfull_epilogue", "single_issuer_no_flush" or
+    "ofree_before_merge".  Returns the most items the converter had claimed
+    beyond the one the producer was on."""
     rng = random.Random(seed)
     SL = 4
     two_issuers = design != "single_issuer_no_flush"
@@ -75,6 +82,8 @@ def simulate(items, S, design="final", seed=0):
     pv_done, epi_done, stage_done = set(), set(), set()
     stage_tile = [None] * S
     first = []
+    producer_at, claimed = [-1], [-1]  # items the producer started and the converter claimed
+    lead = [0]  # most items claimed beyond the producer's
     t = 0
     for nt in items:
         first.append(t)
@@ -92,6 +101,7 @@ def simulate(items, S, design="final", seed=0):
             if k >= SL:
                 yield from wait(iempty[slot], k // SL - 1, "producer iempty")
             ifull[slot].arrive()
+            producer_at[0] = k
             if nt is None:
                 return
             for _ in range(nt):
@@ -109,6 +119,12 @@ def simulate(items, S, design="final", seed=0):
             slot = k % SL
             if k >= SL:
                 yield from wait(iempty[slot], k // SL - 1, "converter iempty")
+            if k > 0 and design != "claim_ahead":
+                # item k is claimed once the producer took item k - 1
+                yield from wait(ifull[(k - 1) % SL], (k - 1) // SL, "converter ifull")
+                assert producer_at[0] >= k - 1
+            claimed[0] = k
+            lead[0] = max(lead[0], claimed[0] - producer_at[0])
             yield "convert"
             ifull[slot].arrive()
             if nt is None:
@@ -274,6 +290,7 @@ def simulate(items, S, design="final", seed=0):
             idle += 1
             if idle > 200:
                 raise Deadlock(f"deadlock; actors alive {alive}")
+    return lead[0]
 
 
 def _cases(n, seed):
@@ -285,7 +302,13 @@ def _cases(n, seed):
 
 def test_final_protocol_never_deadlocks_aliases_or_overwrites():
     for items, S, trial in _cases(400, 7):
-        simulate(items, S, "final", seed=trial)
+        assert simulate(items, S, "final", seed=trial) <= 1
+
+
+def test_converter_claims_at_most_one_item_ahead_of_the_producer():
+    leads = [simulate(items, S, "claim_ahead", seed=trial) for items, S, trial in _cases(200, 7)]
+    assert max(leads) > 1  # without the wait it runs further ahead
+    assert max(simulate(items, S, "final", seed=trial) for items, S, trial in _cases(200, 7)) == 1
 
 
 def _fails(design, n=300):
