@@ -49,6 +49,7 @@ constexpr int kQ8tThreads = 12 * 32;  // producer, S issuer, 4 softmax, 4 epilog
 constexpr int kQ8tItemSlots = 4;
 constexpr int kQ8tStages = 5;
 constexpr int kQ8tMaxG = 4;
+constexpr int kQ8tNearTiles = 4;  // an item's tiles still to issue when the next item is claimed
 constexpr int kQ8tTile = kTileTokens * 128;            // codes of one operand (16 KB)
 constexpr int kQ8tScales = kTileTokens * 4;            // row scales of one operand
 constexpr int kQ8tStage = 2 * kQ8tTile + 2 * kQ8tScales;  // K codes, V codes, K scales, V scales
@@ -80,7 +81,7 @@ template <int BS, int G> struct Q8tCfg {
 };
 
 struct Q8tLayout {
-    uint32_t full, empty, ifull, iempty, wfull, sfull, sfree, pfull, afull, ofull, ofree, done, fin, fin2;
+    uint32_t full, empty, ifull, iempty, wfull, pnear, sfull, sfree, pfull, afull, ofull, ofree, done, fin, fin2;
     uint32_t meta, items, witem, tmem, table, qf, fbuf, abuf, qbuf, pbuf, stages, total;
 };
 
@@ -96,6 +97,8 @@ __host__ __device__ inline Q8tLayout q8t_smem_layout(int S) {
     L.iempty = off;
     off += 8 * kQ8tItemSlots;
     L.wfull = off;
+    off += 8 * kQ8tItemSlots;
+    L.pnear = off;
     off += 8 * kQ8tItemSlots;
     L.sfull = off;
     off += 16;
@@ -269,6 +272,7 @@ __device__ inline void q8t_producer(const DecodeParams &p, const CUtensorMap *tm
         prefetch_tensormap(tsv);
     }
     uint64_t *wfull = reinterpret_cast<uint64_t *>(smem + L.wfull);
+    uint64_t *pnear = reinterpret_cast<uint64_t *>(smem + L.pnear);
     const long long *witem = reinterpret_cast<const long long *>(smem + L.witem);
     Q8tScan<BS> scan;
     uint32_t t = 0;
@@ -310,6 +314,8 @@ __device__ inline void q8t_producer(const DecodeParams &p, const CUtensorMap *tm
             it.pad0 = it.pad1 = 0;
             items[slot] = it;
             mbar_arrive(&ifull[slot]);  // the query converter arrives for the operand
+            if (ntiles <= kQ8tNearTiles)
+                mbar_arrive(&pnear[slot]);  // the next item may be claimed
         }
         __syncwarp();
         const int32_t *row = p.block_tables + static_cast<long long>(s) * p.max_blocks_per_seq + blk_lo;
@@ -349,6 +355,8 @@ __device__ inline void q8t_producer(const DecodeParams &p, const CUtensorMap *tm
                 tma_load_3d(st + 2 * kQ8tTile + lane * C::kR * 4, tsk, 0, BS, z, &full[stage], policy);
                 tma_load_3d(st + 2 * kQ8tTile + kQ8tScales + lane * C::kR * 4, tsv, 0, BS, z, &full[stage], policy);
             }
+            if (lane == 0 && ti == ntiles - 1 - kQ8tNearTiles)
+                mbar_arrive(&pnear[slot]);  // the next item may be claimed
             __syncwarp();
         }
         if (!ok)
@@ -380,6 +388,7 @@ __device__ inline bool q8t_qconvert(const DecodeParams &p, char *smem, const Q8t
     char *qbuf = smem + L.qbuf;
     const char *qg = static_cast<const char *>(p.q);
     uint64_t *wfull = reinterpret_cast<uint64_t *>(smem + L.wfull);
+    uint64_t *pnear = reinterpret_cast<uint64_t *>(smem + L.pnear);
     long long *witem = reinterpret_cast<long long *>(smem + L.witem);
     Q8tScan<BS> scan;
     long long w = blockIdx.x;
@@ -391,12 +400,12 @@ __device__ inline bool q8t_qconvert(const DecodeParams &p, char *smem, const Q8t
         // counter (each CTA takes the next unclaimed one when it has room;
         // the counter numbers them from gridDim.x up), else round-robin
         if (p.work && k > 0) {
-            // item k is claimed once the producer took item k - 1 (its record
-            // completes that slot's phase; this warp arrived for it already):
-            // a CTA holds at most one claimed item it has not started, so the
-            // launch's last items go to the CTAs that run out of work first
+            // item k is claimed once the producer has at most kQ8tNearTiles
+            // tiles of item k - 1 left to issue: a CTA never holds a claimed
+            // item it is far from starting, so the launch's last items go to
+            // the CTAs that run out of work first
             const int ps = static_cast<int>((k - 1) % kQ8tItemSlots);
-            if (!mbar_wait_bounded(&ifull[ps], static_cast<uint32_t>(((k - 1) / kQ8tItemSlots) & 1)))
+            if (!mbar_wait_bounded(&pnear[ps], static_cast<uint32_t>(((k - 1) / kQ8tItemSlots) & 1)))
                 return false;
             unsigned int v = 0;
             if (lane == 0)
@@ -932,6 +941,7 @@ __global__ void __launch_bounds__(kQ8tThreads, 1)
         for (int i = 0; i < kQ8tItemSlots; ++i) {
             mbar_init(&ifull[i], 2);  // item record (producer) and query operand (converter)
             mbar_init(reinterpret_cast<uint64_t *>(smem + L.wfull) + i, 1);
+            mbar_init(reinterpret_cast<uint64_t *>(smem + L.pnear) + i, 1);  // producer near the item's end
             mbar_init(&iempty[i], 2 * 4 + 2);  // softmax and epilogue warps, S commit, P V thread
         }
         for (int i = 0; i < 2; ++i) {

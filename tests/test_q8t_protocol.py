@@ -17,9 +17,10 @@ The epilogue of an item's last tile merges the four quarters from the item's
 final softmax state, which the softmax warps leave in slot g & 3; the model
 checks that the slot still holds that tile's state when the merge has read it.
 
-The query converter claims item k only once the producer has taken item
-k - 1, so a CTA holds at most one claimed item it has not started (claimed up
-to four ahead, the launch's last items sat queued behind other items in a few
+The query converter claims item k only once the producer has at most four
+tiles of item k - 1 left to issue, so a CTA holds at most one claimed item it
+has not started, and only near its current item's end (claimed up to four
+items ahead, the launch's last items sat queued behind other items in a few
 CTAs while the rest had none).
 
 Three variants that were tried on the way are kept as negative checks: an
@@ -77,6 +78,8 @@ def simulate(items, S, design="final", seed=0):
     afull = [Bar(f"afull{i}", 4) for i in range(4)]
     ofull = [Bar(f"ofull{i}", 1) for i in range(2)]
     ofree = [Bar(f"ofree{i}", 4) for i in range(2)]
+    NEAR = 4  # tiles of an item still to issue when the next item is claimed
+    pnear = [Bar(f"pnear{i}", 1) for i in range(SL)]
     tc = []      # tensor core queue, in issue order
     copies = []  # copies in flight, any order
     pv_done, epi_done, stage_done = set(), set(), set()
@@ -104,7 +107,9 @@ def simulate(items, S, design="final", seed=0):
             producer_at[0] = k
             if nt is None:
                 return
-            for _ in range(nt):
+            if nt <= NEAR:
+                pnear[slot].arrive()
+            for ti in range(nt):
                 st = t % S
                 if t >= S:
                     yield from wait(empty[st], t // S - 1, "producer empty")
@@ -113,6 +118,8 @@ def simulate(items, S, design="final", seed=0):
                 copies.append(st)
                 t += 1
                 yield "issue"
+                if ti == nt - 1 - NEAR:
+                    pnear[slot].arrive()
 
     def converter():
         for k, nt in enumerate(items + [None]):
@@ -120,8 +127,9 @@ def simulate(items, S, design="final", seed=0):
             if k >= SL:
                 yield from wait(iempty[slot], k // SL - 1, "converter iempty")
             if k > 0 and design != "claim_ahead":
-                # item k is claimed once the producer took item k - 1
-                yield from wait(ifull[(k - 1) % SL], (k - 1) // SL, "converter ifull")
+                # item k is claimed once the producer has at most NEAR tiles of
+                # item k - 1 left to issue
+                yield from wait(pnear[(k - 1) % SL], (k - 1) // SL, "converter pnear")
                 assert producer_at[0] >= k - 1
             claimed[0] = k
             lead[0] = max(lead[0], claimed[0] - producer_at[0])
