@@ -81,26 +81,39 @@ __device__ inline int kv_tile(const DecodeParams &p, int s, int h, int pb) {
 
 // Items of a persistent decode kernel, for its producer warp: from the
 // launch's counter (DecodeParams::work), each claimed one item ahead so the
-// atomic's latency overlaps the current item, or round-robin without one.
+// atomic's latency overlaps the current item (at the current item's start, or
+// later where the kernel calls claim_next), or round-robin without one.
 // Claimed indices only grow, so the producer's forward scan over the contexts
 // still applies; every claimed index below the item count is processed.
 struct ItemClaim {
-    long long w = 0;        // the current item
+    long long w = 0;         // the current item
     unsigned int ahead = 0;  // the next one (lane 0)
+    bool claimed = false;    // `ahead` holds a claim (warp-uniform)
     // the first item is the CTA's own (no round trip before the first copy);
-    // the counter numbers the later ones from gridDim.x up
-    __device__ void start(const DecodeParams &p) {
-        const int lane = threadIdx.x & 31;
+    // the counter numbers the later ones from gridDim.x up.  late: the next
+    // item is claimed by claim_next (or by next, on demand), not at once
+    __device__ void start(const DecodeParams &p, bool late = false) {
         w = blockIdx.x;
-        if (p.work && lane == 0)
-            ahead = gridDim.x + atomicAdd(p.work, 1u);
+        claimed = false;
+        if (!late)
+            claim_next(p);
     }
-    __device__ void next(const DecodeParams &p) {
+    // claim the item after the current one now (once)
+    __device__ void claim_next(const DecodeParams &p) {
         const int lane = threadIdx.x & 31;
-        if (p.work) {
-            w = __shfl_sync(0xffffffffu, ahead, 0);
+        if (p.work && !claimed) {
             if (lane == 0)
                 ahead = gridDim.x + atomicAdd(p.work, 1u);
+            claimed = true;
+        }
+    }
+    __device__ void next(const DecodeParams &p, bool late = false) {
+        if (p.work) {
+            claim_next(p);
+            w = __shfl_sync(0xffffffffu, ahead, 0);
+            claimed = false;
+            if (!late)
+                claim_next(p);
         } else {
             w += gridDim.x;
         }

@@ -54,6 +54,7 @@ constexpr int kQ8fWarps = 4;  // consumer warps = kv heads per item
 constexpr int kQ8fThreads = (kQ8fWarps + 1) * 32;
 constexpr int kQ8fItemSlots = 4;
 constexpr int kQ8fD = 128;
+constexpr int kQ8fNearBlocks = 4;  // blocks of an item still to issue when the next item is claimed
 // INT8 query rows take the int16 grid while max|q| * d <= 16 * sum |q|
 // (largest element at most 16 times the row's mean magnitude)
 constexpr float kQ8fWideRatio = 16.f;
@@ -252,9 +253,12 @@ __device__ inline void q8f_producer(const DecodeParams &p, char *smem, const Q8f
     bool ok = true;
     const int nquads = (p.num_kv_heads + kQ8fWarps - 1) / kQ8fWarps;
 
+    // the next item is claimed when the current one has kQ8fNearBlocks
+    // blocks left to issue: a CTA never holds a claim it is far from
+    // starting, so the launch's last items go to the CTAs that run out first
     ItemClaim claim;
-    claim.start(p);
-    for (;; claim.next(p)) {
+    claim.start(p, true);
+    for (;; claim.next(p, true)) {
         const long long w = claim.w;
         const long long f = w / nquads;
         const int kvh0 = static_cast<int>(w % nquads) * kQ8fWarps;
@@ -315,6 +319,8 @@ __device__ inline void q8f_producer(const DecodeParams &p, char *smem, const Q8f
         }
         __syncwarp();
         for (int j = 0; j < nb; ++j, ++t) {
+            if (j == max(0, nb - kQ8fNearBlocks))
+                claim.claim_next(p);
             if (!mbar_wait_bounded(&empty[pstage], pphase ^ 1u)) {
                 ok = false;
                 break;
