@@ -52,6 +52,7 @@ namespace pa {
 constexpr int kGqaThreads = 7 * 32;
 constexpr int kGqaSmWarps = 4;    // softmax / epilogue warps
 constexpr int kGqaItemSlots = 4;
+constexpr int kGqaNearTiles = 4;  // tiles of an item still to issue when the next item is claimed
 constexpr int kTileTokens = 128;  // MMA M
 constexpr int kTmemCols = 256;    // S[2] (16 cols) at 0..31, O[2][4 quarters] (16 cols) at 32..159
 
@@ -293,8 +294,11 @@ __device__ inline void gqa_producer(const DecodeParams &p, const CUtensorMap *tm
     bool ok = true;
     const long long hkv = p.num_kv_heads;
 
+    // the next item is claimed (and its table slice loaded) when the current
+    // one has kGqaNearTiles tiles left to issue, so the launch's last items go
+    // to the CTAs that run out of work first
     ItemClaim claim;
-    claim.start(p);
+    claim.start(p, true);
     NextItem cur, nxt;
     prepare_item(p, BS, scan, claim.w, hkv, cur);
     for (long long k = 0;; ++k) {
@@ -377,8 +381,8 @@ __device__ inline void gqa_producer(const DecodeParams &p, const CUtensorMap *tm
             if (lane == 0)
                 mbar_arrive(&zfull[stage]);
             __syncwarp();
-            if (ti == 0) {  // the next item, while this one's first copies are in flight
-                claim.next(p);
+            if (ti == max(0, ntiles - kGqaNearTiles)) {  // the next item, while copies are in flight
+                claim.next(p, true);
                 prepare_item(p, BS, scan, claim.w, hkv, nxt);
                 have_next = true;
             }
@@ -386,7 +390,7 @@ __device__ inline void gqa_producer(const DecodeParams &p, const CUtensorMap *tm
         if (!ok)
             break;
         if (!have_next) {
-            claim.next(p);
+            claim.next(p, true);
             prepare_item(p, BS, scan, claim.w, hkv, nxt);
         }
         cur = nxt;

@@ -39,6 +39,7 @@
 namespace pa {
 
 constexpr int kMhaWarps = 4;
+constexpr int kMhaNearBlocks = 8;  // blocks of an item still to issue when the next item is claimed
 constexpr int kMhaThreads = (kMhaWarps + 1) * 32;
 constexpr int kItemSlots = 4;
 
@@ -257,8 +258,10 @@ __device__ inline void mha_producer(const DecodeParams &p, const CUtensorMap *tm
     const long long hkv = p.num_kv_heads;
 
     ItemClaim claim;
-    claim.start(p);
-    for (;; claim.next(p)) {
+    // the next item is claimed when the current one has kMhaNearBlocks blocks
+    // left to issue, so the launch's last items go to the CTAs that run out first
+    claim.start(p, true);
+    for (;; claim.next(p, true)) {
         const long long w = claim.w;
         const long long f = w / hkv;
         const int kvh = static_cast<int>(w % hkv);
@@ -320,6 +323,8 @@ __device__ inline void mha_producer(const DecodeParams &p, const CUtensorMap *tm
             const int j = j0 + w;
             if (j >= nb)
                 break;
+            if (j == max(0, nb - kMhaNearBlocks))
+                claim.claim_next(p);
             const uint32_t c = cw[w]++;
             const int stage = w * S4 + static_cast<int>(c % S4);
             if (!mbar_wait_bounded(&empty[stage], ((c / S4) & 1u) ^ 1u)) {
