@@ -758,13 +758,19 @@ def host_call_times(st, stream, calls=100):
 
 
 def kernel_source_hash() -> str:
+    """A hash of the decode kernels' code (comments and layout dropped), which
+    keys the ncu traffic figures in profiles/ to the code they were taken on."""
     import hashlib
+    import re
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_cache_251_gb300", "csrc")
     for fn in sorted(os.listdir(csrc)):
         if fn.startswith("pa_decode") or fn in ("pa_device.cuh", "pa_api.cu", "pa_quant.cuh"):
-            with open(os.path.join(csrc, fn), "rb") as f:
-                h.update(fn.encode() + f.read())
+            with open(os.path.join(csrc, fn), encoding="utf-8") as f:
+                text = f.read()
+            text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+            text = re.sub(r"//[^\n]*", " ", text)
+            h.update(fn.encode() + " ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 

@@ -376,8 +376,8 @@ __device__ inline void q8t_producer(const DecodeParams &p, const CUtensorMap *tm
 // Query converter (warp 11): for each item, its 4 x G query rows (consecutive
 // in q) as the B operand of S in the item's slot: row (kv head h, query g,
 // term c) = h * 16 + 3 g + c, each query row scaled by a power of two (its
-// score factor goes to qf).  It walks the same items as the producer and runs
-// up to 4 items ahead of the consumers.
+// score factor goes to qf).  It walks the same items as the producer and
+// claims item k once the producer has kQ8tNearTiles tiles of item k - 1 left.
 template <int BS, int G>
 __device__ inline bool q8t_qconvert(const DecodeParams &p, char *smem, const Q8tLayout &L) {
     constexpr int kRows = kQ8tHeads * G;
