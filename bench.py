@@ -757,13 +757,13 @@ def host_call_times(st, stream, calls=100):
     return out
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(csrc: str | None = None) -> str:
     """A hash of the decode kernels' code (comments and layout dropped), which
     keys the ncu traffic figures in profiles/ to the code they were taken on."""
     import hashlib
     import re
     h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "paged_kv_cache_251_gb300", "csrc")
+    csrc = csrc or os.path.join(ROOT, "paged_kv_cache_251_gb300", "csrc")
     for fn in sorted(os.listdir(csrc)):
         if fn.startswith("pa_decode") or fn in ("pa_device.cuh", "pa_api.cu", "pa_quant.cuh"):
             with open(os.path.join(csrc, fn), encoding="utf-8") as f:

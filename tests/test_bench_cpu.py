@@ -114,3 +114,20 @@ def test_oracle_step_tables_match_the_block_manager():
         assert torch.equal(ost.tables, ps.block_tables) and torch.equal(ost.lens, ps.context_lens)
         assert torch.equal(ost.slots, ps.slots) and torch.equal(ost.pairs, ps.pairs)
         assert (ost.pairs.shape[0] > 0) == (100 % bs != 0)
+
+
+def test_kernel_source_hash_ignores_comments_and_layout_but_not_code(tmp_path):
+    """The hash that keys the ncu traffic figures in profiles/ to the kernel
+    sources changes with the code only."""
+    import bench
+    src = tmp_path / "a"
+    src.mkdir()
+    (src / "pa_decode_x.cuh").write_text("// a comment\nint f(int x) {\n    return x + 1;  // add one\n}\n/* block\n comment */\n")
+    (src / "other.cu").write_text("int unrelated;\n")
+    h0 = bench.kernel_source_hash(str(src))
+    (src / "pa_decode_x.cuh").write_text("// another comment\nint f(int x) { return x + 1; }\n")
+    assert bench.kernel_source_hash(str(src)) == h0
+    (src / "other.cu").write_text("int changed_but_not_hashed;\n")
+    assert bench.kernel_source_hash(str(src)) == h0
+    (src / "pa_decode_x.cuh").write_text("int f(int x) { return x + 2; }\n")
+    assert bench.kernel_source_hash(str(src)) != h0
