@@ -392,3 +392,123 @@ def test_decode_quant_full_gqa_batch_is_repeatable(fmt):
                                  threads=8)
     got = runs[0].cpu()[pairs[:, 0].long(), pairs[:, 1].long()]
     compare(got, ref, torch.float16)
+
+
+def _grown_quant_state(fmt, seed):
+    """An 8-bit cache where each sequence gets one new token: its last, partly
+    filled block is copied to a fresh one (copy-on-write), the token is
+    quantised into the copy, and the decode reads the grown contexts.  Kv heads
+    in fours with 16-bit queries, so E4M3 takes the tensor-core kernel."""
+    N, H, hkv, bs, d = 4, 16, 4, 16, 128
+    lens = [700, 1301, 43, 2100]                  # no context ends on a block boundary
+    held = [(L + bs - 1) // bs for L in lens]
+    nb = sum(held) + N + 4
+    M = max(held) + 1
+    perm = wl.permutation(seed, 1, nb).to(torch.int32)
+    tables = torch.full((N, M), -1, dtype=torch.int32)
+    at = 0
+    for s in range(N):
+        tables[s, :held[s]] = perm[at:at + held[s]]
+        at += held[s]
+    last = torch.tensor(held) - 1
+    pairs = torch.stack([tables[torch.arange(N), last].to(torch.int64), perm[at:at + N].to(torch.int64)], 1)
+    tables[torch.arange(N), last] = perm[at:at + N]
+    slots = torch.tensor([int(tables[s, lens[s] // bs]) * bs + lens[s] % bs for s in range(N)], dtype=torch.int64)
+    pools = _filled_pages(nb, hkv, bs, d, fmt, seed)
+    kn = wl.normal_tensor(seed, 5, (N, hkv, d), dtype=torch.bfloat16)
+    vn = wl.normal_tensor(seed, 6, (N, hkv, d), dtype=torch.bfloat16)
+    q = wl.normal_tensor(seed, 7, (N, H, d), dtype=torch.bfloat16)
+    return q, pools, kn, vn, pairs, slots, tables, torch.tensor(lens, dtype=torch.int32) + 1, hkv
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_quant_cache_step_captured_in_one_graph(fmt):
+    """Block copy, quantise-on-append and decode of an 8-bit cache captured in
+    one CUDA graph (every library kernel a programmatic dependent launch, the
+    decode claiming items and merging partitions): each replay gives the eager
+    step's pages and output bit for bit, and the eager step matches the oracle."""
+    from paged_kv_cache_251_gb300 import pa
+    q, pools, kn, vn, pairs, slots, tables, lens1, hkv = _grown_quant_state(fmt, seed=53)
+    dev = {n: t.cuda() for n, t in dict(q=q, kn=kn, vn=vn, pairs=pairs, slots=slots, bt=tables, cl=lens1).items()}
+    kp, vp = [t.cuda() for t in pools]
+    out = torch.empty(q.shape, dtype=torch.float32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ws = pa.workspace_for(dev["q"], 16, tables.shape[1], 0, 0)
+
+    def step():
+        pa.pa_copy_blocks_quant(dev["pairs"], kp, vp, err_word=err)
+        pa.pa_append_kv_quant(dev["kn"], dev["vn"], dev["slots"], kp, vp, err_word=err)
+        pa.pa_decode_quant(out, dev["q"], kp, vp, dev["bt"], dev["cl"], num_kv_heads=hkv,
+                           scale=1.0 / math.sqrt(128), workspace=ws, err_word=err)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    eager = (out.clone(), kp.clone(), vp.clone())
+
+    want = [t.clone() for t in pools]
+    oracle.copy_blocks(want[0], want[1], pairs)
+    oracle.append_kv_quant(want[0], want[1], kn, vn, slots)
+    _assert_pools_equal([eager[1].cpu(), eager[2].cpu()], want)
+    ref = oracle.paged_attention(q, want[0], want[1], tables, lens1, num_kv_heads=hkv, scale=1.0 / math.sqrt(128),
+                                 threads=8)
+    compare(eager[0].cpu(), ref, torch.bfloat16)
+
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    for _ in range(10):
+        out.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out, eager[0])
+        assert torch.equal(_u8(kp), _u8(eager[1])) and torch.equal(_u8(vp), _u8(eager[2]))
+    assert int(err.item()) == 0
+
+
+def test_quant_concurrent_launches_on_two_streams():
+    """INT8 and E4M3 decodes of GQA-shaped batches (the CUDA-core and the
+    tensor-core 8-bit kernels, each claiming items from a counter) launched ten
+    times each on two streams with no synchronisation in between: each keeps its
+    single-stream result bit for bit."""
+    from paged_kv_cache_251_gb300 import pa
+    lens = [(37 * i * i + 300 * i) % 2100 + 1 for i in range(128)]
+    cases = []
+    for fmt, seed in (("int8", 61), ("e4m3", 67)):
+        inp, pools = _quant_case("streams_" + fmt, 128, 32, 8, 128, 16, lens, 0, torch.bfloat16, fmt, seed=seed)
+        q = inp.q.cuda()
+        kp, vp = [t.cuda() for t in pools]
+        bt, cl = inp.block_tables.cuda(), inp.context_lens.cuda()
+        out = torch.empty(q.shape, dtype=torch.float32, device="cuda")
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        ws = pa.workspace_for(q, 16, bt.shape[1])
+        cases.append((inp, pools, q, kp, vp, bt, cl, out, err, ws, torch.cuda.Stream()))
+
+    def call(c):
+        inp, pools, q, kp, vp, bt, cl, out, err, ws, st = c
+        pa.pa_decode_quant(out, q, kp, vp, bt, cl, num_kv_heads=8, scale=1.0 / math.sqrt(128), workspace=ws,
+                           err_word=err, stream=st)
+
+    alone = []
+    for c in cases:
+        call(c)
+        torch.cuda.synchronize()
+        alone.append(c[7].clone())
+    for c in cases:
+        c[10].wait_stream(torch.cuda.current_stream())
+    for _ in range(10):
+        for c in cases:
+            call(c)
+    torch.cuda.synchronize()
+    for c, ref in zip(cases, alone):
+        assert int(c[8].item()) == 0
+        assert torch.equal(c[7], ref)
+    inp, pools = cases[1][0], cases[1][1]
+    pairs = torch.tensor([[s, h] for s in range(0, 128, 17) for h in (0, 13, 31)], dtype=torch.int32)
+    ref = _oracle_decode_quant(inp, pools, pairs=pairs)
+    got = cases[1][7].cpu()[pairs[:, 0].long(), pairs[:, 1].long()]
+    compare(got, ref, torch.bfloat16)
