@@ -87,3 +87,47 @@ def test_prefix_workload_full_size():
                                  st.context_lens, num_kv_heads=s.num_kv_heads, scale=1 / math.sqrt(s.head_dim),
                                  pairs=pairs, threads=16)
     compare(out.cpu()[pairs[:, 0].long(), pairs[:, 1].long()], ref, s.dtype)
+
+
+@pytest.mark.parametrize("H,hkv", [(8, 8), (8, 4)])
+def test_shared_prefix_replayed_from_a_cuda_graph(H, hkv):
+    """The shared-prefix call (its four kernels: prep, prefix pass, suffix pass,
+    combine) captured in a CUDA graph and replayed: every replay gives the eager
+    call's output bit for bit, which matches the oracle."""
+    from paged_kv_cache_251_gb300 import pa
+    prompts, samples, bs = 3, 4, 16
+    N = prompts * samples
+    plens = [1500, 40, 700]
+    extra = wl.randint(17, 1, N, 1, 300).tolist()
+    tables, lens, k, v = make_groups(prompts, samples, plens, extra, bs, hkv, 128, torch.bfloat16, seed=41 + hkv)
+    q = wl.normal_tensor(19, 3, (N, H, 128), dtype=torch.bfloat16)
+    shared = torch.tensor([pl // bs * bs for pl in plens], dtype=torch.int32)
+    dev = [t.cuda() for t in (q, k, v, tables, lens)]
+    sh = shared.cuda()
+    out = torch.empty((N, H, 128), device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    n = pa.pa_decode_shared_prefix_workspace_size(N, H, 128, bs, tables.shape[1], 0, samples, torch.bfloat16)
+    ws = torch.empty(max(n, 16), dtype=torch.uint8, device="cuda")
+
+    def call():
+        pa.pa_decode_shared_prefix(out, *dev, sh, samples, num_kv_heads=hkv, workspace=ws, err_word=err)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        call()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    eager = out.clone()
+    ref = oracle.paged_attention(q, k, v, tables, lens, num_kv_heads=hkv, scale=1 / math.sqrt(128), threads=8)
+    compare(eager.cpu(), ref, torch.bfloat16)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        call()
+    for _ in range(8):
+        out.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out, eager)
+    assert err.item() == 0
