@@ -80,23 +80,22 @@ __device__ inline int kv_tile(const DecodeParams &p, int s, int h, int pb) {
 }
 
 // Items of a persistent decode kernel, for its producer warp: from the
-// launch's counter (DecodeParams::work), each claimed one item ahead so the
-// atomic's latency overlaps the current item (at the current item's start, or
-// later where the kernel calls claim_next), or round-robin without one.
-// Claimed indices only grow, so the producer's forward scan over the contexts
-// still applies; every claimed index below the item count is processed.
+// launch's counter (DecodeParams::work), or round-robin without one.  A CTA's
+// first item is its own (no round trip before the first copy); the counter
+// numbers the later ones from gridDim.x up.  The kernel claims the item after
+// the current one with claim_next when the current one has a few copies left
+// to issue (next claims it on demand otherwise): a claim taken earlier would
+// sit unstarted, and at the end of a launch the CTAs holding one would finish
+// an item's time after the rest.  Claimed indices only grow, so the producer's
+// forward scan over the contexts still applies; every claimed index below the
+// item count is processed.
 struct ItemClaim {
     long long w = 0;         // the current item
     unsigned int ahead = 0;  // the next one (lane 0)
     bool claimed = false;    // `ahead` holds a claim (warp-uniform)
-    // the first item is the CTA's own (no round trip before the first copy);
-    // the counter numbers the later ones from gridDim.x up.  late: the next
-    // item is claimed by claim_next (or by next, on demand), not at once
-    __device__ void start(const DecodeParams &p, bool late = false) {
+    __device__ void start() {
         w = blockIdx.x;
         claimed = false;
-        if (!late)
-            claim_next(p);
     }
     // claim the item after the current one now (once)
     __device__ void claim_next(const DecodeParams &p) {
@@ -107,13 +106,11 @@ struct ItemClaim {
             claimed = true;
         }
     }
-    __device__ void next(const DecodeParams &p, bool late = false) {
+    __device__ void next(const DecodeParams &p) {
         if (p.work) {
             claim_next(p);
             w = __shfl_sync(0xffffffffu, ahead, 0);
             claimed = false;
-            if (!late)
-                claim_next(p);
         } else {
             w += gridDim.x;
         }

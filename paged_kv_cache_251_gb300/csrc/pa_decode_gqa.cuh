@@ -298,7 +298,7 @@ __device__ inline void gqa_producer(const DecodeParams &p, const CUtensorMap *tm
     // one has kGqaNearTiles tiles left to issue, so the launch's last items go
     // to the CTAs that run out of work first
     ItemClaim claim;
-    claim.start(p, true);
+    claim.start();
     NextItem cur, nxt;
     prepare_item(p, BS, scan, claim.w, hkv, cur);
     for (long long k = 0;; ++k) {
@@ -382,7 +382,7 @@ __device__ inline void gqa_producer(const DecodeParams &p, const CUtensorMap *tm
                 mbar_arrive(&zfull[stage]);
             __syncwarp();
             if (ti == max(0, ntiles - kGqaNearTiles)) {  // the next item, while copies are in flight
-                claim.next(p, true);
+                claim.next(p);
                 prepare_item(p, BS, scan, claim.w, hkv, nxt);
                 have_next = true;
             }
@@ -390,7 +390,7 @@ __device__ inline void gqa_producer(const DecodeParams &p, const CUtensorMap *tm
         if (!ok)
             break;
         if (!have_next) {
-            claim.next(p, true);
+            claim.next(p);
             prepare_item(p, BS, scan, claim.w, hkv, nxt);
         }
         cur = nxt;

@@ -260,8 +260,8 @@ __device__ inline void mha_producer(const DecodeParams &p, const CUtensorMap *tm
     ItemClaim claim;
     // the next item is claimed when the current one has kMhaNearBlocks blocks
     // left to issue, so the launch's last items go to the CTAs that run out first
-    claim.start(p, true);
-    for (;; claim.next(p, true)) {
+    claim.start();
+    for (;; claim.next(p)) {
         const long long w = claim.w;
         const long long f = w / hkv;
         const int kvh = static_cast<int>(w % hkv);

@@ -257,8 +257,8 @@ __device__ inline void q8f_producer(const DecodeParams &p, char *smem, const Q8f
     // blocks left to issue: a CTA never holds a claim it is far from
     // starting, so the launch's last items go to the CTAs that run out first
     ItemClaim claim;
-    claim.start(p, true);
-    for (;; claim.next(p, true)) {
+    claim.start();
+    for (;; claim.next(p)) {
         const long long w = claim.w;
         const long long f = w / nquads;
         const int kvh0 = static_cast<int>(w % nquads) * kQ8fWarps;
