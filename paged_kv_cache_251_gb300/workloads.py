@@ -304,13 +304,6 @@ def quant_pools(inp: DecodeInputs, fmt: str, device="cpu"):
     return kp, vp
 
 
-def window_ring_blocks(shape: Shape, ring_len: int) -> torch.Tensor:
-    """Physical block ids for each sequence's ring: int64 [N, ring_len], a
-    seeded shuffle of the pool."""
-    perm = permutation(shape.seed, _S_PERM, shape.num_seqs * ring_len)
-    return perm.reshape(shape.num_seqs, ring_len)
-
-
 def prefix_draws(seed: int, num_samples: int, lo: int = 1, hi: int = 256) -> torch.Tensor:
     """Divergent-token counts per sample, uniform in [lo, hi]."""
     return randint(seed, _S_NEW, num_samples, lo, hi)
