@@ -58,8 +58,6 @@ template <typename T, int D, int BS> struct MhaCfg {
     static constexpr int kElt = sizeof(T);
     static constexpr int kRow = D * kElt;              // bytes per token row
     static constexpr int kBoxes = kRow / 128;          // 128-byte swizzle boxes per row
-    static constexpr int kBoxElems = 128 / kElt;       // elements per box row
-    static constexpr int kBoxBytes = BS * 128;         // one box of one (block, head) tile
     static constexpr int kTile = BS * kRow;
     static constexpr int kTpr = BS < 16 ? BS : 16;     // tokens per QK round
     static constexpr int kRounds = BS / kTpr;

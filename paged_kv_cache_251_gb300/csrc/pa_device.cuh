@@ -108,33 +108,6 @@ __device__ inline bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
-// try_wait with a suspend-time hint (ns): returns once the phase completes or
-// about that long has passed, without spinning on the issue slots.
-__device__ inline bool mbar_try_wait_for(uint64_t *bar, uint32_t parity, uint32_t ns) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_addr(bar)), "r"(parity), "r"(ns)
-        : "memory");
-    return ok != 0;
-}
-
-// Non-blocking test of a phase: true iff the phase with this parity completed.
-__device__ inline bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_addr(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
 // A wait that gives up: every wait in these kernels ends, either because the
 // phase completed or because about kTimeoutNs passed (the caller then flags
 // PA_DEVERR_TIMEOUT and winds down).
