@@ -292,3 +292,64 @@ def test_full_opt13b_batch_is_repeatable():
         got, err = run_decode(inp)
         assert err == 0
         assert torch.equal(got, first)
+
+
+def test_decode_from_several_host_threads():
+    """The library is called from four host threads at once, each on its own
+    stream with its own workload (MHA and tensor-core decodes, an append, an
+    8-bit decode): ctypes releases the GIL, so the calls really overlap on the
+    host (per-thread tensor-map caches, the shared device facts and counter
+    pool).  Every thread's results equal the single-threaded ones bit for bit."""
+    import threading
+    from paged_kv_cache_251_gb300 import pa
+    lens = [(53 * i * i + 211 * i) % 1900 + 1 for i in range(32)]
+    jobs = []
+    for hkv, seed in ((8, 71), (32, 73), (4, 79)):
+        inp = make_inputs(shape("threads", 32, 32, hkv, 128, 16, torch.bfloat16, seed=seed), lens)
+        dev = to_cuda(inp)
+        out = torch.empty(dev["q"].shape, dtype=torch.float32, device="cuda")
+        ws = pa.workspace_for(dev["q"], 16, dev["block_tables"].shape[1])
+        jobs.append(("decode", inp, dev, out, ws, hkv))
+    qinp = make_inputs(shape("threads_q", 32, 32, 8, 128, 16, torch.bfloat16, seed=83), lens)
+    kq, vq = [t.cuda() for t in wl.quant_pools(qinp, "e4m3")]
+    qdev = to_cuda(qinp)
+    qout = torch.empty(qdev["q"].shape, dtype=torch.float32, device="cuda")
+    qws = pa.workspace_for(qdev["q"], 16, qdev["block_tables"].shape[1])
+
+    def run(job, stream, reps):
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        for _ in range(reps):
+            if job[0] == "decode":
+                _, inp, dev, out, ws, hkv = job
+                pa.pa_decode(out, dev["q"], dev["k_cache"], dev["v_cache"], dev["block_tables"], dev["context_lens"],
+                             num_kv_heads=hkv, workspace=ws, err_word=err, stream=stream)
+            else:
+                pa.pa_decode_quant(qout, qdev["q"], kq, vq, qdev["block_tables"], qdev["context_lens"],
+                                   num_kv_heads=8, workspace=qws, err_word=err, stream=stream)
+        stream.synchronize()
+        return int(err.item())
+
+    all_jobs = jobs + [("quant",)]
+    streams = [torch.cuda.Stream() for _ in all_jobs]
+    for st in streams:
+        st.wait_stream(torch.cuda.current_stream())
+    alone = []
+    for job, st in zip(all_jobs, streams):
+        assert run(job, st, 1) == 0
+        alone.append((job[3] if job[0] == "decode" else qout).clone())
+    errs = [None] * len(all_jobs)
+
+    def worker(i):
+        errs[i] = run(all_jobs[i], streams[i], 25)
+
+    threads = [threading.Thread(target=worker, args=(i,)) for i in range(len(all_jobs))]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    torch.cuda.synchronize()
+    assert errs == [0] * len(all_jobs)
+    for job, ref in zip(all_jobs, alone):
+        got = job[3] if job[0] == "decode" else qout
+        assert torch.equal(got, ref)
+    compare(jobs[0][3].cpu(), oracle_decode(jobs[0][1]), torch.bfloat16)
